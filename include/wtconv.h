@@ -1,0 +1,135 @@
+/*
+ * wtconv.h -- C ABI of the GB300 WTConv2d library (libwtconv.so).
+ *
+ * The layer is the wavelet convolution of "Fast and Memory-Efficient Wavelet
+ * Convolutions via I/O-Aware Reformulation" (Aflalo, Finder, Amoyal,
+ * Treister, Freifeld; arXiv 2608.10805).  Its technical summary on
+ * gist.science ("Problem statement", "Methodology") describes it as a
+ * drop-in replacement for a depthwise convolution built from: a multi-level
+ * 2D Haar analysis; a depthwise k x k convolution of every subband at every
+ * level; learned per-channel scales; the L-step synthesis cascade that adds
+ * each level's reconstruction to the next finer low-pass band; and a base
+ * depthwise convolution with bias, also scaled per channel.  For channel c:
+ *
+ *   y = s_base[c] * (conv(x, W_base[c]) + b[c]) + sum_l F_l^T Z^l,
+ *   Z^l_b = s_w[l,4c+b] * conv(Y^l_b, W_sub[l,4c+b]),   Y^l = F_l x,
+ *
+ * where F_l is the level-l Haar analysis (orthonormal taps +-1/2; the
+ * unconvolved low-pass band feeds the next level; odd sizes are zero-padded
+ * on the bottom/right and cropped after synthesis).  Convolutions are
+ * stride-1 cross-correlations with zero "same" padding and odd k.  Bands:
+ * b = 0 low-pass, 1 row-high (sign (-1)^row), 2 column-high (sign
+ * (-1)^column), 3 diagonal; subband channel index 4c+b.
+ *
+ * The library computes each call on the GPU in one pass over the activations
+ * (the pages' "Methodology": the Haar butterflies are recomputed on chip, the
+ * synthesis is collapsed into one pass indexed by output-coordinate bits, the
+ * scales are folded into the weights).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates device memory; calls that need scratch take a
+ *     caller-provided workspace (size from wtconv_workspace_size).
+ *   - Activations x, y, dy, dx are NCHW, contiguous, in desc->dtype.
+ *     Parameters and parameter gradients are float32, contiguous:
+ *     w_base[C,k,k], b_base[C], w_sub[L,4C,k,k], base_scale[C],
+ *     wavelet_scale[L,4C].  Gradients are overwritten, not accumulated.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: no call synchronises the host.
+ *   - Arithmetic is float32 (float16/bfloat16 activations are widened on
+ *     load and rounded to nearest-even on store).  Results match a float64
+ *     evaluation of the unfused layer up to evaluation order.
+ *   - Errors: a call validates every argument before it enqueues anything.
+ *     On a bad argument it returns an error code and launches nothing.  On a
+ *     CUDA launch error it returns WTCONV_ERR_CUDA.  wtconv_last_error()
+ *     returns a thread-local message describing the last failure.
+ *   - Limits: 3 <= k <= 9, k odd; 1 <= levels <= 8; N >= 0; C, H, W >= 1;
+ *     every plane (with its on-chip pyramid) must fit in one SM's shared
+ *     memory (about H, W <= 128 for the forward calls and H, W <= 88 for the
+ *     parameter-gradient call; larger planes return WTCONV_ERR_UNSUPPORTED).
+ *     N = 0 is a valid empty batch.
+ *   - Pointers must be aligned to their element size (WTCONV_ERR_MISALIGNED
+ *     otherwise); 16-byte alignment enables vector loads and stores.
+ */
+#ifndef WTCONV_H_
+#define WTCONV_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WTCONV_OK = 0,
+  WTCONV_ERR_INVALID_ARG = 1,  /* null pointer, bad size, even k, ...           */
+  WTCONV_ERR_UNSUPPORTED = 2,  /* valid layer, but outside this build's limits  */
+  WTCONV_ERR_MISALIGNED = 3,   /* pointer not aligned to its element size       */
+  WTCONV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required    */
+  WTCONV_ERR_CUDA = 5          /* a CUDA runtime call or launch failed          */
+} wtconv_status_t;
+
+typedef enum { WTCONV_F32 = 0, WTCONV_F16 = 1, WTCONV_BF16 = 2 } wtconv_dtype_t;
+
+typedef enum {
+  WTCONV_OP_FWD = 0,
+  WTCONV_OP_BWD_DATA = 1,
+  WTCONV_OP_BWD_WEIGHT = 2
+} wtconv_op_t;
+
+/* Layer geometry.  All fields are plain ints so the layout is fixed. */
+typedef struct {
+  int N, C, H, W;  /* activation shape, NCHW                                 */
+  int levels;      /* L, number of wavelet decomposition levels             */
+  int k;           /* kernel size of every depthwise convolution (odd)      */
+  int dtype;       /* wtconv_dtype_t of x / y / dy / dx                     */
+} wtconv_desc_t;
+
+/* Bytes of device workspace `op` needs for `desc` (0 if none, or if desc is
+ * invalid).  The workspace must be 256-byte aligned; its contents need not
+ * be initialised and are garbage after the call. */
+size_t wtconv_workspace_size(const wtconv_desc_t* desc, int op);
+
+/* Forward: y = WTConv2d(x).  b_base may be NULL (no bias).
+ * Defined by the technical summary's "Methodology" (fused analysis +
+ * depthwise conv, collapsed synthesis, folded scales) and "Problem
+ * statement" (drop-in for a depthwise conv).  Needs no workspace (ws may be
+ * NULL, ws_bytes 0). */
+wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float* w_base,
+                           const float* b_base, const float* w_sub, const float* base_scale,
+                           const float* wavelet_scale, void* y, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Input gradient: dx = A^T dy, where A is the (linear) layer map without the
+ * bias.  The summary's "Key contributions" report that the fused
+ * implementation reproduces all gradients.  Because the Haar pair is
+ * orthonormal and k is odd, A^T is the same fused pass with every kernel
+ * rotated by 180 degrees, which is how it is computed.  Needs no workspace. */
+wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const float* w_base,
+                                const float* w_sub, const float* base_scale,
+                                const float* wavelet_scale, void* dx, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/* Parameter gradients for upstream gradient dy at input x:
+ *   dw_base[C,k,k], db_base[C] (may be NULL), dw_sub[L,4C,k,k],
+ *   dbase_scale[C], dwavelet_scale[L,4C]   (float32, overwritten).
+ * b_base (may be NULL) enters dbase_scale.  Partial correlation sums are
+ * reduced in a deterministic order through the workspace, which must hold
+ * wtconv_workspace_size(desc, WTCONV_OP_BWD_WEIGHT) bytes. */
+wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, const void* dy,
+                                  const float* w_base, const float* b_base, const float* w_sub,
+                                  const float* base_scale, const float* wavelet_scale,
+                                  float* dw_base, float* db_base, float* dw_sub, float* dbase_scale,
+                                  float* dwavelet_scale, void* ws, size_t ws_bytes, void* stream);
+
+/* Static name of a status code. */
+const char* wtconv_status_string(wtconv_status_t status);
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char* wtconv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WTCONV_H_ */

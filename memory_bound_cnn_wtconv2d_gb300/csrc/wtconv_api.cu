@@ -1,0 +1,312 @@
+// C ABI of libwtconv: argument validation, launch planning, dispatch.
+// The declarations and the contract of every entry point are in
+// include/wtconv.h.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/wtconv.h"
+#include "wtconv_launch.h"
+#include "wtconv_plan.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+wtconv_status_t fail(wtconv_status_t st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+wtconv_status_t fail(wtconv_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+wtconv_status_t ok() {
+  g_last_error[0] = '\0';
+  return WTCONV_OK;
+}
+
+constexpr int kMaxSmemPerBlock = 232448;  // 227 KiB opt-in shared memory per CTA on sm_103
+constexpr int kSmemPerSm = 233472;        // 228 KiB shared memory per SM
+constexpr int kNumSms = 152;              // GB300; only a grid-shaping heuristic
+constexpr int kFwdBudget = 72 * 1024;     // preferred forward CTA footprint (>= 3 CTAs / SM)
+constexpr int kBwBudget = 112 * 1024;     // preferred gradient CTA footprint (>= 2 CTAs / SM)
+
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+size_t elem_size(int dtype) { return dtype == WTCONV_F32 ? 4 : 2; }
+
+wtconv_status_t validate_desc(const wtconv_desc_t* d) {
+  if (!d) return fail(WTCONV_ERR_INVALID_ARG, "desc is NULL");
+  if (d->N < 0 || d->C < 1 || d->H < 1 || d->W < 1)
+    return fail(WTCONV_ERR_INVALID_ARG, "bad shape N=%d C=%d H=%d W=%d", d->N, d->C, d->H, d->W);
+  if (d->levels < 1 || d->levels > WT_MAXL)
+    return fail(WTCONV_ERR_INVALID_ARG, "levels=%d outside [1, %d]", d->levels, WT_MAXL);
+  if (d->k < 3 || d->k > 9 || (d->k % 2) == 0)
+    return fail(WTCONV_ERR_INVALID_ARG, "k=%d: must be odd and in [3, 9]", d->k);
+  if (d->dtype != WTCONV_F32 && d->dtype != WTCONV_F16 && d->dtype != WTCONV_BF16)
+    return fail(WTCONV_ERR_INVALID_ARG, "dtype=%d unknown", d->dtype);
+  if ((int64_t)d->N * d->C > INT32_MAX / 2 || (int64_t)d->H * d->W > (1 << 24))
+    return fail(WTCONV_ERR_UNSUPPORTED, "shape too large for 32-bit plane indexing");
+  return WTCONV_OK;
+}
+
+void level_sizes(const wtconv_desc_t* d, int* Hs, int* Ws) {
+  Hs[0] = d->H;
+  Ws[0] = d->W;
+  for (int l = 1; l <= d->levels; ++l) {
+    Hs[l] = (Hs[l - 1] + 1) / 2;
+    Ws[l] = (Ws[l - 1] + 1) / 2;
+  }
+}
+
+// Places a padded plane buffer of `nb` bands at `off`; returns the next offset.
+int place(WtBuf& b, int off, int er, int ec, int pad, int nb) {
+  b.off = off;
+  b.pad = pad;
+  b.stride = round_up(ec + 2 * pad, 4);
+  b.band = (er + 2 * pad) * b.stride;
+  return off + nb * b.band;
+}
+
+wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
+  memset(&pl, 0, sizeof(pl));
+  pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
+  const int R = d->k / 2, L = d->levels, KK = d->k * d->k;
+  level_sizes(d, pl.Hs, pl.Ws);
+  int er[WT_MAXL + 1], ec[WT_MAXL + 1];
+  for (int l = 1; l <= L; ++l) {
+    pl.tr[l] = ceil_div(pl.Hs[l], WT_TP);
+    pl.tc[l] = ceil_div(pl.Ws[l], WT_TQ);
+    er[l] = pl.tr[l] * WT_TP;
+    ec[l] = pl.tc[l] * WT_TQ;
+  }
+  er[0] = 2 * er[1];
+  ec[0] = 2 * ec[1];
+  int off = 0;
+  off = place(pl.lev[0], off, er[0], ec[0], R, 1);
+  for (int l = 1; l <= L; ++l) off = place(pl.lev[l], off, er[l], ec[l], R, 4);
+  for (int l = 1; l < L; ++l) off = place(pl.syn[l], off, er[l], ec[l], 0, 1);
+  pl.plane_floats = round_up(off, 4);
+  pl.w_band = round_up(KK, 4);
+  const int wfloats = (1 + 4 * L) * pl.w_band;
+  const long plane_bytes = 4L * pl.plane_floats;
+  if (plane_bytes + 4L * wfloats > kMaxSmemPerBlock)
+    return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %ld B of shared memory (max %d)",
+                d->H, d->W, L, plane_bytes + 4L * wfloats, kMaxSmemPerBlock);
+  const int items = pl.tr[1] * pl.tc[1];
+  int P = ceil_div(WT_FWD_THREADS, items);
+  P = P < 1 ? 1 : P;
+  const int fit = (int)((kFwdBudget - 4L * wfloats) / plane_bytes);
+  if (P > fit) P = fit < 1 ? 1 : fit;
+  if (d->N > 0 && P > d->N) P = d->N;
+  pl.P = P;
+  pl.groups = d->N > 0 ? ceil_div(d->N, P) : 0;
+  pl.w_off = P * pl.plane_floats;
+  pl.smem_bytes = 4 * (P * pl.plane_floats + wfloats);
+  return WTCONV_OK;
+}
+
+wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
+  memset(&pl, 0, sizeof(pl));
+  pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
+  const int R = d->k / 2, L = d->levels, KK = d->k * d->k;
+  level_sizes(d, pl.Hs, pl.Ws);
+  int off = 0;
+  pl.item_begin[0] = 0;
+  for (int l = 0; l <= L; ++l) {
+    pl.tr[l] = ceil_div(pl.Hs[l], WT_BT);
+    pl.tc[l] = ceil_div(pl.Ws[l], WT_BT);
+    const int nb = l == 0 ? 1 : 4;
+    off = place(pl.xs[l], off, pl.tr[l] * WT_BT, pl.tc[l] * WT_BT, R, nb);
+    off = place(pl.ds[l], off, pl.tr[l] * WT_BT, pl.tc[l] * WT_BT, 0, nb);
+    pl.item_begin[l + 1] = pl.item_begin[l] + nb * pl.tr[l] * pl.tc[l];
+  }
+  pl.items_per_plane = pl.item_begin[L + 1];
+  pl.plane_floats = round_up(off, 4);
+  pl.nbands = 1 + 4 * L;
+  pl.part_stride = pl.nbands * (KK + 1);
+  const int slots = WT_BW_MAX_ITEMS * WT_BW_THREADS;
+  if (pl.items_per_plane > slots)
+    return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d has %d gradient tiles (max %d per CTA)", d->H, d->W,
+                pl.items_per_plane, slots);
+  const long plane_bytes = 4L * pl.plane_floats;
+  int P = slots / pl.items_per_plane;
+  const int fit = (int)(kBwBudget / plane_bytes);
+  if (P > fit) P = fit < 1 ? 1 : fit;
+  if (d->N > 0 && P > d->N) P = d->N;
+  if (P < 1) P = 1;
+  pl.P = P;
+  long smem = plane_bytes * P;
+  const long red = 4L * P * pl.items_per_plane * (KK + 1);
+  if (red > smem) smem = red;
+  if (smem > kMaxSmemPerBlock)
+    return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %ld B of shared memory (max %d)",
+                d->H, d->W, L, smem, kMaxSmemPerBlock);
+  pl.smem_bytes = (int)smem;
+  // One wave of (channel, chunk) CTAs when the channels allow it.
+  const int per_sm = (int)(kSmemPerSm / (smem + 1024));
+  const int ctas = kNumSms * (per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm));
+  const int batches = d->N > 0 ? ceil_div(d->N, P) : 0;
+  int groups = ctas / d->C;
+  if (groups < 1) groups = 1;
+  if (groups > batches) groups = batches;
+  if (batches > 0) {
+    pl.chunk = ceil_div(batches, groups) * P;
+    pl.groups = ceil_div(d->N, pl.chunk);
+  }
+  return WTCONV_OK;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+wtconv_status_t check_act(const void* p, const char* name, const wtconv_desc_t* d) {
+  if (!p) return fail(WTCONV_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned(p, elem_size(d->dtype)))
+    return fail(WTCONV_ERR_MISALIGNED, "%s is not aligned to its element size", name);
+  return WTCONV_OK;
+}
+
+wtconv_status_t check_param(const void* p, const char* name, bool nullable) {
+  if (!p) return nullable ? WTCONV_OK : fail(WTCONV_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned(p, 4)) return fail(WTCONV_ERR_MISALIGNED, "%s is not 4-byte aligned", name);
+  return WTCONV_OK;
+}
+
+int vec_ok(const wtconv_desc_t* d, const void* a, const void* b) {
+  const int v = (int)(16 / elem_size(d->dtype));
+  return (d->W % v == 0) && aligned(a, 16) && (b == nullptr || aligned(b, 16));
+}
+
+size_t bw_workspace_bytes(const WtBwPlan& pl) {
+  const size_t bytes = (size_t)pl.groups * pl.C * pl.part_stride * sizeof(float);
+  return (bytes + 255) / 256 * 256;
+}
+
+#define WT_TRY(expr)                  \
+  do {                                \
+    wtconv_status_t st_ = (expr);     \
+    if (st_ != WTCONV_OK) return st_; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+size_t wtconv_workspace_size(const wtconv_desc_t* desc, int op) {
+  if (validate_desc(desc) != WTCONV_OK) return 0;
+  if (op != WTCONV_OP_BWD_WEIGHT) return 0;
+  WtBwPlan pl;
+  if (plan_bw(desc, pl) != WTCONV_OK) return 0;
+  return bw_workspace_bytes(pl);
+}
+
+wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float* w_base,
+                           const float* b_base, const float* w_sub, const float* base_scale,
+                           const float* wavelet_scale, void* y, void* ws, size_t ws_bytes,
+                           void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  WT_TRY(validate_desc(desc));
+  WT_TRY(check_param(w_base, "w_base", false));
+  WT_TRY(check_param(b_base, "b_base", true));
+  WT_TRY(check_param(w_sub, "w_sub", false));
+  WT_TRY(check_param(base_scale, "base_scale", false));
+  WT_TRY(check_param(wavelet_scale, "wavelet_scale", false));
+  WtFwdPlan pl;
+  WT_TRY(plan_fwd(desc, pl));
+  if (desc->N == 0) return ok();
+  WT_TRY(check_act(x, "x", desc));
+  WT_TRY(check_act(y, "y", desc));
+  pl.vec_ok = vec_ok(desc, x, y);
+  cudaError_t e = wt::launch_fwd(pl, desc->dtype, false, x, w_base, b_base, w_sub, base_scale,
+                                 wavelet_scale, y, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_fwd: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const float* w_base,
+                                const float* w_sub, const float* base_scale,
+                                const float* wavelet_scale, void* dx, void* ws, size_t ws_bytes,
+                                void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  WT_TRY(validate_desc(desc));
+  WT_TRY(check_param(w_base, "w_base", false));
+  WT_TRY(check_param(w_sub, "w_sub", false));
+  WT_TRY(check_param(base_scale, "base_scale", false));
+  WT_TRY(check_param(wavelet_scale, "wavelet_scale", false));
+  WtFwdPlan pl;
+  WT_TRY(plan_fwd(desc, pl));
+  if (desc->N == 0) return ok();
+  WT_TRY(check_act(dy, "dy", desc));
+  WT_TRY(check_act(dx, "dx", desc));
+  pl.vec_ok = vec_ok(desc, dy, dx);
+  cudaError_t e = wt::launch_fwd(pl, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale,
+                                 wavelet_scale, dx, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_data: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, const void* dy,
+                                  const float* w_base, const float* b_base, const float* w_sub,
+                                  const float* base_scale, const float* wavelet_scale,
+                                  float* dw_base, float* db_base, float* dw_sub, float* dbase_scale,
+                                  float* dwavelet_scale, void* ws, size_t ws_bytes, void* stream) {
+  WT_TRY(validate_desc(desc));
+  WT_TRY(check_param(w_base, "w_base", false));
+  WT_TRY(check_param(b_base, "b_base", true));
+  WT_TRY(check_param(w_sub, "w_sub", false));
+  WT_TRY(check_param(base_scale, "base_scale", false));
+  WT_TRY(check_param(wavelet_scale, "wavelet_scale", false));
+  WT_TRY(check_param(dw_base, "dw_base", false));
+  WT_TRY(check_param(db_base, "db_base", true));
+  WT_TRY(check_param(dw_sub, "dw_sub", false));
+  WT_TRY(check_param(dbase_scale, "dbase_scale", false));
+  WT_TRY(check_param(dwavelet_scale, "dwavelet_scale", false));
+  WtBwPlan pl;
+  WT_TRY(plan_bw(desc, pl));
+  cudaStream_t st = (cudaStream_t)stream;
+  const int C = desc->C, L = desc->levels, KK = desc->k * desc->k;
+  if (desc->N == 0) {  // empty batch: every gradient is an empty sum
+    cudaError_t e = cudaMemsetAsync(dw_base, 0, sizeof(float) * C * KK, st);
+    if (e == cudaSuccess && db_base) e = cudaMemsetAsync(db_base, 0, sizeof(float) * C, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw_sub, 0, sizeof(float) * (size_t)L * 4 * C * KK, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dbase_scale, 0, sizeof(float) * C, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dwavelet_scale, 0, sizeof(float) * (size_t)L * 4 * C, st);
+    if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_weight: %s", cudaGetErrorString(e));
+    return ok();
+  }
+  WT_TRY(check_act(x, "x", desc));
+  WT_TRY(check_act(dy, "dy", desc));
+  const size_t need = bw_workspace_bytes(pl);
+  if (!ws || ws_bytes < need)
+    return fail(WTCONV_ERR_WORKSPACE, "workspace of %zu B given, %zu B needed", ws ? ws_bytes : 0, need);
+  if (!aligned(ws, 256)) return fail(WTCONV_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+  pl.vec_ok = vec_ok(desc, x, dy);
+  cudaError_t e = wt::launch_bwd_weight(pl, desc->dtype, x, dy, w_base, b_base, w_sub, base_scale,
+                                        wavelet_scale, dw_base, db_base, dw_sub, dbase_scale,
+                                        dwavelet_scale, static_cast<float*>(ws), st);
+  if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_weight: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+const char* wtconv_status_string(wtconv_status_t s) {
+  switch (s) {
+    case WTCONV_OK: return "WTCONV_OK";
+    case WTCONV_ERR_INVALID_ARG: return "WTCONV_ERR_INVALID_ARG";
+    case WTCONV_ERR_UNSUPPORTED: return "WTCONV_ERR_UNSUPPORTED";
+    case WTCONV_ERR_MISALIGNED: return "WTCONV_ERR_MISALIGNED";
+    case WTCONV_ERR_WORKSPACE: return "WTCONV_ERR_WORKSPACE";
+    case WTCONV_ERR_CUDA: return "WTCONV_ERR_CUDA";
+  }
+  return "WTCONV_STATUS_UNKNOWN";
+}
+
+const char* wtconv_last_error(void) { return g_last_error; }
+
+}  // extern "C"

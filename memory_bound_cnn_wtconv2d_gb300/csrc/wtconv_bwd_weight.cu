@@ -1,0 +1,214 @@
+// WTConv2d parameter gradients (sm_103a).
+//
+// Paper: "Fast and Memory-Efficient Wavelet Convolutions via I/O-Aware
+// Reformulation" (arXiv 2608.10805); the technical summary's "Key
+// contributions" state that the fused implementation reproduces all
+// parameter gradients.  With the scales folded into the weights
+// (summary, "Methodology", folding learned scales), every parameter
+// gradient follows from raw correlation sums:
+//
+//   base:     G_0[t]   = sum_{n,i,j} dy[i][j] * x[i+du-r][j+dv-r],   g = sum dy
+//   level l:  G_lb[t]  = sum_{n,p,q} D^l_b[p][q] * Y^l_b[p+du-r][q+dv-r]
+//
+// where Y^l = F_l x and D^l = F_l dy are the level-l Haar coefficients of x
+// and of dy (dL/dZ^l = F_l dy because the synthesis is F_l^T), and then
+//   dW_base = s_b G_0, db = s_b g, ds_b = <W_base, G_0> + b g,
+//   dW_l = s_w G_l,    ds_w = <W_l, G_l>.
+//
+// One CTA owns channel c and a chunk of the batch.  Planes of x and dy are
+// read once into shared memory, both pyramids are rebuilt there
+// (unnormalised, so G_l is recovered as 4^-l times the sum), and every
+// thread accumulates the K*K correlations of its fixed 4x4 tiles in
+// registers across the chunk.  At the end the tile sums of each band are
+// reduced through shared memory into one record per (chunk, channel); a
+// second kernel adds the records of all chunks in a fixed order, so the
+// result does not depend on scheduling.
+#include "wtconv_device.cuh"
+#include "wtconv_launch.h"
+
+namespace wt {
+
+template <int K, typename T>
+__global__ void __launch_bounds__(WT_BW_THREADS)
+    bw_kernel(const __grid_constant__ WtBwPlan pl, const T* __restrict__ x, const T* __restrict__ dy,
+              float* __restrict__ part) {
+  extern __shared__ __align__(16) float sm[];
+  constexpr int KK = K * K;
+  constexpr int NT = WT_BW_THREADS;
+  constexpr int MI = WT_BW_MAX_ITEMS;
+  constexpr int BT = WT_BT;
+  const int tid = threadIdx.x;
+  const int C = pl.C, L = pl.L;
+  const int c = blockIdx.x % C;
+  const int gi = blockIdx.x / C;
+  const int n_begin = gi * pl.chunk;
+  const int n_end = min(pl.N, n_begin + pl.chunk);
+  const int PF = pl.plane_floats;
+  const int ipp = pl.items_per_plane;
+
+  zero_smem(sm, pl.P * PF, tid, NT);
+
+  float acc[MI][KK];
+  float gs[MI];
+#pragma unroll
+  for (int s = 0; s < MI; ++s) {
+    gs[s] = 0.f;
+#pragma unroll
+    for (int t = 0; t < KK; ++t) acc[s][t] = 0.f;
+  }
+  __syncthreads();
+
+  for (int nb = n_begin; nb < n_end; nb += pl.P) {
+    const int np = min(pl.P, n_end - nb);
+    load_planes<T>(sm, PF, pl.xs[0], x, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, tid, NT);
+    load_planes<T>(sm, PF, pl.ds[0], dy, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, tid, NT);
+    __syncthreads();
+    for (int l = 1; l <= L; ++l) {
+      haar_level(sm, PF, np, pl.xs[l - 1], pl.xs[l], pl.Hs[l], pl.Ws[l], tid, NT);
+      haar_level(sm, PF, np, pl.ds[l - 1], pl.ds[l], pl.Hs[l], pl.Ws[l], tid, NT);
+      __syncthreads();
+    }
+#pragma unroll
+    for (int s = 0; s < MI; ++s) {
+      const int item = tid + s * NT;
+      if (item < pl.P * ipp) {
+        const int g = item / ipp;
+        if (g < np) {
+          const int local = item - g * ipp;
+          int l = 0;
+          while (l < L && local >= pl.item_begin[l + 1]) ++l;
+          const int tiles = pl.tr[l] * pl.tc[l];
+          const int rel = local - pl.item_begin[l];
+          const int b = rel / tiles;
+          const int t = rel - b * tiles;
+          const int tp = t / pl.tc[l];
+          const int p0 = tp * BT, q0 = (t - tp * pl.tc[l]) * BT;
+          const WtBuf Xb = pl.xs[l], Db = pl.ds[l];
+          const float* ps = sm + g * PF;
+          const float dsum =
+              corr_tile<K, BT, BT>(ps + Xb.off + b * Xb.band + p0 * Xb.stride + q0, Xb.stride,
+                                   ps + Db.off + b * Db.band + p0 * Db.stride + q0, Db.stride, acc[s]);
+          if (l == 0) gs[s] += dsum;
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // Tile sums -> shared memory -> one record per band.
+  float* red = sm;
+  const int rs = KK + 1;
+#pragma unroll
+  for (int s = 0; s < MI; ++s) {
+    const int item = tid + s * NT;
+    if (item < pl.P * ipp) {
+#pragma unroll
+      for (int t = 0; t < KK; ++t) red[item * rs + t] = acc[s][t];
+      red[item * rs + KK] = gs[s];
+    }
+  }
+  __syncthreads();
+  float* rec = part + ((size_t)gi * C + c) * pl.part_stride;
+  for (int qd = tid; qd < pl.nbands * rs; qd += NT) {
+    const int B = qd / rs;
+    const int t = qd - B * rs;
+    const int l = (B == 0) ? 0 : 1 + ((B - 1) >> 2);
+    const int b = (B == 0) ? 0 : ((B - 1) & 3);
+    const int tiles = pl.tr[l] * pl.tc[l];
+    const int first = pl.item_begin[l] + b * tiles;
+    float sum = 0.f;
+    if (B == 0 || t < KK) {
+      for (int g = 0; g < pl.P; ++g)
+        for (int i = 0; i < tiles; ++i) sum += red[(g * ipp + first + i) * rs + t];
+    }
+    rec[qd] = sum;
+  }
+}
+
+// Adds the records of all chunks of channel c in chunk order and unfolds the
+// scales.  One thread per (channel, band).
+__global__ void bw_finalize_kernel(const __grid_constant__ WtBwPlan pl, const float* __restrict__ part,
+                                   const float* __restrict__ w_base, const float* __restrict__ b_base,
+                                   const float* __restrict__ w_sub, const float* __restrict__ s_base,
+                                   const float* __restrict__ s_w, float* __restrict__ dw_base,
+                                   float* __restrict__ db_base, float* __restrict__ dw_sub,
+                                   float* __restrict__ ds_base, float* __restrict__ ds_w) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  const int C = pl.C, K = pl.K, KK = K * K, rs = KK + 1;
+  if (idx >= C * pl.nbands) return;
+  const int c = idx / pl.nbands;
+  const int B = idx - c * pl.nbands;
+  const float* base = part + (size_t)c * pl.part_stride + (size_t)B * rs;
+  const size_t gstride = (size_t)C * pl.part_stride;
+  if (B == 0) {
+    const float sb = s_base[c];
+    double ds = 0.0;  // short dot product, accumulated in double
+    for (int t = 0; t < KK; ++t) {
+      float G = 0.f;
+      for (int g = 0; g < pl.groups; ++g) G += base[g * gstride + t];
+      dw_base[(size_t)c * KK + t] = sb * G;
+      ds += (double)w_base[(size_t)c * KK + t] * G;
+    }
+    float gsum = 0.f;
+    for (int g = 0; g < pl.groups; ++g) gsum += base[g * gstride + KK];
+    if (db_base) db_base[c] = sb * gsum;
+    if (b_base) ds += (double)b_base[c] * gsum;
+    ds_base[c] = (float)ds;
+  } else {
+    const int l = 1 + ((B - 1) >> 2), b = (B - 1) & 3;
+    const size_t ch = (size_t)(l - 1) * 4 * C + 4 * c + b;
+    const float sw = s_w[ch];
+    double ds = 0.0;
+    for (int t = 0; t < KK; ++t) {
+      float G = 0.f;
+      for (int g = 0; g < pl.groups; ++g) G += base[g * gstride + t];
+      G = ldexpf(G, -2 * l);
+      dw_sub[ch * KK + t] = sw * G;
+      ds += (double)w_sub[ch * KK + t] * G;
+    }
+    ds_w[ch] = (float)ds;
+  }
+}
+
+template <int K, typename T>
+static cudaError_t launch_bw_t(const WtBwPlan& pl, const void* x, const void* dy, float* part,
+                               cudaStream_t stream) {
+  auto kern = bw_kernel<K, T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)pl.C * (unsigned)pl.groups;
+  kern<<<grid, WT_BW_THREADS, pl.smem_bytes, stream>>>(pl, static_cast<const T*>(x),
+                                                       static_cast<const T*>(dy), part);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_bw_k(const WtBwPlan& pl, const void* x, const void* dy, float* part,
+                               cudaStream_t stream) {
+  switch (pl.K) {
+    case 3: return launch_bw_t<3, T>(pl, x, dy, part, stream);
+    case 5: return launch_bw_t<5, T>(pl, x, dy, part, stream);
+    case 7: return launch_bw_t<7, T>(pl, x, dy, part, stream);
+    case 9: return launch_bw_t<9, T>(pl, x, dy, part, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_bwd_weight(const WtBwPlan& pl, int dtype, const void* x, const void* dy,
+                              const float* w_base, const float* b_base, const float* w_sub,
+                              const float* s_base, const float* s_w, float* dw_base, float* db_base,
+                              float* dw_sub, float* ds_base, float* ds_w, float* part,
+                              cudaStream_t stream) {
+  cudaError_t e;
+  if (dtype == 0) e = launch_bw_k<float>(pl, x, dy, part, stream);
+  else if (dtype == 1) e = launch_bw_k<__half>(pl, x, dy, part, stream);
+  else e = launch_bw_k<__nv_bfloat16>(pl, x, dy, part, stream);
+  if (e != cudaSuccess) return e;
+  const int n = pl.C * pl.nbands;
+  const int threads = 128;
+  bw_finalize_kernel<<<(n + threads - 1) / threads, threads, 0, stream>>>(
+      pl, part, w_base, b_base, w_sub, s_base, s_w, dw_base, db_base, dw_sub, ds_base, ds_w);
+  return cudaGetLastError();
+}
+
+}  // namespace wt

@@ -1,0 +1,22 @@
+// Internal launchers of libwtconv (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "wtconv_plan.h"
+
+namespace wt {
+
+// Forward pass (rotate = false) or input-gradient pass (rotate = true, no bias).
+cudaError_t launch_fwd(const WtFwdPlan& pl, int dtype, bool rotate, const void* x, const float* w_base,
+                       const float* b_base, const float* w_sub, const float* s_base, const float* s_w,
+                       void* y, cudaStream_t stream);
+
+// Parameter gradients: correlation kernel into `part`, then the finalize kernel.
+cudaError_t launch_bwd_weight(const WtBwPlan& pl, int dtype, const void* x, const void* dy,
+                              const float* w_base, const float* b_base, const float* w_sub,
+                              const float* s_base, const float* s_w, float* dw_base, float* db_base,
+                              float* dw_sub, float* ds_base, float* ds_w, float* part,
+                              cudaStream_t stream);
+
+}  // namespace wt

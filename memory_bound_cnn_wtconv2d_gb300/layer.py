@@ -1,0 +1,58 @@
+"""WTConv2d as a torch autograd function / module on top of the C ABI.
+
+A drop-in replacement for a depthwise k x k convolution ("Fast and
+Memory-Efficient Wavelet Convolutions via I/O-Aware Reformulation",
+arXiv 2608.10805, technical summary "Problem statement").  Forward runs
+``wtconv_fwd``; backward runs ``wtconv_bwd_data`` and ``wtconv_bwd_weight``.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import wtconv as _c
+
+
+class WTConv2dFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k):
+        x = x.contiguous()
+        y = _c.wtconv_fwd(x, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k)
+        ctx.save_for_backward(x, w_base, b_base, w_sub, base_scale, wavelet_scale)
+        ctx.levels, ctx.k, ctx.has_bias = levels, k, b_base is not None
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, w_base, b_base, w_sub, base_scale, wavelet_scale = ctx.saved_tensors
+        dy = dy.contiguous().to(x.dtype)
+        dx = _c.wtconv_bwd_data(dy, w_base, w_sub, base_scale, wavelet_scale, ctx.levels, ctx.k)
+        g = _c.wtconv_bwd_weight(x, dy, w_base, b_base if ctx.has_bias else None, w_sub, base_scale,
+                                 wavelet_scale, ctx.levels, ctx.k)
+        return (dx, g["dw_base"], g["db_base"], g["dw_sub"], g["dbase_scale"], g["dwavelet_scale"],
+                None, None)
+
+
+class WTConv2d(torch.nn.Module):
+    """Wavelet convolution on C channels with `levels` Haar levels and k x k kernels.
+
+    Parameters (float32): weight [C,k,k] and bias [C] of the base depthwise
+    conv, base_scale [C] (init 1), wavelet_weight [L,4C,k,k] (subband channel
+    4c+b), wavelet_scale [L,4C] (init 0.1).
+    """
+
+    def __init__(self, channels: int, kernel_size: int = 5, levels: int = 1, bias: bool = True,
+                 device=None):
+        super().__init__()
+        C, k, L = channels, kernel_size, levels
+        f = dict(device=device, dtype=torch.float32)
+        bound = 1.0 / k
+        self.levels, self.k = L, k
+        self.weight = torch.nn.Parameter(torch.empty(C, k, k, **f).uniform_(-bound, bound))
+        self.bias = torch.nn.Parameter(torch.zeros(C, **f)) if bias else None
+        self.base_scale = torch.nn.Parameter(torch.ones(C, **f))
+        self.wavelet_weight = torch.nn.Parameter(torch.empty(L, 4 * C, k, k, **f).uniform_(-bound, bound))
+        self.wavelet_scale = torch.nn.Parameter(torch.full((L, 4 * C), 0.1, **f))
+
+    def forward(self, x):
+        return WTConv2dFunction.apply(x, self.weight, self.bias, self.wavelet_weight, self.base_scale,
+                                      self.wavelet_scale, self.levels, self.k)

@@ -1,0 +1,91 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+declared in include/wtconv.h, and rejects bad arguments with a status code
+before it touches the device (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+from memory_bound_cnn_wtconv2d_gb300 import build, wtconv
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return wtconv.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "wtconv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(wtconv_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert set(wtconv.EXPORTS) <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code, name in [(0, "WTCONV_OK"), (1, "WTCONV_ERR_INVALID_ARG"), (2, "WTCONV_ERR_UNSUPPORTED"),
+                       (3, "WTCONV_ERR_MISALIGNED"), (4, "WTCONV_ERR_WORKSPACE"), (5, "WTCONV_ERR_CUDA")]:
+        assert L.wtconv_status_string(code).decode() == name
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def call_fwd(L, desc, x=FAKE, y=FAKE, w=FAKE):
+    p = ctypes.c_void_p
+    return L.wtconv_fwd(ctypes.byref(desc), p(x), p(w), None, p(w), p(w), p(w), p(y), None, 0, None)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("k", 4, wtconv.WTCONV_ERR_INVALID_ARG), ("k", 1, wtconv.WTCONV_ERR_INVALID_ARG),
+    ("k", 11, wtconv.WTCONV_ERR_INVALID_ARG), ("levels", 0, wtconv.WTCONV_ERR_INVALID_ARG),
+    ("levels", 9, wtconv.WTCONV_ERR_INVALID_ARG), ("N", -1, wtconv.WTCONV_ERR_INVALID_ARG),
+    ("C", 0, wtconv.WTCONV_ERR_INVALID_ARG), ("H", 0, wtconv.WTCONV_ERR_INVALID_ARG),
+    ("dtype", 7, wtconv.WTCONV_ERR_INVALID_ARG), ("H", 4096, wtconv.WTCONV_ERR_UNSUPPORTED),
+])
+def test_invalid_descriptors(L, field, value, code):
+    d = wtconv.make_desc(2, 3, 16, 16, 2, 5, 0)
+    setattr(d, field, value)
+    if field == "H" and value == 4096:
+        d.W = 4096
+    assert call_fwd(L, d) == code
+    assert L.wtconv_last_error().decode() != ""
+
+
+def test_null_and_misaligned_pointers(L):
+    d = wtconv.make_desc(2, 3, 16, 16, 2, 5, 0)
+    assert call_fwd(L, d, x=0) == wtconv.WTCONV_ERR_INVALID_ARG
+    assert call_fwd(L, d, w=0) == wtconv.WTCONV_ERR_INVALID_ARG
+    assert call_fwd(L, d, x=FAKE + 2) == wtconv.WTCONV_ERR_MISALIGNED
+    d16 = wtconv.make_desc(2, 3, 16, 16, 2, 5, 1)
+    assert call_fwd(L, d16, y=FAKE + 1) == wtconv.WTCONV_ERR_MISALIGNED
+
+
+def test_bwd_weight_workspace_checks(L):
+    d = wtconv.make_desc(4, 8, 28, 28, 3, 5, 0)
+    need = L.wtconv_workspace_size(ctypes.byref(d), wtconv.OP_BWD_WEIGHT)
+    assert need > 0 and need % 256 == 0
+    assert L.wtconv_workspace_size(ctypes.byref(d), wtconv.OP_FWD) == 0
+    p = ctypes.c_void_p(FAKE)
+    rc = L.wtconv_bwd_weight(ctypes.byref(d), p, p, p, None, p, p, p, p, None, p, p, p, p, need - 256, None)
+    assert rc == wtconv.WTCONV_ERR_WORKSPACE
+    rc = L.wtconv_bwd_weight(ctypes.byref(d), p, p, p, None, p, p, p, p, None, p, p, p, None, need, None)
+    assert rc == wtconv.WTCONV_ERR_WORKSPACE
+    rc = L.wtconv_bwd_weight(ctypes.byref(d), p, p, p, None, p, p, p, p, None, p, p, p,
+                             ctypes.c_void_p(FAKE + 16), need, None)
+    assert rc == wtconv.WTCONV_ERR_MISALIGNED
+
+
+def test_workspace_size_invalid_desc_is_zero(L):
+    d = wtconv.make_desc(4, 8, 28, 28, 3, 4, 0)
+    assert L.wtconv_workspace_size(ctypes.byref(d), wtconv.OP_BWD_WEIGHT) == 0
+    assert L.wtconv_workspace_size(None, wtconv.OP_BWD_WEIGHT) == 0
