@@ -122,6 +122,30 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
                                   float* dw_base, float* db_base, float* dw_sub, float* dbase_scale,
                                   float* dwavelet_scale, void* ws, size_t ws_bytes, void* stream);
 
+/* Parameter gradients without a workspace argument, for callers that cannot
+ * allocate device memory themselves (for example a plugin inside a host
+ * application that owns the whole device-memory budget, or a latency-bound
+ * caller that must not call cudaMalloc because it can synchronise the
+ * device).  The paper has no counterpart of this call; it is packaging.
+ * Same arguments, results and errors as wtconv_bwd_weight, except that the
+ * partial sums go to a scratch array of 4 MiB built into the library: a
+ * static device array that every GPU which loads the library holds until the
+ * process exits.  Layers needing more than 4 MiB of scratch (see
+ * wtconv_workspace_size) return WTCONV_ERR_UNSUPPORTED with a message; use
+ * wtconv_bwd_weight for them.  Nothing is allocated by this call.
+ * The first call on a device looks up the array's device address on the
+ * current device (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last
+ * call's contents (every entry is rewritten before use, so nothing needs
+ * clearing): calls that can overlap on the GPU -- on different streams, or
+ * from different host threads -- race on it and must be serialised by the
+ * caller. */
+wtconv_status_t wtconv_bwd_weight_noalloc(const wtconv_desc_t* desc, const void* x, const void* dy,
+                                          const float* w_base, const float* b_base, const float* w_sub,
+                                          const float* base_scale, const float* wavelet_scale,
+                                          float* dw_base, float* db_base, float* dw_sub,
+                                          float* dbase_scale, float* dwavelet_scale, void* stream);
+
 /* Static name of a status code. */
 const char* wtconv_status_string(wtconv_status_t status);
 

@@ -195,6 +195,10 @@ size_t bw_workspace_bytes(const WtBwPlan& pl) {
 
 }  // namespace
 
+namespace wt {
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+}  // namespace wt
+
 extern "C" {
 
 size_t wtconv_workspace_size(const wtconv_desc_t* desc, int op) {

@@ -19,4 +19,7 @@ cudaError_t launch_bwd_weight(const WtBwPlan& pl, int dtype, const void* x, cons
                               float* dw_sub, float* ds_base, float* ds_w, float* part,
                               cudaStream_t stream);
 
+// Sets the thread-local message returned by wtconv_last_error().
+void set_last_error(const char* msg);
+
 }  // namespace wt

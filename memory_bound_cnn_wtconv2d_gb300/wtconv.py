@@ -24,7 +24,7 @@ DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 # entry points declared in include/wtconv.h
 EXPORTS = ("wtconv_workspace_size", "wtconv_fwd", "wtconv_bwd_data", "wtconv_bwd_weight",
-           "wtconv_status_string", "wtconv_last_error")
+           "wtconv_bwd_weight_noalloc", "wtconv_status_string", "wtconv_last_error")
 
 
 class WtconvDesc(ctypes.Structure):
@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         L.wtconv_bwd_data.restype = ctypes.c_int
         L.wtconv_bwd_weight.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.wtconv_bwd_weight.restype = ctypes.c_int
+        L.wtconv_bwd_weight_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.wtconv_bwd_weight_noalloc.restype = ctypes.c_int
         L.wtconv_status_string.argtypes = [ctypes.c_int]
         L.wtconv_status_string.restype = ctypes.c_char_p
         L.wtconv_last_error.argtypes = []
@@ -161,4 +163,26 @@ def wtconv_bwd_weight(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, l
         _ptr(_param(base_scale, "base_scale")), _ptr(_param(wavelet_scale, "wavelet_scale")),
         _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
         _ptr(grads["dwavelet_scale"]), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return grads
+
+
+def wtconv_bwd_weight_noalloc(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k,
+                              grads=None, stream=None):
+    """Parameter gradients through the entry point that allocates nothing: the
+    library's built-in 4 MiB device scratch replaces the workspace.  For callers
+    that cannot allocate device memory; concurrent calls race on the scratch."""
+    _act(x, "x")
+    _act(dy, "dy")
+    desc = desc_for(x, levels, k)
+    if grads is None:
+        grads = dict(dw_base=torch.empty_like(w_base),
+                     db_base=None if b_base is None else torch.empty_like(b_base),
+                     dw_sub=torch.empty_like(w_sub), dbase_scale=torch.empty_like(base_scale),
+                     dwavelet_scale=torch.empty_like(wavelet_scale))
+    _check(lib().wtconv_bwd_weight_noalloc(
+        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(_param(w_base, "w_base")),
+        _ptr(_param(b_base, "b_base", True)), _ptr(_param(w_sub, "w_sub")),
+        _ptr(_param(base_scale, "base_scale")), _ptr(_param(wavelet_scale, "wavelet_scale")),
+        _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
+        _ptr(grads["dwavelet_scale"]), _stream(stream)))
     return grads
