@@ -38,6 +38,15 @@ constexpr int kBwBudget = 112 * 1024;     // preferred gradient CTA footprint (>
 int round_up(int a, int b) { return (a + b - 1) / b * b; }
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+WtDiv make_div(int d) {
+  uint32_t s = 0;
+  while ((1u << s) < (uint32_t)d) ++s;
+  WtDiv f;
+  f.shift = s;
+  f.mul = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << s) - (uint64_t)d)) / (uint64_t)d + 1);
+  return f;
+}
+
 size_t elem_size(int dtype) { return dtype == WTCONV_F32 ? 4 : 2; }
 
 wtconv_status_t validate_desc(const wtconv_desc_t* d) {
@@ -64,12 +73,15 @@ void level_sizes(const wtconv_desc_t* d, int* Hs, int* Ws) {
   }
 }
 
-// Places a padded plane buffer of `nb` bands at `off`; returns the next offset.
-int place(WtBuf& b, int off, int er, int ec, int pad, int nb) {
+// Places a plane buffer of `nb` bands at `off`; the interior is er x ec with
+// prow/pcol zero rows/columns before it and at least as many after it; rows
+// are padded to `min_stride` floats and to a multiple of 4.  Returns the next offset.
+int place(WtBuf& b, int off, int er, int ec, int prow, int pcol, int nb, int min_stride = 0) {
   b.off = off;
-  b.pad = pad;
-  b.stride = round_up(ec + 2 * pad, 4);
-  b.band = (er + 2 * pad) * b.stride;
+  b.prow = prow;
+  b.pcol = pcol;
+  b.stride = round_up(ec + 2 * pcol > min_stride ? ec + 2 * pcol : min_stride, 4);
+  b.band = (er + 2 * prow) * b.stride;
   return off + nb * b.band;
 }
 
@@ -78,27 +90,37 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
   const int R = d->k / 2, L = d->levels, KK = d->k * d->k;
   level_sizes(d, pl.Hs, pl.Ws);
-  int er[WT_MAXL + 1], ec[WT_MAXL + 1];
+  pl.ftr = ceil_div(pl.Hs[1], WT_TP);
+  pl.ftc = ceil_div(pl.Ws[1], WT_TQ);
+  // Input plane (own buffer): R zero rows above, a 4-float (16-byte) left
+  // margin so its interior rows are 16-byte aligned.  Rows cover the final
+  // tiles' windows (4*ftr + 2R) and row length covers their reads.
+  pl.xf = round_up(place(pl.lev[0], 0, 2 * WT_TP * pl.ftr, 2 * WT_TQ * pl.ftc, R, 4, 1,
+                        2 * WT_TQ * pl.ftc + 8), 4);
+  int off = 0;  // work area: pyramid levels 1..L, then convolved bands
+  pl.zbegin[1] = 0;
   for (int l = 1; l <= L; ++l) {
-    pl.tr[l] = ceil_div(pl.Hs[l], WT_TP);
-    pl.tc[l] = ceil_div(pl.Ws[l], WT_TQ);
-    er[l] = pl.tr[l] * WT_TP;
-    ec[l] = pl.tc[l] * WT_TQ;
+    pl.ztr[l] = ceil_div(pl.Hs[l], WT_ZT);
+    pl.ztc[l] = ceil_div(pl.Ws[l], WT_ZT);
+    off = place(pl.lev[l], off, WT_ZT * pl.ztr[l], WT_ZT * pl.ztc[l], R, R, 4);
+    pl.zbegin[l + 1] = pl.zbegin[l] + 4 * pl.ztr[l] * pl.ztc[l];
   }
-  er[0] = 2 * er[1];
-  ec[0] = 2 * ec[1];
-  int off = 0;
-  off = place(pl.lev[0], off, er[0], ec[0], R, 1);
-  for (int l = 1; l <= L; ++l) off = place(pl.lev[l], off, er[l], ec[l], R, 4);
-  for (int l = 1; l < L; ++l) off = place(pl.syn[l], off, er[l], ec[l], 0, 1);
-  pl.plane_floats = round_up(off, 4);
+  pl.zipp = pl.zbegin[L + 1];
+  for (int l = 1; l <= L; ++l) {
+    // Z^l: written on the band-convolution grid, read by the final tiles at
+    // (p >> (l-1), q >> (l-1)) for every level-1 position of the tile grid.
+    const int zr = WT_ZT * pl.ztr[l], zc = WT_ZT * pl.ztc[l];
+    const int fr = ((WT_TP * pl.ftr - 1) >> (l - 1)) + 1, fc = ((WT_TQ * pl.ftc - 1) >> (l - 1)) + 1;
+    off = place(pl.zb[l], off, zr > fr ? zr : fr, zc > fc ? zc : fc, 0, 0, 4);
+  }
+  pl.wf = round_up(off, 4);
   pl.w_band = round_up(KK, 4);
   const int wfloats = (1 + 4 * L) * pl.w_band;
-  const long plane_bytes = 4L * pl.plane_floats;
+  const long plane_bytes = 4L * (2 * pl.xf + pl.wf);
   if (plane_bytes + 4L * wfloats > kMaxSmemPerBlock)
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %ld B of shared memory (max %d)",
                 d->H, d->W, L, plane_bytes + 4L * wfloats, kMaxSmemPerBlock);
-  const int items = pl.tr[1] * pl.tc[1];
+  const int items = pl.ftr * pl.ftc;
   int P = ceil_div(WT_FWD_THREADS, items);
   P = P < 1 ? 1 : P;
   const int fit = (int)((kFwdBudget - 4L * wfloats) / plane_bytes);
@@ -106,8 +128,27 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   if (d->N > 0 && P > d->N) P = d->N;
   pl.P = P;
   pl.groups = d->N > 0 ? ceil_div(d->N, P) : 0;
-  pl.w_off = P * pl.plane_floats;
-  pl.smem_bytes = 4 * (P * pl.plane_floats + wfloats);
+  pl.work_off = 2 * P * pl.xf;
+  pl.w_off = pl.work_off + P * pl.wf;
+  pl.smem_bytes = 4 * (pl.w_off + wfloats);
+  if (L == 1) {
+    pl.an_pp[1] = make_div(pl.Hs[1] * pl.Ws[1]);
+    pl.an_w[1] = make_div(pl.Ws[1]);
+  } else {
+    pl.an_pp[2] = make_div(pl.Hs[2] * pl.Ws[2]);
+    pl.an_w[2] = make_div(pl.Ws[2]);
+  }
+  for (int l = 3; l <= L; ++l) {
+    pl.an_pp[l] = make_div(pl.Hs[l] * pl.Ws[l]);
+    pl.an_w[l] = make_div(pl.Ws[l]);
+  }
+  pl.z_ipp = make_div(pl.zipp);
+  for (int l = 1; l <= L; ++l) {
+    pl.z_tiles[l] = make_div(pl.ztr[l] * pl.ztc[l]);
+    pl.z_tc[l] = make_div(pl.ztc[l]);
+  }
+  pl.f_pp = make_div(pl.ftr * pl.ftc);
+  pl.f_c = make_div(pl.ftc);
   return WTCONV_OK;
 }
 
@@ -122,8 +163,8 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
     pl.tr[l] = ceil_div(pl.Hs[l], WT_BT);
     pl.tc[l] = ceil_div(pl.Ws[l], WT_BT);
     const int nb = l == 0 ? 1 : 4;
-    off = place(pl.xs[l], off, pl.tr[l] * WT_BT, pl.tc[l] * WT_BT, R, nb);
-    off = place(pl.ds[l], off, pl.tr[l] * WT_BT, pl.tc[l] * WT_BT, 0, nb);
+    off = place(pl.xs[l], off, pl.tr[l] * WT_BT, pl.tc[l] * WT_BT, R, R, nb);
+    off = place(pl.ds[l], off, pl.tr[l] * WT_BT, pl.tc[l] * WT_BT, 0, 0, nb);
     pl.item_begin[l + 1] = pl.item_begin[l] + nb * pl.tr[l] * pl.tc[l];
   }
   pl.items_per_plane = pl.item_begin[L + 1];
@@ -148,9 +189,19 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %ld B of shared memory (max %d)",
                 d->H, d->W, L, smem, kMaxSmemPerBlock);
   pl.smem_bytes = (int)smem;
-  // One wave of (channel, chunk) CTAs when the channels allow it.
-  const int per_sm = (int)(kSmemPerSm / (smem + 1024));
-  const int ctas = kNumSms * (per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm));
+  for (int l = 0; l <= L; ++l) {
+    pl.an_pp[l] = make_div(pl.Hs[l] * pl.Ws[l]);
+    pl.an_w[l] = make_div(pl.Ws[l]);
+    pl.tiles[l] = make_div(pl.tr[l] * pl.tc[l]);
+    pl.tcd[l] = make_div(pl.tc[l]);
+  }
+  pl.ipp = make_div(pl.items_per_plane);
+  // One wave of (channel, chunk) CTAs when the channels allow it.  Resident
+  // CTAs per SM: limited by shared memory and by registers (256 threads of
+  // up to 128 registers each -> 2).
+  int per_sm = (int)(kSmemPerSm / (smem + 1024));
+  if (per_sm > 2) per_sm = 2;
+  const int ctas = kNumSms * (per_sm < 1 ? 1 : per_sm);
   const int batches = d->N > 0 ? ceil_div(d->N, P) : 0;
   int groups = ctas / d->C;
   if (groups < 1) groups = 1;
@@ -180,6 +231,15 @@ wtconv_status_t check_param(const void* p, const char* name, bool nullable) {
 int vec_ok(const wtconv_desc_t* d, const void* a, const void* b) {
   const int v = (int)(16 / elem_size(d->dtype));
   return (d->W % v == 0) && aligned(a, 16) && (b == nullptr || aligned(b, 16));
+}
+
+// Plane-load loop divisors: 16-byte items when the rows allow it, else elements.
+template <typename Plan>
+void set_load_divs(Plan& pl, const wtconv_desc_t* d, int vec) {
+  pl.vec_ok = vec;
+  const int per_row = vec ? d->W / (int)(16 / elem_size(d->dtype)) : d->W;
+  pl.ld_pp = make_div(d->H * per_row);
+  pl.ld_w = make_div(per_row);
 }
 
 size_t bw_workspace_bytes(const WtBwPlan& pl) {
@@ -226,7 +286,7 @@ wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float
   if (desc->N == 0) return ok();
   WT_TRY(check_act(x, "x", desc));
   WT_TRY(check_act(y, "y", desc));
-  pl.vec_ok = vec_ok(desc, x, y);
+  set_load_divs(pl, desc, vec_ok(desc, x, y));
   cudaError_t e = wt::launch_fwd(pl, desc->dtype, false, x, w_base, b_base, w_sub, base_scale,
                                  wavelet_scale, y, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_fwd: %s", cudaGetErrorString(e));
@@ -249,7 +309,7 @@ wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const
   if (desc->N == 0) return ok();
   WT_TRY(check_act(dy, "dy", desc));
   WT_TRY(check_act(dx, "dx", desc));
-  pl.vec_ok = vec_ok(desc, dy, dx);
+  set_load_divs(pl, desc, vec_ok(desc, dy, dx));
   cudaError_t e = wt::launch_fwd(pl, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale,
                                  wavelet_scale, dx, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_data: %s", cudaGetErrorString(e));
@@ -291,7 +351,7 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
   if (!ws || ws_bytes < need)
     return fail(WTCONV_ERR_WORKSPACE, "workspace of %zu B given, %zu B needed", ws ? ws_bytes : 0, need);
   if (!aligned(ws, 256)) return fail(WTCONV_ERR_MISALIGNED, "workspace is not 256-byte aligned");
-  pl.vec_ok = vec_ok(desc, x, dy);
+  set_load_divs(pl, desc, vec_ok(desc, x, dy));
   cudaError_t e = wt::launch_bwd_weight(pl, desc->dtype, x, dy, w_base, b_base, w_sub, base_scale,
                                         wavelet_scale, dw_base, db_base, dw_sub, dbase_scale,
                                         dwavelet_scale, static_cast<float*>(ws), st);

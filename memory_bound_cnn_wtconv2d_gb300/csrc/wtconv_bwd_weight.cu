@@ -60,28 +60,28 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
 
   for (int nb = n_begin; nb < n_end; nb += pl.P) {
     const int np = min(pl.P, n_end - nb);
-    load_planes<T>(sm, PF, pl.xs[0], x, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, tid, NT);
-    load_planes<T>(sm, PF, pl.ds[0], dy, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, tid, NT);
+    load_planes<T>(sm, PF, pl.xs[0], x, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+    load_planes<T>(sm, PF, pl.ds[0], dy, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
     __syncthreads();
     for (int l = 1; l <= L; ++l) {
-      haar_level(sm, PF, np, pl.xs[l - 1], pl.xs[l], pl.Hs[l], pl.Ws[l], tid, NT);
-      haar_level(sm, PF, np, pl.ds[l - 1], pl.ds[l], pl.Hs[l], pl.Ws[l], tid, NT);
+      haar_level(sm, PF, sm, PF, np, pl.xs[l - 1], pl.xs[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
+      haar_level(sm, PF, sm, PF, np, pl.ds[l - 1], pl.ds[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
       __syncthreads();
     }
 #pragma unroll
     for (int s = 0; s < MI; ++s) {
       const int item = tid + s * NT;
       if (item < pl.P * ipp) {
-        const int g = item / ipp;
+        const int g = fdiv(item, pl.ipp);
         if (g < np) {
           const int local = item - g * ipp;
           int l = 0;
           while (l < L && local >= pl.item_begin[l + 1]) ++l;
           const int tiles = pl.tr[l] * pl.tc[l];
           const int rel = local - pl.item_begin[l];
-          const int b = rel / tiles;
+          const int b = fdiv(rel, pl.tiles[l]);
           const int t = rel - b * tiles;
-          const int tp = t / pl.tc[l];
+          const int tp = fdiv(t, pl.tcd[l]);
           const int p0 = tp * BT, q0 = (t - tp * pl.tc[l]) * BT;
           const WtBuf Xb = pl.xs[l], Db = pl.ds[l];
           const float* ps = sm + g * PF;
@@ -126,47 +126,58 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
 }
 
 // Adds the records of all chunks of channel c in chunk order and unfolds the
-// scales.  One thread per (channel, band).
+// scales.  One warp per (channel, band): lane t owns taps t, t+32, t+64; the
+// scale gradient <W, G> is reduced with a fixed shuffle tree, so the result
+// does not depend on scheduling.
 __global__ void bw_finalize_kernel(const __grid_constant__ WtBwPlan pl, const float* __restrict__ part,
                                    const float* __restrict__ w_base, const float* __restrict__ b_base,
                                    const float* __restrict__ w_sub, const float* __restrict__ s_base,
                                    const float* __restrict__ s_w, float* __restrict__ dw_base,
                                    float* __restrict__ db_base, float* __restrict__ dw_sub,
                                    float* __restrict__ ds_base, float* __restrict__ ds_w) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
   const int C = pl.C, K = pl.K, KK = K * K, rs = KK + 1;
-  if (idx >= C * pl.nbands) return;
-  const int c = idx / pl.nbands;
-  const int B = idx - c * pl.nbands;
-  const float* base = part + (size_t)c * pl.part_stride + (size_t)B * rs;
+  if (warp >= C * pl.nbands) return;  // whole warps exit together
+  const int c = warp / pl.nbands;
+  const int B = warp - c * pl.nbands;
+  const float* rec = part + (size_t)c * pl.part_stride + (size_t)B * rs;
   const size_t gstride = (size_t)C * pl.part_stride;
+  int l = 0;
+  size_t ch = 0;
+  float scale;
+  const float* w;
+  float* dw;
   if (B == 0) {
-    const float sb = s_base[c];
-    double ds = 0.0;  // short dot product, accumulated in double
-    for (int t = 0; t < KK; ++t) {
-      float G = 0.f;
-      for (int g = 0; g < pl.groups; ++g) G += base[g * gstride + t];
-      dw_base[(size_t)c * KK + t] = sb * G;
-      ds += (double)w_base[(size_t)c * KK + t] * G;
-    }
-    float gsum = 0.f;
-    for (int g = 0; g < pl.groups; ++g) gsum += base[g * gstride + KK];
-    if (db_base) db_base[c] = sb * gsum;
-    if (b_base) ds += (double)b_base[c] * gsum;
-    ds_base[c] = (float)ds;
+    scale = s_base[c];
+    w = w_base + (size_t)c * KK;
+    dw = dw_base + (size_t)c * KK;
   } else {
-    const int l = 1 + ((B - 1) >> 2), b = (B - 1) & 3;
-    const size_t ch = (size_t)(l - 1) * 4 * C + 4 * c + b;
-    const float sw = s_w[ch];
-    double ds = 0.0;
-    for (int t = 0; t < KK; ++t) {
-      float G = 0.f;
-      for (int g = 0; g < pl.groups; ++g) G += base[g * gstride + t];
-      G = ldexpf(G, -2 * l);
-      dw_sub[ch * KK + t] = sw * G;
-      ds += (double)w_sub[ch * KK + t] * G;
+    l = 1 + ((B - 1) >> 2);
+    ch = (size_t)(l - 1) * 4 * C + 4 * c + ((B - 1) & 3);
+    scale = s_w[ch];
+    w = w_sub + ch * KK;
+    dw = dw_sub + ch * KK;
+  }
+  float dot = 0.f;
+  for (int t = lane; t < KK; t += 32) {
+    float G = 0.f;
+    for (int g = 0; g < pl.groups; ++g) G += rec[g * gstride + t];
+    G = ldexpf(G, -2 * l);  // level-l sums were taken on unnormalised coefficients
+    dw[t] = scale * G;
+    dot = fmaf(w[t], G, dot);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  if (lane == 0) {
+    if (B == 0) {
+      float gsum = 0.f;
+      for (int g = 0; g < pl.groups; ++g) gsum += rec[g * gstride + KK];
+      if (db_base) db_base[c] = scale * gsum;
+      ds_base[c] = b_base ? fmaf(b_base[c], gsum, dot) : dot;
+    } else {
+      ds_w[ch] = dot;
     }
-    ds_w[ch] = (float)ds;
   }
 }
 
@@ -204,9 +215,9 @@ cudaError_t launch_bwd_weight(const WtBwPlan& pl, int dtype, const void* x, cons
   else if (dtype == 1) e = launch_bw_k<__half>(pl, x, dy, part, stream);
   else e = launch_bw_k<__nv_bfloat16>(pl, x, dy, part, stream);
   if (e != cudaSuccess) return e;
-  const int n = pl.C * pl.nbands;
-  const int threads = 128;
-  bw_finalize_kernel<<<(n + threads - 1) / threads, threads, 0, stream>>>(
+  const int warps = pl.C * pl.nbands;
+  const int threads = 256;
+  bw_finalize_kernel<<<(warps * 32 + threads - 1) / threads, threads, 0, stream>>>(
       pl, part, w_base, b_base, w_sub, s_base, s_w, dw_base, db_base, dw_sub, ds_base, ds_w);
   return cudaGetLastError();
 }

@@ -25,6 +25,10 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
   return __float2bfloat16_rn(v);
 }
 
+__device__ __forceinline__ int fdiv(int n, const WtDiv& f) {
+  return (int)((__umulhi((uint32_t)n, f.mul) + (uint32_t)n) >> f.shift);
+}
+
 // Elements per 16-byte global access.
 template <typename T> struct Vec16 { static constexpr int N = 16 / (int)sizeof(T); };
 
@@ -59,6 +63,25 @@ __device__ __forceinline__ void stg16(T* __restrict__ p, const float* v) {
     for (int e = 0; e < 8; ++e) h[e] = from_f32<T>(v[e]);
   }
   *reinterpret_cast<uint4*>(p) = u;
+}
+
+// Stores N consecutive outputs (rounded to T) with one N*sizeof(T)-byte
+// access when that is 8 or 16 bytes; dst must be aligned to that size.
+template <typename T, int N>
+__device__ __forceinline__ void stg_row(T* __restrict__ dst, const float* v) {
+  constexpr int BYTES = N * (int)sizeof(T);
+  if constexpr (BYTES == 16) {
+    stg16<T>(dst, v);
+  } else if constexpr (BYTES == 8) {
+    uint2 u;
+    T* h = reinterpret_cast<T*>(&u);
+#pragma unroll
+    for (int e = 0; e < N; ++e) h[e] = from_f32<T>(v[e]);
+    *reinterpret_cast<uint2*>(dst) = u;
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) dst[e] = from_f32<T>(v[e]);
+  }
 }
 
 // NV aligned float4 loads from shared memory.
@@ -115,6 +138,51 @@ __device__ __forceinline__ void conv_tile(const float* __restrict__ win, int str
   }
 }
 
+// seg[0..N) = p[OFF .. OFF+N) with the widest aligned shared loads; p is
+// 16-byte aligned and OFF, N are compile-time, so the pattern unrolls fully.
+template <int OFF, int N, int I = 0>
+__device__ __forceinline__ void lds_span(const float* p, float (&seg)[N]) {
+  if constexpr (I < N) {
+    constexpr int a = OFF + I;
+    if constexpr (a % 4 == 0 && I + 4 <= N) {
+      const float4 t = *reinterpret_cast<const float4*>(p + a);
+      seg[I] = t.x; seg[I + 1] = t.y; seg[I + 2] = t.z; seg[I + 3] = t.w;
+      lds_span<OFF, N, I + 4>(p, seg);
+    } else if constexpr (a % 2 == 0 && I + 2 <= N) {
+      const float2 t = *reinterpret_cast<const float2*>(p + a);
+      seg[I] = t.x; seg[I + 1] = t.y;
+      lds_span<OFF, N, I + 2>(p, seg);
+    } else {
+      seg[I] = p[a];
+      lds_span<OFF, N, I + 1>(p, seg);
+    }
+  }
+}
+
+// conv_tile for a window whose first column sits OFF floats after a 16-byte
+// boundary: reads exactly TC+K-1 floats per row.
+template <int K, int TR, int TC, int OFF>
+__device__ __forceinline__ void conv_tile_off(const float* __restrict__ row0, int stride,
+                                              const float* __restrict__ w, float (&acc)[TR][TC]) {
+  float wr[K * K];
+  load_weights<K>(w, wr);
+#pragma unroll
+  for (int a = 0; a < TR + K - 1; ++a) {
+    float seg[TC + K - 1];
+    lds_span<OFF, TC + K - 1>(row0 + a * stride, seg);
+#pragma unroll
+    for (int o = 0; o < TR; ++o) {
+      const int du = a - o;
+      if (du >= 0 && du < K) {
+#pragma unroll
+        for (int dv = 0; dv < K; ++dv)
+#pragma unroll
+          for (int j = 0; j < TC; ++j) acc[o][j] = fmaf(wr[du * K + dv], seg[j + dv], acc[o][j]);
+      }
+    }
+  }
+}
+
 // acc[du*K+dv] += sum_{o,j} d[o][j] * win[(o+du)*stride + j+dv]   (weight-gradient correlation)
 // Returns the sum of the d tile (for the bias gradient).
 template <int K, int TR, int TC>
@@ -156,19 +224,21 @@ __device__ __forceinline__ float corr_tile(const float* __restrict__ win, int ws
 // One Haar analysis level on the planes g < np of a CTA:
 //   dst_b[p][q] = sum_{u,v} sign_b(u,v) * src[2p+u][2q+v],  p < Hl, q < Wl
 // (unnormalised: the 1/2 per level is folded into the weights).  Reads past
-// the source interior hit its zero margin.
-__device__ __forceinline__ void haar_level(float* sm, int plane_floats, int np, const WtBuf S,
-                                           const WtBuf D, int Hl, int Wl, int tid, int nthreads) {
+// the source interior hit its zero margin.  Plane g's source buffer starts at
+// sbase + g*sps, its destination at dbase + g*dps.
+__device__ __forceinline__ void haar_level(const float* sbase, int sps, float* dbase, int dps, int np,
+                                           const WtBuf S, const WtBuf D, int Hl, int Wl, const WtDiv& dpp,
+                                           const WtDiv& dw, int tid, int nthreads) {
   const int per_plane = Hl * Wl;
   for (int it = tid; it < np * per_plane; it += nthreads) {
-    const int g = it / per_plane;
+    const int g = fdiv(it, dpp);
     const int rem = it - g * per_plane;
-    const int p = rem / Wl;
+    const int p = fdiv(rem, dw);
     const int q = rem - p * Wl;
-    const float* s = sm + g * plane_floats + S.off + (2 * p + S.pad) * S.stride + 2 * q + S.pad;
+    const float* s = sbase + g * sps + S.off + (2 * p + S.prow) * S.stride + 2 * q + S.pcol;
     const float a = s[0], b = s[1], c = s[S.stride], d = s[S.stride + 1];
     const float s0 = a + b, d0 = a - b, s1 = c + d, d1 = c - d;
-    float* o = sm + g * plane_floats + D.off + (p + D.pad) * D.stride + q + D.pad;
+    float* o = dbase + g * dps + D.off + (p + D.prow) * D.stride + q + D.pcol;
     o[0] = s0 + s1;           // low-pass
     o[D.band] = s0 - s1;      // row-high:    sign (-1)^u
     o[2 * D.band] = d0 + d1;  // column-high: sign (-1)^v
@@ -176,37 +246,159 @@ __device__ __forceinline__ void haar_level(float* sm, int plane_floats, int np, 
   }
 }
 
+// Haar levels 1 and 2 in one pass: each item reads a 4x4 block of the input
+// plane and writes the 2x2 level-1 positions of all four bands and the one
+// level-2 position built from their low-pass values (same unnormalised
+// butterflies as haar_level).  Items cover the level-2 grid H2 x W2; level-1
+// positions past H1 x W1 are skipped (they lie in the zero margin, and the
+// input rows/columns they read there are zero).
+__device__ __forceinline__ void butterfly4(float a, float b, float c, float d, float (&o)[4]) {
+  const float s0 = a + b, d0 = a - b, s1 = c + d, d1 = c - d;
+  o[0] = s0 + s1;
+  o[1] = s0 - s1;
+  o[2] = d0 + d1;
+  o[3] = d0 - d1;
+}
+
+__device__ __forceinline__ void haar_levels12(const float* sbase, int sps, float* dbase, int dps, int np,
+                                              const WtBuf S, const WtBuf D1, const WtBuf D2, int H1, int W1,
+                                              int H2, int W2, const WtDiv& dpp, const WtDiv& dw, int tid,
+                                              int nthreads) {
+  const int per_plane = H2 * W2;
+  for (int it = tid; it < np * per_plane; it += nthreads) {
+    const int g = fdiv(it, dpp);
+    const int rem = it - g * per_plane;
+    const int P = fdiv(rem, dw);
+    const int Q = rem - P * W2;
+    float* ps = dbase + g * dps;
+    const float* s = sbase + g * sps + S.off + (4 * P + S.prow) * S.stride + 4 * Q + S.pcol;
+    float x[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const float* r = s + a * S.stride;
+      if ((S.pcol & 3) == 0) {
+        const float4 t = *reinterpret_cast<const float4*>(r);
+        x[a][0] = t.x; x[a][1] = t.y; x[a][2] = t.z; x[a][3] = t.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[a][e] = r[e];
+      }
+    }
+    float ll[2][2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float o[2][4];
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        butterfly4(x[2 * u][2 * v], x[2 * u][2 * v + 1], x[2 * u + 1][2 * v], x[2 * u + 1][2 * v + 1], o[v]);
+        ll[u][v] = o[v][0];
+      }
+      const int p = 2 * P + u, q = 2 * Q;
+      if (p < H1) {
+        float* d = ps + D1.off + (p + D1.prow) * D1.stride + q + D1.pcol;
+        if (q + 1 < W1 && (D1.pcol & 1) == 0) {  // both columns valid, 8-byte aligned pair
+#pragma unroll
+          for (int b = 0; b < 4; ++b) *reinterpret_cast<float2*>(d + b * D1.band) = make_float2(o[0][b], o[1][b]);
+        } else {
+#pragma unroll
+          for (int v = 0; v < 2; ++v)
+            if (q + v < W1) {
+#pragma unroll
+              for (int b = 0; b < 4; ++b) d[b * D1.band + v] = o[v][b];
+            }
+        }
+      }
+    }
+    float o2[4];
+    butterfly4(ll[0][0], ll[0][1], ll[1][0], ll[1][1], o2);
+    float* d = ps + D2.off + (P + D2.prow) * D2.stride + Q + D2.pcol;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) d[b * D2.band] = o2[b];
+  }
+}
+
 // Copy planes n0 .. n0+np-1 of channel c from global memory into the
 // interiors of buffer B of each plane slot.
 template <typename T>
-__device__ __forceinline__ void load_planes(float* sm, int plane_floats, const WtBuf B,
+__device__ __forceinline__ void load_planes(float* dbase, int dps, const WtBuf B,
                                             const T* __restrict__ src, int n0, int np, int c, int C,
-                                            int H, int W, bool vec, int tid, int nthreads) {
+                                            int H, int W, bool vec, const WtDiv& dpp, const WtDiv& dw,
+                                            int tid, int nthreads) {
   const size_t HW = (size_t)H * W;
   if (vec) {
     constexpr int V = Vec16<T>::N;
     const int Wv = W / V;
     const int per_plane = H * Wv;
     for (int it = tid; it < np * per_plane; it += nthreads) {
-      const int g = it / per_plane;
+      const int g = fdiv(it, dpp);
       const int rem = it - g * per_plane;
-      const int i = rem / Wv;
+      const int i = fdiv(rem, dw);
       const int jv = rem - i * Wv;
       float v[V];
       ldg16<T>(src + ((size_t)(n0 + g) * C + c) * HW + (size_t)i * W + jv * V, v);
-      float* d = sm + g * plane_floats + B.off + (i + B.pad) * B.stride + jv * V + B.pad;
+      float* d = dbase + g * dps + B.off + (i + B.prow) * B.stride + jv * V + B.pcol;
+      if ((B.pcol & 3) == 0) {
 #pragma unroll
-      for (int e = 0; e < V; ++e) d[e] = v[e];
+        for (int e = 0; e < V; e += 4)
+          *reinterpret_cast<float4*>(d + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e) d[e] = v[e];
+      }
     }
   } else {
     const int per_plane = H * W;
     for (int it = tid; it < np * per_plane; it += nthreads) {
-      const int g = it / per_plane;
+      const int g = fdiv(it, dpp);
       const int rem = it - g * per_plane;
-      const int i = rem / W;
+      const int i = fdiv(rem, dw);
       const int j = rem - i * W;
       const float v = to_f32(src[((size_t)(n0 + g) * C + c) * HW + rem]);
-      sm[g * plane_floats + B.off + (i + B.pad) * B.stride + j + B.pad] = v;
+      dbase[g * dps + B.off + (i + B.prow) * B.stride + j + B.pcol] = v;
+    }
+  }
+}
+
+// Asynchronous copy of float32 planes n0 .. n0+np-1 of channel c into the
+// interiors of buffer B (cp.async: global -> shared without registers).
+// 16-byte copies when rows are 16-byte aligned in both spaces, else 4-byte.
+// The caller commits and waits (cp_async_wait_all) before a barrier.
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+__device__ __forceinline__ void load_planes_async(float* dbase, int dps, const WtBuf B,
+                                                  const float* __restrict__ src, int n0, int np, int c,
+                                                  int C, int H, int W, bool vec, const WtDiv& dpp,
+                                                  const WtDiv& dw, int tid, int nthreads) {
+  const size_t HW = (size_t)H * W;
+  if (vec && (B.pcol & 3) == 0) {
+    const int Wv = W >> 2;
+    const int per_plane = H * Wv;
+    for (int it = tid; it < np * per_plane; it += nthreads) {
+      const int g = fdiv(it, dpp);
+      const int rem = it - g * per_plane;
+      const int i = fdiv(rem, dw);
+      const int jv = rem - i * Wv;
+      cp_async16(dbase + g * dps + B.off + (i + B.prow) * B.stride + 4 * jv + B.pcol,
+                 src + ((size_t)(n0 + g) * C + c) * HW + (size_t)i * W + 4 * jv);
+    }
+  } else {
+    const int per_plane = H * W;
+    for (int it = tid; it < np * per_plane; it += nthreads) {
+      const int g = fdiv(it, dpp);
+      const int rem = it - g * per_plane;
+      const int i = fdiv(rem, dw);
+      const int j = rem - i * W;
+      cp_async4(dbase + g * dps + B.off + (i + B.prow) * B.stride + j + B.pcol,
+                src + ((size_t)(n0 + g) * C + c) * HW + rem);
     }
   }
 }

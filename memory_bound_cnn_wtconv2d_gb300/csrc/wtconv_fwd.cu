@@ -1,10 +1,10 @@
 // Fused WTConv2d forward pass and input-gradient pass (sm_103a).
 //
 // One CTA owns P planes of one channel.  The planes cross HBM once: they are
-// read into shared memory, the Haar pyramid is rebuilt there, every level is
-// convolved with scale-folded weights, and the synthesis of all levels is
-// summed tile by tile from the coarsest level down, so that the finest tiles
-// write the output straight from registers.
+// read into shared memory, the Haar pyramid is rebuilt there, every band of
+// every level is convolved with scale-folded weights, and the final tiles
+// add the base convolution and the synthesis of all levels in registers and
+// write the output directly.
 //
 // Paper: "Fast and Memory-Efficient Wavelet Convolutions via I/O-Aware
 // Reformulation" (arXiv 2608.10805), technical summary, "Methodology":
@@ -15,11 +15,12 @@
 //      sum_b sign_b(bit_{l-1}(i), bit_{l-1}(j)) * Z^l_b[i >> l][j >> l];
 //  (3) the per-channel scales are folded into the convolution weights (and
 //      the base scale into the bias).
-// Here (2) is evaluated in shared memory from level L to 2 as running sums
-// T^{l-1}[2p+u][2q+v] = sum_b sign_b(u,v) Z^l_b[p][q] + T^l[p][q] (the same
-// sum, grouped by coarse pixel), and level 1 adds it in registers.  The
-// 2^-l normalisations of analysis and synthesis (4^-l in total) are folded
-// into the level-l weights, so the butterflies are pure adds.
+// The 2^-l normalisations of analysis and synthesis (4^-l in total) are also
+// folded into the level-l weights, so every butterfly is a pure add.
+//
+// Phases per group of planes (one CTA barrier after each):
+//   load -> Haar levels 1+2 (fused) -> Haar levels 3..L -> band convolutions
+//   of all levels (Z buffers) -> final tiles (base conv + (2), stored to HBM).
 //
 // The input-gradient pass is the same kernel with every kernel rotated by
 // 180 degrees and no bias: the layer map is A = s_b*Conv_b + sum_l F_l^T K_l F_l
@@ -31,44 +32,26 @@
 
 namespace wt {
 
-// v[2o+u][2j+v] += sign_b(u, v) * z[o][j] for one band b.
-template <int TP, int TQ>
-__device__ __forceinline__ void add_band(float (&v)[2 * TP][2 * TQ], const float (&z)[TP][TQ], int b) {
-#pragma unroll
-  for (int o = 0; o < TP; ++o)
-#pragma unroll
-    for (int j = 0; j < TQ; ++j) {
-      const float zz = z[o][j];
-      v[2 * o][2 * j] += zz;
-      v[2 * o][2 * j + 1] += (b & 2) ? -zz : zz;             // sign (-1)^v for bands 2, 3
-      v[2 * o + 1][2 * j] += (b & 1) ? -zz : zz;             // sign (-1)^u for bands 1, 3
-      v[2 * o + 1][2 * j + 1] += (b == 1 || b == 2) ? -zz : zz;
-    }
+// Adds sum_b sign_b(u, v) * z_b to c[u][v] for the four parities (u, v).
+__device__ __forceinline__ void add_parities(float z0, float z1, float z2, float z3, float (&c)[2][2]) {
+  const float e0 = z0 + z1, e1 = z0 - z1, f0 = z2 + z3, f1 = z2 - z3;
+  c[0][0] += e0 + f0;  // (u, v) = (0, 0): all bands +
+  c[0][1] += e0 - f0;  // (0, 1): column-high and diagonal -
+  c[1][0] += e1 + f1;  // (1, 0): row-high and diagonal -
+  c[1][1] += e1 - f1;  // (1, 1): row-high and column-high -
 }
 
-template <int K, typename T, bool ROT>
-__global__ void __launch_bounds__(WT_FWD_THREADS)
-    fwd_kernel(const __grid_constant__ WtFwdPlan pl, const T* __restrict__ x,
-               const float* __restrict__ w_base, const float* __restrict__ b_base,
-               const float* __restrict__ w_sub, const float* __restrict__ s_base,
-               const float* __restrict__ s_w, T* __restrict__ y) {
-  extern __shared__ __align__(16) float sm[];
+// Stages the folded weights of channel c: band 0 = s_base*W_base, band
+// 1 + 4(l-1) + b = 4^-l * s_w * W_l,b (all rotated by 180 degrees for the
+// input gradient); the padding entries of each band are zero.
+template <int K, bool ROT>
+__device__ __forceinline__ void stage_weights(float* wsm, int wb, int L, int C, int c,
+                                              const float* __restrict__ w_base,
+                                              const float* __restrict__ w_sub,
+                                              const float* __restrict__ s_base,
+                                              const float* __restrict__ s_w, int tid, int nthreads) {
   constexpr int KK = K * K;
-  constexpr int NT = WT_FWD_THREADS;
-  constexpr int TP = WT_TP, TQ = WT_TQ;
-  const int tid = threadIdx.x;
-  const int C = pl.C, L = pl.L;
-  const int c = blockIdx.x % C;
-  const int n0 = (blockIdx.x / C) * pl.P;
-  const int np = min(pl.P, pl.N - n0);
-  const int PF = pl.plane_floats;
-
-  zero_smem(sm, pl.P * PF, tid, NT);
-
-  // (3) fold scales: base kernel * s_base; level-l kernels * s_w * 4^-l.
-  float* wsm = sm + pl.w_off;
-  const int wb = pl.w_band;
-  for (int i = tid; i < (1 + 4 * L) * wb; i += NT) {
+  for (int i = tid; i < (1 + 4 * L) * wb; i += nthreads) {
     const int band = i / wb;
     const int t = i - band * wb;
     float v = 0.f;
@@ -79,128 +62,208 @@ __global__ void __launch_bounds__(WT_FWD_THREADS)
       } else {
         const int l = (band - 1) >> 2, b = (band - 1) & 3;
         const int ch = l * 4 * C + 4 * c + b;
-        v = ldexpf(s_w[ch], -2 * (l + 1)) * w_sub[(size_t)ch * KK + ts];
+        const float norm = __int_as_float((127 - 2 * (l + 1)) << 23);  // 4^-(l+1), exact
+        v = norm * s_w[ch] * w_sub[(size_t)ch * KK + ts];
       }
     }
     wsm[i] = v;
   }
-  const float bias = (!ROT && b_base != nullptr) ? s_base[c] * b_base[c] : 0.f;
-  __syncthreads();
+}
 
-  load_planes<T>(sm, PF, pl.lev[0], x, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, tid, NT);
-  __syncthreads();
+// Persistent: CTA b owns the units [b*U/G, (b+1)*U/G) of the channel-major
+// unit list (unit = P planes of one channel), so consecutive units usually
+// share a channel and its folded weights.  Shared memory holds two sets of
+// input-plane buffers (the next unit's planes are prefetched with cp.async
+// while the current unit is computed, for float32), one work area per plane
+// (pyramid + convolved bands) and the weights.  It is zeroed once; later
+// writes touch interiors only, so every margin stays zero.
+template <int K, typename T, bool ROT>
+__global__ void __launch_bounds__(WT_FWD_THREADS, 3)
+    fwd_kernel(const __grid_constant__ WtFwdPlan pl, const T* __restrict__ x,
+               const float* __restrict__ w_base, const float* __restrict__ b_base,
+               const float* __restrict__ w_sub, const float* __restrict__ s_base,
+               const float* __restrict__ s_w, T* __restrict__ y) {
+  extern __shared__ __align__(16) float sm[];
+  constexpr int R = K / 2;
+  constexpr int NT = WT_FWD_THREADS;
+  constexpr int TP = WT_TP, TQ = WT_TQ, ZT = WT_ZT;
+  constexpr bool ASYNC = sizeof(T) == 4;
+  const int tid = threadIdx.x;
+  const int C = pl.C, L = pl.L;
+  const int XF = pl.xf, WF = pl.wf;
+  const long long units = (long long)C * pl.groups;
+  const int u_begin = (int)(units * blockIdx.x / gridDim.x);
+  const int u_end = (int)(units * (blockIdx.x + 1) / gridDim.x);
+  float* const wsm = sm + pl.w_off;
+  float* const work = sm + pl.work_off;
+  const int wb = pl.w_band;
 
-  // (1) Haar pyramid, levels 1..L, on chip.
-  for (int l = 1; l <= L; ++l) {
-    haar_level(sm, PF, np, pl.lev[l - 1], pl.lev[l], pl.Hs[l], pl.Ws[l], tid, NT);
+  zero_smem(sm, pl.w_off, tid, NT);
+  __syncthreads();  // the zero fill must land before any plane copy
+  int c_prev = -1;
+  int slot = 0;
+  for (int u = u_begin; u < u_end; ++u, slot ^= 1) {
+    const int c = u / pl.groups;
+    const int n0 = (u - c * pl.groups) * pl.P;
+    const int np = min(pl.P, pl.N - n0);
+    float* const xs = sm + slot * pl.P * XF;
+    if (c != c_prev) {
+      stage_weights<K, ROT>(wsm, wb, L, C, c, w_base, w_sub, s_base, s_w, tid, NT);
+      c_prev = c;
+    }
+    if (!ASYNC) {
+      load_planes<T>(xs, XF, pl.lev[0], x, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+    } else {
+      if (u == u_begin) {
+        load_planes_async(xs, XF, pl.lev[0], reinterpret_cast<const float*>(x), n0, np, c, C, pl.H, pl.W,
+                          pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+        cp_async_commit();
+        cp_async_wait_all();
+      }
+      if (u + 1 < u_end) {  // prefetch the next unit into the other buffer set
+        const int c1 = (u + 1) / pl.groups;
+        const int n1 = (u + 1 - c1 * pl.groups) * pl.P;
+        load_planes_async(sm + (slot ^ 1) * pl.P * XF, XF, pl.lev[0], reinterpret_cast<const float*>(x), n1,
+                          min(pl.P, pl.N - n1), c1, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+        cp_async_commit();
+      }
+    }
+    const float bias = (!ROT && b_base != nullptr) ? s_base[c] * b_base[c] : 0.f;
+    __syncthreads();  // planes of unit u and the weights are visible
+
+    // (1) Haar pyramid on chip.
+    if (L == 1) {
+      haar_level(xs, XF, work, WF, np, pl.lev[0], pl.lev[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
+    } else {
+      haar_levels12(xs, XF, work, WF, np, pl.lev[0], pl.lev[1], pl.lev[2], pl.Hs[1], pl.Ws[1], pl.Hs[2],
+                    pl.Ws[2], pl.an_pp[2], pl.an_w[2], tid, NT);
+    }
     __syncthreads();
-  }
+    for (int l = 3; l <= L; ++l) {
+      haar_level(work, WF, work, WF, np, pl.lev[l - 1], pl.lev[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l],
+                 tid, NT);
+      __syncthreads();
+    }
 
-  // (2) synthesis, coarse levels L..2 -> running sums T^{l-1}.
-  for (int l = L; l >= 2; --l) {
-    const WtBuf Yb = pl.lev[l];
-    const WtBuf Ti = pl.syn[l];      // read (l < L)
-    const WtBuf To = pl.syn[l - 1];  // write
-    const int tcn = pl.tc[l];
-    const int per_plane = pl.tr[l] * tcn;
-    const int Hd = pl.Hs[l - 1], Wd = pl.Ws[l - 1];
-    const float* wl = wsm + (1 + 4 * (l - 1)) * wb;
-    for (int it = tid; it < np * per_plane; it += NT) {
-      const int g = it / per_plane;
-      const int rem = it - g * per_plane;
-      const int tp = rem / tcn;
-      const int p0 = tp * TP, q0 = (rem - tp * tcn) * TQ;
-      float* ps = sm + g * PF;
-      float v[2 * TP][2 * TQ];
+    // Band convolutions of every level: Z^l_b = conv(Y^l_b, folded W_l,b), ZT x ZT tiles.
+    for (int it = tid; it < np * pl.zipp; it += NT) {
+      const int g = fdiv(it, pl.z_ipp);
+      const int local = it - g * pl.zipp;
+      int l = 1;
+      while (l < L && local >= pl.zbegin[l + 1]) ++l;
+      const int rel = local - pl.zbegin[l];
+      const int b = fdiv(rel, pl.z_tiles[l]);
+      const int t = rel - b * (pl.ztr[l] * pl.ztc[l]);
+      const int tp = fdiv(t, pl.z_tc[l]);
+      const int p0 = tp * ZT, q0 = (t - tp * pl.ztc[l]) * ZT;
+      float* ps = work + g * WF;
+      const WtBuf Yb = pl.lev[l];
+      float z[ZT][ZT];
 #pragma unroll
-      for (int o = 0; o < TP; ++o) {
-        float tv[TQ];
-        if (l < L) {
-          lds_row<TQ / 4>(ps + Ti.off + (p0 + o) * Ti.stride + q0, tv);
-        } else {
+      for (int o = 0; o < ZT; ++o)
 #pragma unroll
-          for (int j = 0; j < TQ; ++j) tv[j] = 0.f;
-        }
+        for (int j = 0; j < ZT; ++j) z[o][j] = 0.f;
+      conv_tile<K, ZT, ZT>(ps + Yb.off + b * Yb.band + p0 * Yb.stride + q0, Yb.stride,
+                           wsm + (1 + 4 * (l - 1) + b) * wb, z);
+      const WtBuf Zb = pl.zb[l];
+      float* dst = ps + Zb.off + b * Zb.band + p0 * Zb.stride + q0;
+      const int Hl = pl.Hs[l], Wl = pl.Ws[l];
+      if (p0 + ZT <= Hl && q0 + ZT <= Wl) {
 #pragma unroll
-        for (int j = 0; j < TQ; ++j) {
-          v[2 * o][2 * j] = tv[j];
-          v[2 * o][2 * j + 1] = tv[j];
-          v[2 * o + 1][2 * j] = tv[j];
-          v[2 * o + 1][2 * j + 1] = tv[j];
-        }
-      }
+        for (int o = 0; o < ZT; ++o)
+          *reinterpret_cast<float4*>(dst + o * Zb.stride) = make_float4(z[o][0], z[o][1], z[o][2], z[o][3]);
+      } else {
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        float z[TP][TQ];
+        for (int o = 0; o < ZT; ++o)
 #pragma unroll
-        for (int o = 0; o < TP; ++o)
-#pragma unroll
-          for (int j = 0; j < TQ; ++j) z[o][j] = 0.f;
-        conv_tile<K, TP, TQ>(ps + Yb.off + b * Yb.band + p0 * Yb.stride + q0, Yb.stride, wl + b * wb, z);
-        add_band<TP, TQ>(v, z, b);
-      }
-#pragma unroll
-      for (int oo = 0; oo < 2 * TP; ++oo) {
-        const int i = 2 * p0 + oo;
-        if (i < Hd) {
-          float* dst = ps + To.off + i * To.stride;
-#pragma unroll
-          for (int jj = 0; jj < 2 * TQ; ++jj)
-            if (2 * q0 + jj < Wd) dst[2 * q0 + jj] = v[oo][jj];
-        }
+          for (int j = 0; j < ZT; ++j)
+            if (p0 + o < Hl && q0 + j < Wl) dst[o * Zb.stride + j] = z[o][j];
       }
     }
     __syncthreads();
-  }
 
-  // Level 1 + base conv: outputs straight from registers.
-  {
+    // (2) final tiles: TP x TQ level-1 positions = 2TP x 2TQ outputs.
     const WtBuf X = pl.lev[0];
-    const WtBuf Y1 = pl.lev[1];
-    const WtBuf T1 = pl.syn[1];
-    const int tcn = pl.tc[1];
-    const int per_plane = pl.tr[1] * tcn;
     const int H = pl.H, W = pl.W;
     const size_t HW = (size_t)H * W;
-    const float* w1 = wsm + wb;
+    const int per_plane = pl.ftr * pl.ftc;
     for (int it = tid; it < np * per_plane; it += NT) {
-      const int g = it / per_plane;
+      const int g = fdiv(it, pl.f_pp);
       const int rem = it - g * per_plane;
-      const int tp = rem / tcn;
-      const int p0 = tp * TP, q0 = (rem - tp * tcn) * TQ;
-      const float* ps = sm + g * PF;
-      float v[2 * TP][2 * TQ];
+      const int tp = fdiv(rem, pl.f_c);
+      const int p0 = tp * TP, q0 = (rem - tp * pl.ftc) * TQ;
+      const float* ps = work + g * WF;
+      const float* px = xs + g * XF;
+
+      // Coarse levels 2..L, gathered per level-1 position (p0 + o, q0 + j):
+      // level l contributes the parity value (bit l-2 of p, bit l-2 of q) of
+      // its coefficients at (p >> (l-1), q >> (l-1)).
+      float cc[TP][TQ];
+#pragma unroll
+      for (int o = 0; o < TP; ++o)
+#pragma unroll
+        for (int j = 0; j < TQ; ++j) cc[o][j] = bias;
+      if (L >= 2) {
+        // level 2: rows p0/2 and p0/2 + 1, column q0/2; parity (o & 1, j)
+        const WtBuf Z2 = pl.zb[2];
+        const float* z2 = ps + Z2.off + (p0 >> 1) * Z2.stride + (q0 >> 1);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float* zk = z2 + k * Z2.stride;
+          float par[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+          add_parities(zk[0], zk[Z2.band], zk[2 * Z2.band], zk[3 * Z2.band], par);
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int j = 0; j < TQ; ++j) cc[2 * k + u][j] += par[u][j];
+        }
+      }
+      for (int l = 3; l <= L; ++l) {
+        // one coarse position per tile; column parity fixed, row parity from bit l-2 of p0 + o
+        const WtBuf Zl = pl.zb[l];
+        const float* zl = ps + Zl.off + (p0 >> (l - 1)) * Zl.stride + (q0 >> (l - 1));
+        float par[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        add_parities(zl[0], zl[Zl.band], zl[2 * Zl.band], zl[3 * Zl.band], par);
+        const int v = (q0 >> (l - 2)) & 1;
+#pragma unroll
+        for (int o = 0; o < TP; ++o) {
+          const int u = ((p0 + o) >> (l - 2)) & 1;
+          const float add = u ? (v ? par[1][1] : par[1][0]) : (v ? par[0][1] : par[0][0]);
+#pragma unroll
+          for (int j = 0; j < TQ; ++j) cc[o][j] += add;
+        }
+      }
+
+      // Level 1 per output parity, plus the coarse sum.
+      float out[2 * TP][2 * TQ];
+      const WtBuf Z1 = pl.zb[1];
 #pragma unroll
       for (int o = 0; o < TP; ++o) {
-        float tv[TQ];
-        if (L > 1) {
-          lds_row<TQ / 4>(ps + T1.off + (p0 + o) * T1.stride + q0, tv);
-        } else {
+        const float* z1 = ps + Z1.off + (p0 + o) * Z1.stride + q0;
+        float2 zr[4];
 #pragma unroll
-          for (int j = 0; j < TQ; ++j) tv[j] = 0.f;
-        }
+        for (int b = 0; b < 4; ++b) zr[b] = *reinterpret_cast<const float2*>(z1 + b * Z1.band);
 #pragma unroll
         for (int j = 0; j < TQ; ++j) {
-          v[2 * o][2 * j] = tv[j] + bias;
-          v[2 * o][2 * j + 1] = tv[j] + bias;
-          v[2 * o + 1][2 * j] = tv[j] + bias;
-          v[2 * o + 1][2 * j + 1] = tv[j] + bias;
+          float par[2][2] = {{cc[o][j], cc[o][j]}, {cc[o][j], cc[o][j]}};
+          if (j == 0) add_parities(zr[0].x, zr[1].x, zr[2].x, zr[3].x, par);
+          else add_parities(zr[0].y, zr[1].y, zr[2].y, zr[3].y, par);
+          out[2 * o][2 * j] = par[0][0];
+          out[2 * o][2 * j + 1] = par[0][1];
+          out[2 * o + 1][2 * j] = par[1][0];
+          out[2 * o + 1][2 * j + 1] = par[1][1];
         }
       }
-      conv_tile<K, 2 * TP, 2 * TQ>(ps + X.off + 2 * p0 * X.stride + 2 * q0, X.stride, wsm, v);
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        float z[TP][TQ];
-#pragma unroll
-        for (int o = 0; o < TP; ++o)
-#pragma unroll
-          for (int j = 0; j < TQ; ++j) z[o][j] = 0.f;
-        conv_tile<K, TP, TQ>(ps + Y1.off + b * Y1.band + p0 * Y1.stride + q0, Y1.stride, w1 + b * wb, z);
-        add_band<TP, TQ>(v, z, b);
-      }
+
+      // Base convolution from the input plane (interior column 0 sits 4 floats
+      // into each row, so the window starts 4 - r floats after a 16-byte boundary).
+      conv_tile_off<K, 2 * TP, 2 * TQ, 4 - R>(px + X.off + 2 * p0 * X.stride + 2 * q0, X.stride, wsm, out);
+
       T* plane = y + ((size_t)(n0 + g) * C + c) * HW;
       const int j0 = 2 * q0;
-      constexpr int V = Vec16<T>::N;
+      // One 2TQ-wide store per row: 16 bytes (float32) or 8 bytes (16-bit).
+      // Rows start on that boundary when vec_ok (W*sizeof(T) % 16 == 0, base
+      // 16-byte aligned) since j0*sizeof(T) = tile column * 2TQ*sizeof(T).
       const bool full_row = pl.vec_ok && (j0 + 2 * TQ <= W);
 #pragma unroll
       for (int oo = 0; oo < 2 * TP; ++oo) {
@@ -208,17 +271,18 @@ __global__ void __launch_bounds__(WT_FWD_THREADS)
         if (i < H) {
           T* dst = plane + (size_t)i * W + j0;
           if (full_row) {
-#pragma unroll
-            for (int s = 0; s < 2 * TQ; s += V) stg16<T>(dst + s, &v[oo][s]);
+            stg_row<T, 2 * TQ>(dst, out[oo]);
           } else {
 #pragma unroll
             for (int jj = 0; jj < 2 * TQ; ++jj)
-              if (j0 + jj < W) dst[jj] = from_f32<T>(v[oo][jj]);
+              if (j0 + jj < W) dst[jj] = from_f32<T>(out[oo][jj]);
           }
         }
       }
     }
-  }
+    if (ASYNC) cp_async_wait_all();  // this thread's copies of the next unit have landed
+    __syncthreads();                 // ... and all reads of unit u are done
+  }  // unit loop
 }
 
 template <int K, typename T, bool ROT>
@@ -228,7 +292,14 @@ static cudaError_t launch_fwd_t(const WtFwdPlan& pl, const void* x, const float*
   auto kern = fwd_kernel<K, T, ROT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)pl.C * (unsigned)pl.groups;
+  int per_sm = 0, dev = 0, sms = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, WT_FWD_THREADS, pl.smem_bytes);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long units = (long long)pl.C * pl.groups;
+  long long slots = (long long)(per_sm < 1 ? 1 : per_sm) * sms;
+  const unsigned grid = (unsigned)(units < slots ? units : slots);
   kern<<<grid, WT_FWD_THREADS, pl.smem_bytes, stream>>>(pl, static_cast<const T*>(x), w_base, b_base,
                                                         w_sub, s_base, s_w, static_cast<T*>(y));
   return cudaGetLastError();

@@ -11,34 +11,56 @@
 
 #define WT_MAXL 8  // largest number of decomposition levels
 
+// Division by a launch-constant divisor d without a hardware divide:
+// q = (umulhi(n, mul) + n) >> shift with shift = ceil(log2 d) and
+// mul = floor(2^32 (2^shift - d) / d) + 1 (Granlund & Montgomery, "Division
+// by invariant integers using multiplication", PLDI 1994).  Exact for
+// 0 <= n < 2^24, which bounds every index it is used on.
+struct WtDiv {
+  uint32_t mul;
+  uint32_t shift;
+};
+
 // A shared-memory plane buffer (float32).  The interior element (i, j) of
-// band b lives at  off + b*band + (i + pad)*stride + (j + pad).  Everything
-// outside the interior (halo, tile-rounding margin) holds zeros.
+// band b lives at  off + b*band + (i + prow)*stride + (j + pcol).
+// Everything outside the interior (halo, tile-rounding margin) holds zeros.
 struct WtBuf {
   int off;     // floats from the start of the plane slot
   int stride;  // floats per row, a multiple of 4
-  int pad;     // zero rows/columns before the interior
+  int prow;    // zero rows above the interior
+  int pcol;    // zero columns left of the interior
   int band;    // floats between consecutive bands
 };
 
 // Forward / input-gradient pass.  One CTA owns P planes of one channel c
-// (n = gi*P .. gi*P+P-1) and runs: load -> Haar analysis levels 1..L ->
-// synthesis tiles from level L down to 1 -> store.
+// (n = gi*P .. gi*P+P-1) and runs: load -> Haar analysis (levels 1 and 2
+// fused, then 3..L) -> band convolutions of every level into Z buffers ->
+// final tiles (base conv + bit-indexed synthesis) -> store.
 struct WtFwdPlan {
   int N, C, H, W, L, K;
   int P;                 // planes per CTA
   int groups;            // ceil(N / P); grid = C * groups
   int Hs[WT_MAXL + 1];   // level sizes, Hs[0] = H, Hs[l] = ceil(Hs[l-1] / 2)
   int Ws[WT_MAXL + 1];
-  int tr[WT_MAXL + 1];   // tile rows / columns at level l >= 1 (tiles of TP x TQ)
-  int tc[WT_MAXL + 1];
-  WtBuf lev[WT_MAXL + 1];  // lev[0] = input plane, lev[l] = 4 coefficient bands of level l
-  WtBuf syn[WT_MAXL + 1];  // syn[l] (1 <= l < L): coarse synthesis sum T^l (pad 0, 1 band)
-  int plane_floats;      // floats per plane slot
-  int w_off;             // folded weights, after the P plane slots
+  WtBuf lev[WT_MAXL + 1];  // lev[0] = input plane (pcol 4), lev[l] = 4 coefficient bands (pad r)
+  WtBuf zb[WT_MAXL + 1];   // zb[l]: the 4 convolved, scale-folded bands of level l (pad 0)
+  int ztr[WT_MAXL + 1];    // band-convolution tiles (WT_ZT x WT_ZT) per level: rows, columns
+  int ztc[WT_MAXL + 1];
+  int zbegin[WT_MAXL + 2];  // first (band, tile) item of level l within a plane; [L+1] = total
+  int zipp;                 // band-convolution items per plane
+  int ftr, ftc;             // final tiles (WT_TP x WT_TQ level-1 positions) per plane: rows, columns
+  int xf;                // floats per input-plane buffer (2P of them: two buffer sets)
+  int wf;                // floats per work area (pyramid + convolved bands; P of them)
+  int work_off;          // = 2 * P * xf
+  int w_off;             // folded weights, after the work areas
   int w_band;            // floats per folded kernel (k*k rounded up to 4)
   int smem_bytes;
   int vec_ok;            // rows can use 16-byte global accesses (W % elems-per-16B == 0)
+  WtDiv ld_pp, ld_w;     // plane load: items per plane, items per row
+  WtDiv an_pp[WT_MAXL + 1], an_w[WT_MAXL + 1];  // analysis at level l (l = 2: the fused 1+2 pass)
+  WtDiv z_ipp;                                  // band-convolution items per plane
+  WtDiv z_tiles[WT_MAXL + 1], z_tc[WT_MAXL + 1];  // ztr*ztc and ztc per level
+  WtDiv f_pp, f_c;                              // final tiles per plane, per row
 };
 
 // Parameter-gradient pass.  One CTA owns channel c and the planes
@@ -62,11 +84,16 @@ struct WtBwPlan {
   int nbands;            // 1 + 4L
   int part_stride;       // floats per (group, channel) partial record = nbands*(k*k+1)
   int vec_ok;
+  WtDiv ld_pp, ld_w;
+  WtDiv an_pp[WT_MAXL + 1], an_w[WT_MAXL + 1];
+  WtDiv ipp;                                   // items per plane
+  WtDiv tiles[WT_MAXL + 1], tcd[WT_MAXL + 1];  // tr*tc and tc per level
 };
 
 #define WT_FWD_THREADS 128
 #define WT_BW_THREADS 256
 #define WT_BW_MAX_ITEMS 2  // tile items per thread in the parameter-gradient pass
-#define WT_TP 2            // forward tile: TP x TQ coefficient positions per level
-#define WT_TQ 4
+#define WT_TP 4            // final tile: TP x TQ level-1 positions = 2TP x 2TQ outputs
+#define WT_TQ 2
+#define WT_ZT 4            // band-convolution tile: ZT x ZT coefficient positions
 #define WT_BT 4            // parameter-gradient tile: WT_BT x WT_BT positions
