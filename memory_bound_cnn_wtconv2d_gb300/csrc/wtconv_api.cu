@@ -152,37 +152,60 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   return WTCONV_OK;
 }
 
+// Tile grid and item list of the parameter-gradient pass for tbr-row tiles.
+void bw_tiles(const wtconv_desc_t* d, WtBwPlan& pl, int tbr) {
+  pl.tbr = tbr;
+  pl.tcw = 4;
+  pl.item_begin[0] = 0;
+  for (int l = 0; l <= d->levels; ++l) {
+    pl.tr[l] = ceil_div(pl.Hs[l], tbr);
+    pl.tc[l] = ceil_div(pl.Ws[l], 4);
+    pl.item_begin[l + 1] = pl.item_begin[l] + (l == 0 ? 1 : 4) * pl.tr[l] * pl.tc[l];
+  }
+}
+
 wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
   memset(&pl, 0, sizeof(pl));
   pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
   const int R = d->k / 2, L = d->levels, KK = d->k * d->k;
   level_sizes(d, pl.Hs, pl.Ws);
-  int off = 0;
-  pl.item_begin[0] = 0;
-  for (int l = 0; l <= L; ++l) {
-    pl.tr[l] = ceil_div(pl.Hs[l], WT_BT);
-    pl.tc[l] = ceil_div(pl.Ws[l], WT_BT);
-    const int nb = l == 0 ? 1 : 4;
-    off = place(pl.xs[l], off, pl.tr[l] * WT_BT, pl.tc[l] * WT_BT, R, R, nb);
-    off = place(pl.ds[l], off, pl.tr[l] * WT_BT, pl.tc[l] * WT_BT, 0, 0, nb);
-    pl.item_begin[l + 1] = pl.item_begin[l] + nb * pl.tr[l] * pl.tc[l];
+  // 8x4 tiles (one per thread) when a plane's tiles fit in one CTA and waste
+  // no more FMAs than 4x4 tiles would; otherwise 4x4 tiles (two per thread).
+  long useful = 0;
+  for (int l = 0; l <= L; ++l) useful += (long)(l == 0 ? 1 : 4) * pl.Hs[l] * pl.Ws[l];
+  bw_tiles(d, pl, 4);
+  const long work4 = 16L * pl.item_begin[L + 1];
+  bw_tiles(d, pl, 8);
+  const long work8 = 32L * pl.item_begin[L + 1];
+  if (pl.item_begin[L + 1] > WT_BW_THREADS || work8 > work4 + useful / 8) bw_tiles(d, pl, 4);
+  // Input slot: raw x (r-wide zero margin: the correlation windows shift it)
+  // and raw dy (no margin); the fused level-1/2 analysis reads them up to
+  // row/column 4*ceil(H2) - 1, which the tile-rounded extents cover.
+  int off = place(pl.xs[0], 0, pl.tbr * pl.tr[0], pl.tcw * pl.tc[0], R, R, 1);
+  off = place(pl.ds[0], off, pl.tbr * pl.tr[0], pl.tcw * pl.tc[0], 0, 0, 1);
+  pl.isf = round_up(off, 4);
+  off = 0;
+  for (int l = 1; l <= L; ++l) {
+    off = place(pl.xs[l], off, pl.tbr * pl.tr[l], pl.tcw * pl.tc[l], R, R, 4);
+    off = place(pl.ds[l], off, pl.tbr * pl.tr[l], pl.tcw * pl.tc[l], 0, 0, 4);
   }
+  pl.wf = round_up(off, 4);
   pl.items_per_plane = pl.item_begin[L + 1];
-  pl.plane_floats = round_up(off, 4);
   pl.nbands = 1 + 4 * L;
   pl.part_stride = pl.nbands * (KK + 1);
-  const int slots = WT_BW_MAX_ITEMS * WT_BW_THREADS;
+  const int slots = (pl.tbr == 8 ? 1 : WT_BW_MAX_ITEMS) * WT_BW_THREADS;
   if (pl.items_per_plane > slots)
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d has %d gradient tiles (max %d per CTA)", d->H, d->W,
                 pl.items_per_plane, slots);
-  const long plane_bytes = 4L * pl.plane_floats;
+  const long plane_bytes = 4L * (2 * pl.isf + pl.wf);
   int P = slots / pl.items_per_plane;
   const int fit = (int)(kBwBudget / plane_bytes);
   if (P > fit) P = fit < 1 ? 1 : fit;
   if (d->N > 0 && P > d->N) P = d->N;
   if (P < 1) P = 1;
   pl.P = P;
-  long smem = plane_bytes * P;
+  pl.work_off = 2 * P * pl.isf;
+  long smem = 4L * (pl.work_off + (long)P * pl.wf);
   const long red = 4L * P * pl.items_per_plane * (KK + 1);
   if (red > smem) smem = red;
   if (smem > kMaxSmemPerBlock)
@@ -194,6 +217,10 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
     pl.an_w[l] = make_div(pl.Ws[l]);
     pl.tiles[l] = make_div(pl.tr[l] * pl.tc[l]);
     pl.tcd[l] = make_div(pl.tc[l]);
+  }
+  if (L >= 2) {  // the fused level-1/2 pass walks the level-2 grid
+    pl.an_pp[2] = make_div(pl.Hs[2] * pl.Ws[2]);
+    pl.an_w[2] = make_div(pl.Ws[2]);
   }
   pl.ipp = make_div(pl.items_per_plane);
   // One wave of (channel, chunk) CTAs when the channels allow it.  Resident

@@ -28,25 +28,33 @@
 
 namespace wt {
 
-template <int K, typename T>
+// TR = 8: 8x4 tiles, one per thread; TR = 4: 4x4 tiles, up to two per thread.
+// Tiles are 4 columns wide so neighbouring lanes read neighbouring 16-byte
+// chunks of a row (no shared-memory bank conflicts within a row).
+template <int K, typename T, int TR>
 __global__ void __launch_bounds__(WT_BW_THREADS)
     bw_kernel(const __grid_constant__ WtBwPlan pl, const T* __restrict__ x, const T* __restrict__ dy,
               float* __restrict__ part) {
   extern __shared__ __align__(16) float sm[];
   constexpr int KK = K * K;
   constexpr int NT = WT_BW_THREADS;
-  constexpr int MI = WT_BW_MAX_ITEMS;
-  constexpr int BT = WT_BT;
+  constexpr int MI = TR == 8 ? 1 : WT_BW_MAX_ITEMS;
+  constexpr int TC = 4;
+  constexpr bool ASYNC = sizeof(T) == 4;
   const int tid = threadIdx.x;
   const int C = pl.C, L = pl.L;
   const int c = blockIdx.x % C;
   const int gi = blockIdx.x / C;
   const int n_begin = gi * pl.chunk;
   const int n_end = min(pl.N, n_begin + pl.chunk);
-  const int PF = pl.plane_floats;
+  const int ISF = pl.isf, WF = pl.wf;
   const int ipp = pl.items_per_plane;
+  float* const work = sm + pl.work_off;
+  const float* const xf = reinterpret_cast<const float*>(x);
+  const float* const dyf = reinterpret_cast<const float*>(dy);
 
-  zero_smem(sm, pl.P * PF, tid, NT);
+  // Zeroed once: interiors are rewritten per batch, margins stay zero.
+  zero_smem(sm, pl.work_off + pl.P * WF, tid, NT);
 
   float acc[MI][KK];
   float gs[MI];
@@ -58,14 +66,43 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
   }
   __syncthreads();
 
-  for (int nb = n_begin; nb < n_end; nb += pl.P) {
+  if (ASYNC && n_begin < n_end) {  // first batch
+    const int np0 = min(pl.P, n_end - n_begin);
+    load_planes_async(sm, ISF, pl.xs[0], xf, n_begin, np0, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+    load_planes_async(sm, ISF, pl.ds[0], dyf, n_begin, np0, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+    cp_async_commit();
+    cp_async_wait_all();
+  }
+  int slot = 0;
+  for (int nb = n_begin; nb < n_end; nb += pl.P, slot ^= 1) {
     const int np = min(pl.P, n_end - nb);
-    load_planes<T>(sm, PF, pl.xs[0], x, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-    load_planes<T>(sm, PF, pl.ds[0], dy, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+    float* const in = sm + slot * pl.P * ISF;  // this batch's raw x / dy planes
+    if (!ASYNC) {
+      load_planes<T>(in, ISF, pl.xs[0], x, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+      load_planes<T>(in, ISF, pl.ds[0], dy, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+    } else if (nb + pl.P < n_end) {  // prefetch the next batch into the other slot set
+      const int n1 = nb + pl.P, np1 = min(pl.P, n_end - n1);
+      float* const nxt = sm + (slot ^ 1) * pl.P * ISF;
+      load_planes_async(nxt, ISF, pl.xs[0], xf, n1, np1, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+      load_planes_async(nxt, ISF, pl.ds[0], dyf, n1, np1, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+      cp_async_commit();
+    }
+    __syncthreads();  // this batch's planes are visible
+
+    // Both pyramids: levels 1+2 fused, then 3..L.
+    if (L == 1) {
+      haar_level(in, ISF, work, WF, np, pl.xs[0], pl.xs[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
+      haar_level(in, ISF, work, WF, np, pl.ds[0], pl.ds[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
+    } else {
+      haar_levels12(in, ISF, work, WF, np, pl.xs[0], pl.xs[1], pl.xs[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
+                    pl.an_pp[2], pl.an_w[2], tid, NT);
+      haar_levels12(in, ISF, work, WF, np, pl.ds[0], pl.ds[1], pl.ds[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
+                    pl.an_pp[2], pl.an_w[2], tid, NT);
+    }
     __syncthreads();
-    for (int l = 1; l <= L; ++l) {
-      haar_level(sm, PF, sm, PF, np, pl.xs[l - 1], pl.xs[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
-      haar_level(sm, PF, sm, PF, np, pl.ds[l - 1], pl.ds[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
+    for (int l = 3; l <= L; ++l) {
+      haar_level(work, WF, work, WF, np, pl.xs[l - 1], pl.xs[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
+      haar_level(work, WF, work, WF, np, pl.ds[l - 1], pl.ds[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
       __syncthreads();
     }
 #pragma unroll
@@ -82,17 +119,18 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
           const int b = fdiv(rel, pl.tiles[l]);
           const int t = rel - b * tiles;
           const int tp = fdiv(t, pl.tcd[l]);
-          const int p0 = tp * BT, q0 = (t - tp * pl.tc[l]) * BT;
+          const int p0 = tp * TR, q0 = (t - tp * pl.tc[l]) * TC;
           const WtBuf Xb = pl.xs[l], Db = pl.ds[l];
-          const float* ps = sm + g * PF;
-          const float dsum =
-              corr_tile<K, BT, BT>(ps + Xb.off + b * Xb.band + p0 * Xb.stride + q0, Xb.stride,
-                                   ps + Db.off + b * Db.band + p0 * Db.stride + q0, Db.stride, acc[s]);
+          const float* ps = (l == 0) ? in + g * ISF : work + g * WF;
+          const float* xw = ps + Xb.off + b * Xb.band + p0 * Xb.stride + q0;
+          const float* dw = ps + Db.off + b * Db.band + p0 * Db.stride + q0;
+          const float dsum = corr_tile<K, TR, TC>(xw, Xb.stride, dw, Db.stride, acc[s]);
           if (l == 0) gs[s] += dsum;
         }
       }
     }
-    __syncthreads();
+    if (ASYNC) cp_async_wait_all();  // this thread's copies of the next batch have landed
+    __syncthreads();                 // ... and every read of this batch is done
   }
 
   // Tile sums -> shared memory -> one record per band.
@@ -184,7 +222,7 @@ __global__ void bw_finalize_kernel(const __grid_constant__ WtBwPlan pl, const fl
 template <int K, typename T>
 static cudaError_t launch_bw_t(const WtBwPlan& pl, const void* x, const void* dy, float* part,
                                cudaStream_t stream) {
-  auto kern = bw_kernel<K, T>;
+  auto kern = pl.tbr == 8 ? bw_kernel<K, T, 8> : bw_kernel<K, T, 4>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)pl.C * (unsigned)pl.groups;

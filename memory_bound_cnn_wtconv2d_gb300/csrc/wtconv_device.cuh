@@ -374,21 +374,39 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
+__device__ __forceinline__ void cp_async8(float* dst, const float* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(src) : "memory");
+}
+
+// Copies with the widest granule G (4, 2 or 1 floats) that keeps both sides
+// aligned: G = 4 needs 16-byte aligned rows in global memory (vec) and a
+// buffer margin that is a multiple of 4 floats; G = 2 a margin that is even.
 __device__ __forceinline__ void load_planes_async(float* dbase, int dps, const WtBuf B,
                                                   const float* __restrict__ src, int n0, int np, int c,
                                                   int C, int H, int W, bool vec, const WtDiv& dpp,
                                                   const WtDiv& dw, int tid, int nthreads) {
   const size_t HW = (size_t)H * W;
-  if (vec && (B.pcol & 3) == 0) {
+  if (vec) {  // W % 4 == 0 and 16-byte aligned rows: items are 4-float groups
     const int Wv = W >> 2;
     const int per_plane = H * Wv;
+    const bool g4 = (B.pcol & 3) == 0, g2 = (B.pcol & 1) == 0;
     for (int it = tid; it < np * per_plane; it += nthreads) {
       const int g = fdiv(it, dpp);
       const int rem = it - g * per_plane;
       const int i = fdiv(rem, dw);
       const int jv = rem - i * Wv;
-      cp_async16(dbase + g * dps + B.off + (i + B.prow) * B.stride + 4 * jv + B.pcol,
-                 src + ((size_t)(n0 + g) * C + c) * HW + (size_t)i * W + 4 * jv);
+      float* d = dbase + g * dps + B.off + (i + B.prow) * B.stride + 4 * jv + B.pcol;
+      const float* sp = src + ((size_t)(n0 + g) * C + c) * HW + (size_t)i * W + 4 * jv;
+      if (g4) {
+        cp_async16(d, sp);
+      } else if (g2) {
+        cp_async8(d, sp);
+        cp_async8(d + 2, sp + 2);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cp_async4(d + e, sp + e);
+      }
     }
   } else {
     const int per_plane = H * W;

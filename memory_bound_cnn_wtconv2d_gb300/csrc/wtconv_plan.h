@@ -64,7 +64,9 @@ struct WtFwdPlan {
 };
 
 // Parameter-gradient pass.  One CTA owns channel c and the planes
-// n in [gi*chunk, min(N, (gi+1)*chunk)), P at a time.  "Bands" B number the
+// n in [gi*chunk, min(N, (gi+1)*chunk)), P at a time (the next P are
+// prefetched into a second set of input slots while the current ones are
+// correlated).  "Bands" B number the
 // correlations: B = 0 base path, B = 1 + 4*(l-1) + b for level l, band b.
 struct WtBwPlan {
   int N, C, H, W, L, K;
@@ -73,13 +75,17 @@ struct WtBwPlan {
   int groups;            // ceil(N / chunk); grid = C * groups
   int Hs[WT_MAXL + 1];
   int Ws[WT_MAXL + 1];
-  int tr[WT_MAXL + 1];   // 4x4-tile rows / columns per level (level 0 = base path)
+  int tbr;               // tile rows: 8 (one tile per thread) or 4 (up to two per thread)
+  int tcw;               // tile columns: 4
+  int tr[WT_MAXL + 1];   // tbr x tcw tiles per level (level 0 = base path): rows, columns
   int tc[WT_MAXL + 1];
   int item_begin[WT_MAXL + 2];  // first tile item of level l within a plane (l = 0..L), [L+1] = total
   int items_per_plane;
-  WtBuf xs[WT_MAXL + 1];  // shifted operand: x (l = 0) and its level-l bands, pad = r
-  WtBuf ds[WT_MAXL + 1];  // unshifted operand: dy (l = 0) and its level-l bands, pad = 0
-  int plane_floats;
+  WtBuf xs[WT_MAXL + 1];  // shifted operand: x (l = 0, in an input slot) and its level-l bands, pad = r
+  WtBuf ds[WT_MAXL + 1];  // unshifted operand: dy (l = 0, in an input slot) and its level-l bands, pad = 0
+  int isf;               // floats per input slot (raw x and dy planes; 2P slots: two sets)
+  int wf;                // floats per work area (both pyramids; P of them)
+  int work_off;          // = 2 * P * isf
   int smem_bytes;
   int nbands;            // 1 + 4L
   int part_stride;       // floats per (group, channel) partial record = nbands*(k*k+1)
