@@ -152,6 +152,14 @@ const char* wtconv_status_string(wtconv_status_t status);
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* wtconv_last_error(void);
 
+/* Number of in-kernel waits on the current device that gave up since the
+ * previous call, then resets the count.  The kernels wait for their own
+ * asynchronous (TMA) plane copies with a time limit of about a second; a
+ * wait that runs out records itself here and the kernel stops early (its
+ * outputs are then invalid).  0 in normal operation.  Synchronises the
+ * current device. */
+unsigned int wtconv_device_faults(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,11 +1,14 @@
 // C ABI of libwtconv: argument validation, launch planning, dispatch.
 // The declarations and the contract of every entry point are in
 // include/wtconv.h.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "../../include/wtconv.h"
 #include "wtconv_launch.h"
@@ -116,7 +119,7 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   pl.wf = round_up(off, 4);
   pl.w_band = round_up(KK, 4);
   const int wfloats = (1 + 4 * L) * pl.w_band;
-  const long plane_bytes = 4L * (2 * pl.xf + pl.wf);
+  const long plane_bytes = 4L * (2 * pl.xf + pl.wf) + 256;
   if (plane_bytes + 4L * wfloats > kMaxSmemPerBlock)
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %ld B of shared memory (max %d)",
                 d->H, d->W, L, plane_bytes + 4L * wfloats, kMaxSmemPerBlock);
@@ -128,9 +131,15 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   if (d->N > 0 && P > d->N) P = d->N;
   pl.P = P;
   pl.groups = d->N > 0 ? ceil_div(d->N, P) : 0;
-  pl.work_off = 2 * P * pl.xf;
+  pl.xslot = round_up(P * pl.xf, 32);  // 128-byte aligned buffer sets (TMA destinations)
+  pl.work_off = 2 * pl.xslot;
   pl.w_off = pl.work_off + P * pl.wf;
-  pl.smem_bytes = 4 * (pl.w_off + wfloats);
+  pl.mb_off = round_up(pl.w_off + wfloats, 2);
+  pl.smem_bytes = 4 * pl.mb_off + 16 + WT_SMEM_SLACK;
+  if (pl.smem_bytes > kMaxSmemPerBlock)
+    return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %d B of shared memory (max %d)",
+                d->H, d->W, L, pl.smem_bytes, kMaxSmemPerBlock);
+  pl.tma_bytes = (uint32_t)(4L * P * pl.xf);
   if (L == 1) {
     pl.an_pp[1] = make_div(pl.Hs[1] * pl.Ws[1]);
     pl.an_w[1] = make_div(pl.Ws[1]);
@@ -178,13 +187,14 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
   bw_tiles(d, pl, 8);
   const long work8 = 32L * pl.item_begin[L + 1];
   if (pl.item_begin[L + 1] > WT_BW_THREADS || work8 > work4 + useful / 8) bw_tiles(d, pl, 4);
-  // Input slot: raw x (r-wide zero margin: the correlation windows shift it)
-  // and raw dy (no margin); the fused level-1/2 analysis reads them up to
-  // row/column 4*ceil(H2) - 1, which the tile-rounded extents cover.
-  int off = place(pl.xs[0], 0, pl.tbr * pl.tr[0], pl.tcw * pl.tc[0], R, R, 1);
-  off = place(pl.ds[0], off, pl.tbr * pl.tr[0], pl.tcw * pl.tc[0], 0, 0, 1);
-  pl.isf = round_up(off, 4);
-  off = 0;
+  // Input set: P raw x planes (r zero rows above and below, a 4-float zero
+  // margin left and right so rows start 16-byte aligned; the correlation
+  // windows read up to r columns beyond the interior) and P raw dy planes (no
+  // margin).  The fused level-1/2 analysis reads both up to row/column
+  // 4*ceil(H2) - 1, which the tile-rounded extents cover.
+  pl.xbf = place(pl.xs[0], 0, pl.tbr * pl.tr[0], pl.tcw * pl.tc[0], R, 4, 1);
+  pl.dbf = place(pl.ds[0], 0, pl.tbr * pl.tr[0], pl.tcw * pl.tc[0], 0, 0, 1);
+  int off = 0;
   for (int l = 1; l <= L; ++l) {
     off = place(pl.xs[l], off, pl.tbr * pl.tr[l], pl.tcw * pl.tc[l], R, R, 4);
     off = place(pl.ds[l], off, pl.tbr * pl.tr[l], pl.tcw * pl.tc[l], 0, 0, 4);
@@ -197,21 +207,26 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
   if (pl.items_per_plane > slots)
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d has %d gradient tiles (max %d per CTA)", d->H, d->W,
                 pl.items_per_plane, slots);
-  const long plane_bytes = 4L * (2 * pl.isf + pl.wf);
+  const long plane_bytes = 4L * (2 * (pl.xbf + pl.dbf) + pl.wf) + 256;
   int P = slots / pl.items_per_plane;
   const int fit = (int)(kBwBudget / plane_bytes);
   if (P > fit) P = fit < 1 ? 1 : fit;
   if (d->N > 0 && P > d->N) P = d->N;
   if (P < 1) P = 1;
   pl.P = P;
-  pl.work_off = 2 * P * pl.isf;
-  long smem = 4L * (pl.work_off + (long)P * pl.wf);
-  const long red = 4L * P * pl.items_per_plane * (KK + 1);
-  if (red > smem) smem = red;
+  pl.xr = round_up(P * pl.xbf, 32);  // 128-byte aligned TMA destinations
+  pl.islot = pl.xr + round_up(P * pl.dbf, 32);
+  pl.work_off = 2 * pl.islot;
+  long floats = pl.work_off + (long)P * pl.wf;
+  const long red = (long)P * pl.items_per_plane * (KK + 1);  // end-of-CTA reduction (aliases the inputs)
+  if (red > floats) floats = red;
+  pl.mb_off = (int)round_up(floats, 2);
+  const long smem = 4L * pl.mb_off + 16 + WT_SMEM_SLACK;
   if (smem > kMaxSmemPerBlock)
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %ld B of shared memory (max %d)",
                 d->H, d->W, L, smem, kMaxSmemPerBlock);
   pl.smem_bytes = (int)smem;
+  pl.tma_bytes = (uint32_t)(4L * P * (pl.xbf + pl.dbf));
   for (int l = 0; l <= L; ++l) {
     pl.an_pp[l] = make_div(pl.Hs[l] * pl.Ws[l]);
     pl.an_w[l] = make_div(pl.Ws[l]);
@@ -241,6 +256,44 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
 }
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime so the
+// library does not link libcuda directly.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Tensor map over a float32 NCHW tensor, dimensions (W, H, C, N) innermost
+// first, with box (box_w, box_h, 1, P): one box is P planes of one channel
+// with a margin, landing in shared memory as P consecutive padded planes.
+// Out-of-range elements read as zero.  Returns false if TMA cannot be used.
+bool encode_plane_map(CUtensorMap* m, const void* base, const wtconv_desc_t* d, int box_w, int box_h, int P) {
+  if (d->dtype != WTCONV_F32 || (d->W % 4) != 0 || !aligned(base, 16)) return false;
+  if (box_w > 256 || box_h > 256 || P > 256 || (box_w % 4) != 0) return false;
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)d->W, (cuuint64_t)d->H, (cuuint64_t)d->C, (cuuint64_t)d->N};
+  const cuuint64_t strides[3] = {4ull * d->W, 4ull * d->W * d->H, 4ull * d->W * d->H * d->C};
+  const cuuint32_t box[4] = {(cuuint32_t)box_w, (cuuint32_t)box_h, 1u, (cuuint32_t)P};
+  const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 wtconv_status_t check_act(const void* p, const char* name, const wtconv_desc_t* d) {
   if (!p) return fail(WTCONV_ERR_INVALID_ARG, "%s is NULL", name);
@@ -314,7 +367,10 @@ wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float
   WT_TRY(check_act(x, "x", desc));
   WT_TRY(check_act(y, "y", desc));
   set_load_divs(pl, desc, vec_ok(desc, x, y));
-  cudaError_t e = wt::launch_fwd(pl, desc->dtype, false, x, w_base, b_base, w_sub, base_scale,
+  alignas(64) CUtensorMap tmx;
+  memset(&tmx, 0, sizeof(tmx));
+  pl.use_tma = encode_plane_map(&tmx, x, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
+  cudaError_t e = wt::launch_fwd(pl, tmx, desc->dtype, false, x, w_base, b_base, w_sub, base_scale,
                                  wavelet_scale, y, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_fwd: %s", cudaGetErrorString(e));
   return ok();
@@ -337,7 +393,10 @@ wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const
   WT_TRY(check_act(dy, "dy", desc));
   WT_TRY(check_act(dx, "dx", desc));
   set_load_divs(pl, desc, vec_ok(desc, dy, dx));
-  cudaError_t e = wt::launch_fwd(pl, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale,
+  alignas(64) CUtensorMap tmx;
+  memset(&tmx, 0, sizeof(tmx));
+  pl.use_tma = encode_plane_map(&tmx, dy, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
+  cudaError_t e = wt::launch_fwd(pl, tmx, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale,
                                  wavelet_scale, dx, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_data: %s", cudaGetErrorString(e));
   return ok();
@@ -379,7 +438,12 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
     return fail(WTCONV_ERR_WORKSPACE, "workspace of %zu B given, %zu B needed", ws ? ws_bytes : 0, need);
   if (!aligned(ws, 256)) return fail(WTCONV_ERR_MISALIGNED, "workspace is not 256-byte aligned");
   set_load_divs(pl, desc, vec_ok(desc, x, dy));
-  cudaError_t e = wt::launch_bwd_weight(pl, desc->dtype, x, dy, w_base, b_base, w_sub, base_scale,
+  alignas(64) CUtensorMap tmx, tmd;
+  memset(&tmx, 0, sizeof(tmx));
+  memset(&tmd, 0, sizeof(tmd));
+  pl.use_tma = encode_plane_map(&tmx, x, desc, pl.xs[0].stride, pl.xbf / pl.xs[0].stride, pl.P) &&
+               encode_plane_map(&tmd, dy, desc, pl.ds[0].stride, pl.dbf / pl.ds[0].stride, pl.P);
+  cudaError_t e = wt::launch_bwd_weight(pl, tmx, tmd, desc->dtype, x, dy, w_base, b_base, w_sub, base_scale,
                                         wavelet_scale, dw_base, db_base, dw_sub, dbase_scale,
                                         dwavelet_scale, static_cast<float*>(ws), st);
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_weight: %s", cudaGetErrorString(e));
@@ -399,5 +463,10 @@ const char* wtconv_status_string(wtconv_status_t s) {
 }
 
 const char* wtconv_last_error(void) { return g_last_error; }
+
+unsigned int wtconv_device_faults(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return 0;
+  return wt::take_fwd_faults() + wt::take_bw_faults();
+}
 
 }  // extern "C"

@@ -28,14 +28,19 @@
 
 namespace wt {
 
+// Bounded waits that gave up (see mbar_wait_bounded); read by take_bw_faults().
+static __device__ unsigned int g_bw_faults;
+
 // TR = 8: 8x4 tiles, one per thread; TR = 4: 4x4 tiles, up to two per thread.
 // Tiles are 4 columns wide so neighbouring lanes read neighbouring 16-byte
 // chunks of a row (no shared-memory bank conflicts within a row).
 template <int K, typename T, int TR>
 __global__ void __launch_bounds__(WT_BW_THREADS)
-    bw_kernel(const __grid_constant__ WtBwPlan pl, const T* __restrict__ x, const T* __restrict__ dy,
+    bw_kernel(const __grid_constant__ WtBwPlan pl, const __grid_constant__ CUtensorMap tmx,
+              const __grid_constant__ CUtensorMap tmd, const T* __restrict__ x, const T* __restrict__ dy,
               float* __restrict__ part) {
-  extern __shared__ __align__(16) float sm[];
+  extern __shared__ __align__(16) float sm_raw[];
+  float* const sm = align_smem128(sm_raw);  // TMA box destinations need 128-byte alignment
   constexpr int KK = K * K;
   constexpr int NT = WT_BW_THREADS;
   constexpr int MI = TR == 8 ? 1 : WT_BW_MAX_ITEMS;
@@ -47,14 +52,30 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
   const int gi = blockIdx.x / C;
   const int n_begin = gi * pl.chunk;
   const int n_end = min(pl.N, n_begin + pl.chunk);
-  const int ISF = pl.isf, WF = pl.wf;
+  constexpr int R = K / 2;
+  const int XBF = pl.xbf, DBF = pl.dbf, WF = pl.wf;
   const int ipp = pl.items_per_plane;
   float* const work = sm + pl.work_off;
   const float* const xf = reinterpret_cast<const float*>(x);
   const float* const dyf = reinterpret_cast<const float*>(dy);
+  // TMA path (float32, 16-byte rows): one thread issues the x and dy box
+  // copies of a batch into input slot `slot`; both complete on mbar[slot].
+  const bool tma = ASYNC && pl.use_tma;
+  uint64_t* const mbar = reinterpret_cast<uint64_t*>(sm + pl.mb_off);
+  __shared__ int s_ok;
+  uint32_t parity = 0;  // thread 0: phase parity of mbar[0] (bit 0) and mbar[1] (bit 1)
+  auto issue = [&](int n0, int s) {
+    float* const dst = sm + s * pl.islot;
+    fence_proxy_async();  // earlier generic accesses of the set precede the copies
+    mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes);
+    tma_load_4d(dst, &tmx, -4, -R, c, n0, &mbar[s]);
+    tma_load_4d(dst + pl.xr, &tmd, 0, 0, c, n0, &mbar[s]);
+  };
 
-  // Zeroed once: interiors are rewritten per batch, margins stay zero.
-  zero_smem(sm, pl.work_off + pl.P * WF, tid, NT);
+  // Zeroed once: interiors are rewritten per batch, margins stay zero (the
+  // box copies write whole padded planes themselves).
+  if (tma) zero_smem(work, pl.P * WF, tid, NT);
+  else zero_smem(sm, pl.work_off + pl.P * WF, tid, NT);
 
   float acc[MI][KK];
   float gs[MI];
@@ -64,39 +85,62 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
 #pragma unroll
     for (int t = 0; t < KK; ++t) acc[s][t] = 0.f;
   }
+  if (tma && tid == 0) {
+    mbar_init(&mbar[0], 1);
+    mbar_init(&mbar[1], 1);
+    fence_mbar_init();
+  }
   __syncthreads();
 
-  if (ASYNC && n_begin < n_end) {  // first batch
+  if (tma) {
+    if (tid == 0 && n_begin < n_end) issue(n_begin, 0);
+  } else if (ASYNC && n_begin < n_end) {  // first batch
     const int np0 = min(pl.P, n_end - n_begin);
-    load_planes_async(sm, ISF, pl.xs[0], xf, n_begin, np0, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-    load_planes_async(sm, ISF, pl.ds[0], dyf, n_begin, np0, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+    load_planes_async(sm, XBF, pl.xs[0], xf, n_begin, np0, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+    load_planes_async(sm + pl.xr, DBF, pl.ds[0], dyf, n_begin, np0, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
     cp_async_commit();
     cp_async_wait_all();
   }
   int slot = 0;
   for (int nb = n_begin; nb < n_end; nb += pl.P, slot ^= 1) {
     const int np = min(pl.P, n_end - nb);
-    float* const in = sm + slot * pl.P * ISF;  // this batch's raw x / dy planes
-    if (!ASYNC) {
-      load_planes<T>(in, ISF, pl.xs[0], x, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-      load_planes<T>(in, ISF, pl.ds[0], dy, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-    } else if (nb + pl.P < n_end) {  // prefetch the next batch into the other slot set
+    float* const in_x = sm + slot * pl.islot;  // this batch's raw x planes
+    float* const in_d = in_x + pl.xr;          // ... and raw dy planes
+    if (tma) {
+      if (tid == 0) {
+        const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u);
+        parity ^= 1u << slot;
+        if (ok && nb + pl.P < n_end) issue(nb + pl.P, slot ^ 1);  // the other set was last read by batch nb-P
+        s_ok = ok;
+      }
+    } else if (!ASYNC) {
+      load_planes<T>(in_x, XBF, pl.xs[0], x, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+      load_planes<T>(in_d, DBF, pl.ds[0], dy, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+    } else if (nb + pl.P < n_end) {  // prefetch the next batch into the other slot
       const int n1 = nb + pl.P, np1 = min(pl.P, n_end - n1);
-      float* const nxt = sm + (slot ^ 1) * pl.P * ISF;
-      load_planes_async(nxt, ISF, pl.xs[0], xf, n1, np1, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-      load_planes_async(nxt, ISF, pl.ds[0], dyf, n1, np1, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+      float* const nxt = sm + (slot ^ 1) * pl.islot;
+      load_planes_async(nxt, XBF, pl.xs[0], xf, n1, np1, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+      load_planes_async(nxt + pl.xr, DBF, pl.ds[0], dyf, n1, np1, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
       cp_async_commit();
     }
     __syncthreads();  // this batch's planes are visible
+    if (tma && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
+      if (tid == 0) {
+        atomicAdd(&g_bw_faults, 1u);
+        mbar_wait_bounded(&mbar[slot], ((parity >> slot) & 1u) ^ 1u);  // let the copy in flight land
+      }
+      __syncthreads();
+      return;  // partial sums are not written: the caller sees the fault count
+    }
 
     // Both pyramids: levels 1+2 fused, then 3..L.
     if (L == 1) {
-      haar_level(in, ISF, work, WF, np, pl.xs[0], pl.xs[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
-      haar_level(in, ISF, work, WF, np, pl.ds[0], pl.ds[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
+      haar_level(in_x, XBF, work, WF, np, pl.xs[0], pl.xs[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
+      haar_level(in_d, DBF, work, WF, np, pl.ds[0], pl.ds[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
     } else {
-      haar_levels12(in, ISF, work, WF, np, pl.xs[0], pl.xs[1], pl.xs[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
+      haar_levels12(in_x, XBF, work, WF, np, pl.xs[0], pl.xs[1], pl.xs[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
                     pl.an_pp[2], pl.an_w[2], tid, NT);
-      haar_levels12(in, ISF, work, WF, np, pl.ds[0], pl.ds[1], pl.ds[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
+      haar_levels12(in_d, DBF, work, WF, np, pl.ds[0], pl.ds[1], pl.ds[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
                     pl.an_pp[2], pl.an_w[2], tid, NT);
     }
     __syncthreads();
@@ -121,16 +165,22 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
           const int tp = fdiv(t, pl.tcd[l]);
           const int p0 = tp * TR, q0 = (t - tp * pl.tc[l]) * TC;
           const WtBuf Xb = pl.xs[l], Db = pl.ds[l];
-          const float* ps = (l == 0) ? in + g * ISF : work + g * WF;
-          const float* xw = ps + Xb.off + b * Xb.band + p0 * Xb.stride + q0;
-          const float* dw = ps + Db.off + b * Db.band + p0 * Db.stride + q0;
-          const float dsum = corr_tile<K, TR, TC>(xw, Xb.stride, dw, Db.stride, acc[s]);
-          if (l == 0) gs[s] += dsum;
+          float dsum;
+          if (l == 0) {  // raw planes; x's interior starts 4 floats into each row
+            const float* xw = in_x + g * XBF + Xb.off + p0 * Xb.stride + q0;
+            const float* dw = in_d + g * DBF + Db.off + p0 * Db.stride + q0;
+            dsum = corr_tile<K, TR, TC, 4 - R>(xw, Xb.stride, dw, Db.stride, acc[s]);
+            gs[s] += dsum;
+          } else {
+            const float* ps = work + g * WF;
+            dsum = corr_tile<K, TR, TC>(ps + Xb.off + b * Xb.band + p0 * Xb.stride + q0, Xb.stride,
+                                        ps + Db.off + b * Db.band + p0 * Db.stride + q0, Db.stride, acc[s]);
+          }
         }
       }
     }
-    if (ASYNC) cp_async_wait_all();  // this thread's copies of the next batch have landed
-    __syncthreads();                 // ... and every read of this batch is done
+    if (ASYNC && !tma) cp_async_wait_all();  // this thread's copies of the next batch have landed
+    __syncthreads();                         // ... and every read of this batch is done
   }
 
   // Tile sums -> shared memory -> one record per band.
@@ -220,44 +270,52 @@ __global__ void bw_finalize_kernel(const __grid_constant__ WtBwPlan pl, const fl
 }
 
 template <int K, typename T>
-static cudaError_t launch_bw_t(const WtBwPlan& pl, const void* x, const void* dy, float* part,
-                               cudaStream_t stream) {
+static cudaError_t launch_bw_t(const WtBwPlan& pl, const CUtensorMap& tmx, const CUtensorMap& tmd, const void* x,
+                               const void* dy, float* part, cudaStream_t stream) {
   auto kern = pl.tbr == 8 ? bw_kernel<K, T, 8> : bw_kernel<K, T, 4>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)pl.C * (unsigned)pl.groups;
-  kern<<<grid, WT_BW_THREADS, pl.smem_bytes, stream>>>(pl, static_cast<const T*>(x),
+  kern<<<grid, WT_BW_THREADS, pl.smem_bytes, stream>>>(pl, tmx, tmd, static_cast<const T*>(x),
                                                        static_cast<const T*>(dy), part);
   return cudaGetLastError();
 }
 
 template <typename T>
-static cudaError_t launch_bw_k(const WtBwPlan& pl, const void* x, const void* dy, float* part,
-                               cudaStream_t stream) {
+static cudaError_t launch_bw_k(const WtBwPlan& pl, const CUtensorMap& tmx, const CUtensorMap& tmd, const void* x,
+                               const void* dy, float* part, cudaStream_t stream) {
   switch (pl.K) {
-    case 3: return launch_bw_t<3, T>(pl, x, dy, part, stream);
-    case 5: return launch_bw_t<5, T>(pl, x, dy, part, stream);
-    case 7: return launch_bw_t<7, T>(pl, x, dy, part, stream);
-    case 9: return launch_bw_t<9, T>(pl, x, dy, part, stream);
+    case 3: return launch_bw_t<3, T>(pl, tmx, tmd, x, dy, part, stream);
+    case 5: return launch_bw_t<5, T>(pl, tmx, tmd, x, dy, part, stream);
+    case 7: return launch_bw_t<7, T>(pl, tmx, tmd, x, dy, part, stream);
+    case 9: return launch_bw_t<9, T>(pl, tmx, tmd, x, dy, part, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_bwd_weight(const WtBwPlan& pl, int dtype, const void* x, const void* dy,
+cudaError_t launch_bwd_weight(const WtBwPlan& pl, const CUtensorMap& tmx, const CUtensorMap& tmd, int dtype,
+                              const void* x, const void* dy,
                               const float* w_base, const float* b_base, const float* w_sub,
                               const float* s_base, const float* s_w, float* dw_base, float* db_base,
                               float* dw_sub, float* ds_base, float* ds_w, float* part,
                               cudaStream_t stream) {
   cudaError_t e;
-  if (dtype == 0) e = launch_bw_k<float>(pl, x, dy, part, stream);
-  else if (dtype == 1) e = launch_bw_k<__half>(pl, x, dy, part, stream);
-  else e = launch_bw_k<__nv_bfloat16>(pl, x, dy, part, stream);
+  if (dtype == 0) e = launch_bw_k<float>(pl, tmx, tmd, x, dy, part, stream);
+  else if (dtype == 1) e = launch_bw_k<__half>(pl, tmx, tmd, x, dy, part, stream);
+  else e = launch_bw_k<__nv_bfloat16>(pl, tmx, tmd, x, dy, part, stream);
   if (e != cudaSuccess) return e;
   const int warps = pl.C * pl.nbands;
   const int threads = 256;
   bw_finalize_kernel<<<(warps * 32 + threads - 1) / threads, threads, 0, stream>>>(
       pl, part, w_base, b_base, w_sub, s_base, s_w, dw_base, db_base, dw_sub, ds_base, ds_w);
   return cudaGetLastError();
+}
+
+unsigned int take_bw_faults() {
+  unsigned int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_bw_faults, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_bw_faults, &z, sizeof(z));
+  return v;
 }
 
 }  // namespace wt

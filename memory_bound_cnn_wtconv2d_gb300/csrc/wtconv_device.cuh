@@ -6,6 +6,7 @@
 // 16-byte loads.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -185,11 +186,15 @@ __device__ __forceinline__ void conv_tile_off(const float* __restrict__ row0, in
 
 // acc[du*K+dv] += sum_{o,j} d[o][j] * win[(o+du)*stride + j+dv]   (weight-gradient correlation)
 // Returns the sum of the d tile (for the bias gradient).
-template <int K, int TR, int TC>
+// The window's first column sits OFF floats after the 16-byte-aligned `win`
+// (OFF = 0: whole float4s are read, the row stride leaves room; else exactly
+// TC+K-1 floats are read).
+template <int K, int TR, int TC, int OFF = 0>
 __device__ __forceinline__ float corr_tile(const float* __restrict__ win, int wstride,
                                            const float* __restrict__ dsrc, int dstride,
                                            float (&acc)[K * K]) {
   constexpr int NV = (TC + K - 1 + 3) / 4;
+  constexpr int NS = OFF == 0 ? 4 * NV : TC + K - 1;
   static_assert(TC % 4 == 0, "tile width must be a multiple of 4");
   float d[TR][TC];
   float dsum = 0.f;
@@ -205,8 +210,9 @@ __device__ __forceinline__ float corr_tile(const float* __restrict__ win, int ws
   }
 #pragma unroll
   for (int a = 0; a < TR + K - 1; ++a) {
-    float seg[4 * NV];
-    lds_row<NV>(win + a * wstride, seg);
+    float seg[NS];
+    if constexpr (OFF == 0) lds_row<NV>(win + a * wstride, seg);
+    else lds_span<OFF, NS>(win + a * wstride, seg);
 #pragma unroll
     for (int o = 0; o < TR; ++o) {
       const int du = a - o;
@@ -419,6 +425,68 @@ __device__ __forceinline__ void load_planes_async(float* dbase, int dps, const W
                 src + ((size_t)(n0 + g) * C + c) * HW + rem);
     }
   }
+}
+
+// ---- TMA plane loads (cp.async.bulk.tensor) with mbarrier completion ----
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// First 128-byte aligned float at or after p (shared memory); the launch
+// reserves WT_SMEM_SLACK extra bytes for the shift.
+__device__ __forceinline__ float* align_smem128(float* p) {
+  return p + (((128u - (smem_u32(p) & 127u)) & 127u) >> 2);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* mbar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(mbar)), "r"(count) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses (and
+// mbarrier initialisation) before later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// Makes this thread's mbarrier initialisations visible to the async proxy
+// (and to the rest of the CTA after the next barrier).
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(mbar)), "r"(bytes)
+               : "memory");
+}
+
+// 4-D tiled tensor load: box at coordinates (c0, c1, c2, c3) into dst; the
+// transfer signals complete_tx on mbar.  Out-of-range elements are zero.
+__device__ __forceinline__ void tma_load_4d(float* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                           uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(mbar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* mbar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(mbar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of mbar to complete, giving up after about 2^31
+// clock cycles (about a second).  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* mbar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(mbar, parity)) {
+    if (clock64() - t0 > (1ll << 31)) return false;
+  }
+  return true;
 }
 
 __device__ __forceinline__ void zero_smem(float* sm, int nfloats, int tid, int nthreads) {

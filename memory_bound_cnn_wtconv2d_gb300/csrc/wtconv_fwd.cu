@@ -32,6 +32,9 @@
 
 namespace wt {
 
+// Bounded waits that gave up (see mbar_wait_bounded); read by take_fwd_faults().
+static __device__ unsigned int g_fwd_faults;
+
 // Adds sum_b sign_b(u, v) * z_b to c[u][v] for the four parities (u, v).
 __device__ __forceinline__ void add_parities(float z0, float z1, float z2, float z3, float (&c)[2][2]) {
   const float e0 = z0 + z1, e1 = z0 - z1, f0 = z2 + z3, f1 = z2 - z3;
@@ -79,11 +82,13 @@ __device__ __forceinline__ void stage_weights(float* wsm, int wb, int L, int C, 
 // writes touch interiors only, so every margin stays zero.
 template <int K, typename T, bool ROT>
 __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
-    fwd_kernel(const __grid_constant__ WtFwdPlan pl, const T* __restrict__ x,
+    fwd_kernel(const __grid_constant__ WtFwdPlan pl, const __grid_constant__ CUtensorMap tmx,
+               const T* __restrict__ x,
                const float* __restrict__ w_base, const float* __restrict__ b_base,
                const float* __restrict__ w_sub, const float* __restrict__ s_base,
                const float* __restrict__ s_w, T* __restrict__ y) {
-  extern __shared__ __align__(16) float sm[];
+  extern __shared__ __align__(16) float sm_raw[];
+  float* const sm = align_smem128(sm_raw);  // TMA box destinations need 128-byte alignment
   constexpr int R = K / 2;
   constexpr int NT = WT_FWD_THREADS;
   constexpr int TP = WT_TP, TQ = WT_TQ, ZT = WT_ZT;
@@ -98,20 +103,50 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
   float* const work = sm + pl.work_off;
   const int wb = pl.w_band;
 
-  zero_smem(sm, pl.w_off, tid, NT);
-  __syncthreads();  // the zero fill must land before any plane copy
+  // TMA path (float32, 16-byte rows): one thread issues one box copy per
+  // unit into the input buffer set `slot`; the copy engine writes the whole
+  // padded box (margins zero-filled) and completes on mbar[slot].
+  const bool tma = ASYNC && pl.use_tma;
+  uint64_t* const mbar = reinterpret_cast<uint64_t*>(sm + pl.mb_off);
+  __shared__ int s_ok;
+  uint32_t parity = 0;  // thread 0: current phase parity of mbar[0] (bit 0) and mbar[1] (bit 1)
+  auto issue = [&](int uu, int s) {
+    const int cc = uu / pl.groups;
+    const int nn = (uu - cc * pl.groups) * pl.P;
+    fence_proxy_async();  // earlier generic accesses of the buffer set precede the copy
+    mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes);
+    tma_load_4d(sm + s * pl.xslot, &tmx, -4, -R, cc, nn, &mbar[s]);
+  };
+
+  // Zero margins once (the box copies write whole padded planes themselves).
+  if (tma) zero_smem(sm + pl.work_off, pl.w_off - pl.work_off, tid, NT);
+  else zero_smem(sm, pl.w_off, tid, NT);
+  if (tma && tid == 0) {
+    mbar_init(&mbar[0], 1);
+    mbar_init(&mbar[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();  // the zero fill and barrier init land before any plane copy
+  if (tma && tid == 0 && u_begin < u_end) issue(u_begin, 0);
   int c_prev = -1;
   int slot = 0;
   for (int u = u_begin; u < u_end; ++u, slot ^= 1) {
     const int c = u / pl.groups;
     const int n0 = (u - c * pl.groups) * pl.P;
     const int np = min(pl.P, pl.N - n0);
-    float* const xs = sm + slot * pl.P * XF;
+    float* const xs = sm + slot * pl.xslot;
     if (c != c_prev) {
       stage_weights<K, ROT>(wsm, wb, L, C, c, w_base, w_sub, s_base, s_w, tid, NT);
       c_prev = c;
     }
-    if (!ASYNC) {
+    if (tma) {
+      if (tid == 0) {
+        const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u);
+        parity ^= 1u << slot;
+        if (ok && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
+        s_ok = ok;
+      }
+    } else if (!ASYNC) {
       load_planes<T>(xs, XF, pl.lev[0], x, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
     } else {
       if (u == u_begin) {
@@ -123,13 +158,21 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
       if (u + 1 < u_end) {  // prefetch the next unit into the other buffer set
         const int c1 = (u + 1) / pl.groups;
         const int n1 = (u + 1 - c1 * pl.groups) * pl.P;
-        load_planes_async(sm + (slot ^ 1) * pl.P * XF, XF, pl.lev[0], reinterpret_cast<const float*>(x), n1,
+        load_planes_async(sm + (slot ^ 1) * pl.xslot, XF, pl.lev[0], reinterpret_cast<const float*>(x), n1,
                           min(pl.P, pl.N - n1), c1, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
         cp_async_commit();
       }
     }
     const float bias = (!ROT && b_base != nullptr) ? s_base[c] * b_base[c] : 0.f;
     __syncthreads();  // planes of unit u and the weights are visible
+    if (tma && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
+      if (tid == 0) {
+        atomicAdd(&g_fwd_faults, 1u);
+        mbar_wait_bounded(&mbar[slot], ((parity >> slot) & 1u) ^ 1u);  // let the copy in flight land
+      }
+      __syncthreads();
+      break;
+    }
 
     // (1) Haar pyramid on chip.
     if (L == 1) {
@@ -280,13 +323,13 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
         }
       }
     }
-    if (ASYNC) cp_async_wait_all();  // this thread's copies of the next unit have landed
+    if (ASYNC && !tma) cp_async_wait_all();  // this thread's copies of the next unit have landed
     __syncthreads();                 // ... and all reads of unit u are done
   }  // unit loop
 }
 
 template <int K, typename T, bool ROT>
-static cudaError_t launch_fwd_t(const WtFwdPlan& pl, const void* x, const float* w_base,
+static cudaError_t launch_fwd_t(const WtFwdPlan& pl, const CUtensorMap& tmx, const void* x, const float* w_base,
                                 const float* b_base, const float* w_sub, const float* s_base,
                                 const float* s_w, void* y, cudaStream_t stream) {
   auto kern = fwd_kernel<K, T, ROT>;
@@ -300,35 +343,42 @@ static cudaError_t launch_fwd_t(const WtFwdPlan& pl, const void* x, const float*
   const long long units = (long long)pl.C * pl.groups;
   long long slots = (long long)(per_sm < 1 ? 1 : per_sm) * sms;
   const unsigned grid = (unsigned)(units < slots ? units : slots);
-  kern<<<grid, WT_FWD_THREADS, pl.smem_bytes, stream>>>(pl, static_cast<const T*>(x), w_base, b_base,
+  kern<<<grid, WT_FWD_THREADS, pl.smem_bytes, stream>>>(pl, tmx, static_cast<const T*>(x), w_base, b_base,
                                                         w_sub, s_base, s_w, static_cast<T*>(y));
   return cudaGetLastError();
 }
 
 template <typename T, bool ROT>
-static cudaError_t launch_fwd_k(const WtFwdPlan& pl, const void* x, const float* w_base,
-                                const float* b_base, const float* w_sub, const float* s_base,
-                                const float* s_w, void* y, cudaStream_t stream) {
+static cudaError_t launch_fwd_k(const WtFwdPlan& pl, const CUtensorMap& tmx, const void* x,
+                                const float* w_base, const float* b_base, const float* w_sub,
+                                const float* s_base, const float* s_w, void* y, cudaStream_t stream) {
   switch (pl.K) {
-    case 3: return launch_fwd_t<3, T, ROT>(pl, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
-    case 5: return launch_fwd_t<5, T, ROT>(pl, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
-    case 7: return launch_fwd_t<7, T, ROT>(pl, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
-    case 9: return launch_fwd_t<9, T, ROT>(pl, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
+    case 3: return launch_fwd_t<3, T, ROT>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
+    case 5: return launch_fwd_t<5, T, ROT>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
+    case 7: return launch_fwd_t<7, T, ROT>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
+    case 9: return launch_fwd_t<9, T, ROT>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_fwd(const WtFwdPlan& pl, int dtype, bool rotate, const void* x, const float* w_base,
-                       const float* b_base, const float* w_sub, const float* s_base, const float* s_w,
-                       void* y, cudaStream_t stream) {
+cudaError_t launch_fwd(const WtFwdPlan& pl, const CUtensorMap& tmx, int dtype, bool rotate, const void* x,
+                       const float* w_base, const float* b_base, const float* w_sub, const float* s_base,
+                       const float* s_w, void* y, cudaStream_t stream) {
   if (dtype == 0)
-    return rotate ? launch_fwd_k<float, true>(pl, x, w_base, b_base, w_sub, s_base, s_w, y, stream)
-                  : launch_fwd_k<float, false>(pl, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
+    return rotate ? launch_fwd_k<float, true>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream)
+                  : launch_fwd_k<float, false>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
   if (dtype == 1)
-    return rotate ? launch_fwd_k<__half, true>(pl, x, w_base, b_base, w_sub, s_base, s_w, y, stream)
-                  : launch_fwd_k<__half, false>(pl, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
-  return rotate ? launch_fwd_k<__nv_bfloat16, true>(pl, x, w_base, b_base, w_sub, s_base, s_w, y, stream)
-                : launch_fwd_k<__nv_bfloat16, false>(pl, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
+    return rotate ? launch_fwd_k<__half, true>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream)
+                  : launch_fwd_k<__half, false>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
+  return rotate ? launch_fwd_k<__nv_bfloat16, true>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream)
+                : launch_fwd_k<__nv_bfloat16, false>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
+}
+
+unsigned int take_fwd_faults() {
+  unsigned int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fwd_faults, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_fwd_faults, &z, sizeof(z));
+  return v;
 }
 
 }  // namespace wt

@@ -1,6 +1,7 @@
 // Internal launchers of libwtconv (host side).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "wtconv_plan.h"
@@ -8,12 +9,19 @@
 namespace wt {
 
 // Forward pass (rotate = false) or input-gradient pass (rotate = true, no bias).
-cudaError_t launch_fwd(const WtFwdPlan& pl, int dtype, bool rotate, const void* x, const float* w_base,
-                       const float* b_base, const float* w_sub, const float* s_base, const float* s_w,
-                       void* y, cudaStream_t stream);
+// tmx describes x for the TMA path (used when pl.use_tma).
+cudaError_t launch_fwd(const WtFwdPlan& pl, const CUtensorMap& tmx, int dtype, bool rotate, const void* x,
+                       const float* w_base, const float* b_base, const float* w_sub, const float* s_base,
+                       const float* s_w, void* y, cudaStream_t stream);
+
+// Number of bounded in-kernel waits that gave up since the last call
+// (reads and clears a device counter; synchronises the device).
+unsigned int take_fwd_faults();
+unsigned int take_bw_faults();
 
 // Parameter gradients: correlation kernel into `part`, then the finalize kernel.
-cudaError_t launch_bwd_weight(const WtBwPlan& pl, int dtype, const void* x, const void* dy,
+cudaError_t launch_bwd_weight(const WtBwPlan& pl, const CUtensorMap& tmx, const CUtensorMap& tmd, int dtype,
+                              const void* x, const void* dy,
                               const float* w_base, const float* b_base, const float* w_sub,
                               const float* s_base, const float* s_w, float* dw_base, float* db_base,
                               float* dw_sub, float* ds_base, float* ds_w, float* part,

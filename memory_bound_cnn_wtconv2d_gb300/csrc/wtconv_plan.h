@@ -49,13 +49,17 @@ struct WtFwdPlan {
   int zbegin[WT_MAXL + 2];  // first (band, tile) item of level l within a plane; [L+1] = total
   int zipp;                 // band-convolution items per plane
   int ftr, ftc;             // final tiles (WT_TP x WT_TQ level-1 positions) per plane: rows, columns
-  int xf;                // floats per input-plane buffer (2P of them: two buffer sets)
+  int xf;                // floats per input-plane buffer (= TMA box of one plane)
+  int xslot;             // floats per input buffer set (P planes, 128-byte multiple); two sets
   int wf;                // floats per work area (pyramid + convolved bands; P of them)
-  int work_off;          // = 2 * P * xf
+  int work_off;          // = 2 * xslot
   int w_off;             // folded weights, after the work areas
   int w_band;            // floats per folded kernel (k*k rounded up to 4)
+  int mb_off;            // two mbarriers (8-byte aligned), after the weights
   int smem_bytes;
   int vec_ok;            // rows can use 16-byte global accesses (W % elems-per-16B == 0)
+  int use_tma;           // input planes arrive by TMA box copies (float32, 16-byte rows)
+  uint32_t tma_bytes;    // bytes of one box (P planes)
   WtDiv ld_pp, ld_w;     // plane load: items per plane, items per row
   WtDiv an_pp[WT_MAXL + 1], an_w[WT_MAXL + 1];  // analysis at level l (l = 2: the fused 1+2 pass)
   WtDiv z_ipp;                                  // band-convolution items per plane
@@ -81,12 +85,17 @@ struct WtBwPlan {
   int tc[WT_MAXL + 1];
   int item_begin[WT_MAXL + 2];  // first tile item of level l within a plane (l = 0..L), [L+1] = total
   int items_per_plane;
-  WtBuf xs[WT_MAXL + 1];  // shifted operand: x (l = 0, in an input slot) and its level-l bands, pad = r
-  WtBuf ds[WT_MAXL + 1];  // unshifted operand: dy (l = 0, in an input slot) and its level-l bands, pad = 0
-  int isf;               // floats per input slot (raw x and dy planes; 2P slots: two sets)
+  WtBuf xs[WT_MAXL + 1];  // shifted operand: x (l = 0: r zero rows, 4 zero columns) and its level-l bands, pad r
+  WtBuf ds[WT_MAXL + 1];  // unshifted operand: dy (l = 0, pad 0) and its level-l bands, pad 0
+  int xbf, dbf;          // floats per raw x plane / raw dy plane (= one TMA box row set of one plane)
+  int xr;                // offset of the dy planes within an input set (128-byte multiple)
+  int islot;             // floats per input set (P x planes, then P dy planes); two sets
   int wf;                // floats per work area (both pyramids; P of them)
-  int work_off;          // = 2 * P * isf
+  int work_off;          // = 2 * islot
+  int mb_off;            // two mbarriers (8-byte aligned), after everything else
   int smem_bytes;
+  int use_tma;           // input planes arrive by TMA box copies (float32, 16-byte rows)
+  uint32_t tma_bytes;    // bytes of one input set (x and dy boxes)
   int nbands;            // 1 + 4L
   int part_stride;       // floats per (group, channel) partial record = nbands*(k*k+1)
   int vec_ok;
@@ -96,6 +105,7 @@ struct WtBwPlan {
   WtDiv tiles[WT_MAXL + 1], tcd[WT_MAXL + 1];  // tr*tc and tc per level
 };
 
+#define WT_SMEM_SLACK 128  // bytes added to every dynamic shared-memory size for 128-byte realignment
 #define WT_FWD_THREADS 128
 #define WT_BW_THREADS 256
 #define WT_BW_MAX_ITEMS 2  // tile items per thread in the parameter-gradient pass

@@ -24,7 +24,8 @@ DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 # entry points declared in include/wtconv.h
 EXPORTS = ("wtconv_workspace_size", "wtconv_fwd", "wtconv_bwd_data", "wtconv_bwd_weight",
-           "wtconv_bwd_weight_noalloc", "wtconv_status_string", "wtconv_last_error")
+           "wtconv_bwd_weight_noalloc", "wtconv_status_string", "wtconv_last_error",
+           "wtconv_device_faults")
 
 
 class WtconvDesc(ctypes.Structure):
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.wtconv_status_string.restype = ctypes.c_char_p
         L.wtconv_last_error.argtypes = []
         L.wtconv_last_error.restype = ctypes.c_char_p
+        L.wtconv_device_faults.argtypes = []
+        L.wtconv_device_faults.restype = ctypes.c_uint
         _LIB = L
     return _LIB
 
@@ -186,3 +189,9 @@ def wtconv_bwd_weight_noalloc(x, dy, w_base, b_base, w_sub, base_scale, wavelet_
         _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
         _ptr(grads["dwavelet_scale"]), _stream(stream)))
     return grads
+
+
+def wtconv_device_faults() -> int:
+    """In-kernel bounded waits that gave up since the previous call (0 in
+    normal operation); synchronises the device and resets the count."""
+    return int(lib().wtconv_device_faults())

@@ -47,6 +47,7 @@ def run_gpu(wt, inp, d=None):
     g = wt.wtconv_bwd_weight(d["x"], d["dy"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"],
                              d["wavelet_scale"], L, k)
     torch.cuda.synchronize()
+    assert wt.wtconv_device_faults() == 0, "an in-kernel bounded wait gave up"
     out = dict(y=y.float().cpu().numpy(), dx=dx.float().cpu().numpy())
     for name in GRADS:
         out[name] = None if g[name] is None else g[name].cpu().numpy()
