@@ -52,6 +52,35 @@ def fma_per_plane(H, W, L, k):
     return k * k * (H * W + 4 * sum(Hs[l] * Ws[l] for l in range(1, L + 1)))
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
+# kernel, from one ncu capture of the stage-1 layer (profiles/ncu_full_stage1_f32.md),
+# valid only for the kernel sources they were taken on (hash below).
+MEASURED_TRAFFIC = {
+    "csrc_sha256": "8e13c6a1d3194ec875e038bdce258726c891f8dc80ce663fbbba9a3f3ad842d9",
+    "workload": "stage1",
+    "bytes": {"fwd": 108_307_456, "bwd_data": 108_124_416, "bwd_weight": 157_428_736},
+}
+
+
+def csrc_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "memory_bound_cnn_wtconv2d_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel):
+    t = MEASURED_TRAFFIC
+    if WORKLOAD != t["workload"] or csrc_sha256() != t["csrc_sha256"]:
+        return None  # the kernels changed since the counters were taken
+    return t["bytes"].get(kernel)
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -307,7 +336,8 @@ def run_ours(args, world, rank, local):
     alu_peak = NUM_SMS * FP32_LANES * 2 * SM_MAX_MHZ * 1e6 / 1e12  # TFLOP/s at the maximum SM clock
     achieved_alu = 2 * fma / (avg[dom] * 1e-3) / 1e12
     roofline = {"bound": "alu", "kernel": dom, "achieved": round(achieved_alu, 2), "peak": round(alu_peak, 2),
-                "unit": "TFLOP/s", "frac": round(achieved_alu / alu_peak, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(achieved_alu / alu_peak, 4), "traffic": measured_traffic(dom),
+                "traffic_unit": "bytes per launch (ncu dram read+write)",
                 "peak_source": f"{NUM_SMS} SMs x {FP32_LANES} FP32 FMA/clk x 2 x {SM_MAX_MHZ:.0f} MHz",
                 "algorithmic_fma_per_launch": fma}
     hbm = {"achieved_step_tbs": round(hbm_tbs, 3), "peak_gbs": peaks.get("hbm_gbs"), "peak_kind": peak_kind,
