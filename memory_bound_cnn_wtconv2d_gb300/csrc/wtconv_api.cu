@@ -119,7 +119,11 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   pl.wf = round_up(off, 4);
   pl.w_band = round_up(KK, 4);
   const int wfloats = (1 + 4 * L) * pl.w_band;
-  const long plane_bytes = 4L * (2 * pl.xf + pl.wf) + 256;
+  // Two input sets: float32 planes stream into one while the other is
+  // processed.  (16-bit planes, loaded synchronously, measured faster with
+  // the same layout too.)
+  pl.nsets = 2;
+  const long plane_bytes = 4L * (pl.nsets * pl.xf + pl.wf) + 256;
   if (plane_bytes + 4L * wfloats > kMaxSmemPerBlock)
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %ld B of shared memory (max %d)",
                 d->H, d->W, L, plane_bytes + 4L * wfloats, kMaxSmemPerBlock);
@@ -132,7 +136,7 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   pl.P = P;
   pl.groups = d->N > 0 ? ceil_div(d->N, P) : 0;
   pl.xslot = round_up(P * pl.xf, 32);  // 128-byte aligned buffer sets (TMA destinations)
-  pl.work_off = 2 * pl.xslot;
+  pl.work_off = pl.nsets * pl.xslot;
   pl.w_off = pl.work_off + P * pl.wf;
   pl.mb_off = round_up(pl.w_off + wfloats, 2);
   pl.smem_bytes = 4 * pl.mb_off + 16 + WT_SMEM_SLACK;
@@ -171,6 +175,25 @@ void bw_tiles(const wtconv_desc_t* d, WtBwPlan& pl, int tbr) {
     pl.tc[l] = ceil_div(pl.Ws[l], 4);
     pl.item_begin[l + 1] = pl.item_begin[l] + (l == 0 ? 1 : 4) * pl.tr[l] * pl.tc[l];
   }
+}
+
+// Shared-memory layout of the parameter-gradient pass for `nsets` input sets:
+// [input sets][P work areas, or the end-of-channel reduction if larger]
+// [mbarriers].  TMA destinations are 128-byte aligned.
+void bw_layout(WtBwPlan& pl, int nsets) {
+  const int P = pl.P, KK = pl.K * pl.K;
+  pl.nsets = nsets;
+  pl.xr = round_up(P * pl.xbf, 32);
+  pl.islot = pl.xr + round_up(P * pl.dbf, 32);
+  pl.work_off = nsets * pl.islot;
+  long region = (long)P * pl.wf;
+  const long red = (long)P * pl.items_per_plane * (KK + 1);  // end-of-channel reduction (reuses the work area)
+  if (red > region) region = red;
+  pl.red_floats = (int)((region + 3) / 4 * 4);
+  pl.mb_off = pl.work_off + pl.red_floats;
+  const long smem = 4L * pl.mb_off + 16 + WT_SMEM_SLACK;
+  pl.smem_bytes = smem > INT32_MAX ? INT32_MAX : (int)smem;
+  pl.tma_bytes = (uint32_t)(4L * P * (pl.xbf + pl.dbf));
 }
 
 wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
@@ -214,19 +237,13 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
   if (d->N > 0 && P > d->N) P = d->N;
   if (P < 1) P = 1;
   pl.P = P;
-  pl.xr = round_up(P * pl.xbf, 32);  // 128-byte aligned TMA destinations
-  pl.islot = pl.xr + round_up(P * pl.dbf, 32);
-  pl.work_off = 2 * pl.islot;
-  long floats = pl.work_off + (long)P * pl.wf;
-  const long red = (long)P * pl.items_per_plane * (KK + 1);  // end-of-CTA reduction (aliases the inputs)
-  if (red > floats) floats = red;
-  pl.mb_off = (int)round_up(floats, 2);
-  const long smem = 4L * pl.mb_off + 16 + WT_SMEM_SLACK;
-  if (smem > kMaxSmemPerBlock)
-    return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %ld B of shared memory (max %d)",
-                d->H, d->W, L, smem, kMaxSmemPerBlock);
-  pl.smem_bytes = (int)smem;
-  pl.tma_bytes = (uint32_t)(4L * P * (pl.xbf + pl.dbf));
+  bw_layout(pl, 2);
+  if (pl.smem_bytes > kMaxSmemPerBlock) {
+    bw_layout(pl, 1);
+    if (pl.smem_bytes > kMaxSmemPerBlock)
+      return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %d B of shared memory (max %d)",
+                  d->H, d->W, L, pl.smem_bytes, kMaxSmemPerBlock);
+  }
   for (int l = 0; l <= L; ++l) {
     pl.an_pp[l] = make_div(pl.Hs[l] * pl.Ws[l]);
     pl.an_w[l] = make_div(pl.Ws[l]);
@@ -238,19 +255,38 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
     pl.an_w[2] = make_div(pl.Ws[2]);
   }
   pl.ipp = make_div(pl.items_per_plane);
-  // One wave of (channel, chunk) CTAs when the channels allow it.  Resident
-  // CTAs per SM: limited by shared memory and by registers (256 threads of
-  // up to 128 registers each -> 2).
-  int per_sm = (int)(kSmemPerSm / (smem + 1024));
-  if (per_sm > 2) per_sm = 2;
-  const int ctas = kNumSms * (per_sm < 1 ? 1 : per_sm);
-  const int batches = d->N > 0 ? ceil_div(d->N, P) : 0;
-  int groups = ctas / d->C;
-  if (groups < 1) groups = 1;
-  if (groups > batches) groups = batches;
-  if (batches > 0) {
-    pl.chunk = ceil_div(batches, groups) * P;
-    pl.groups = ceil_div(d->N, pl.chunk);
+  // Resident CTAs per SM from the occupancy calculator (registers and shared
+  // memory); without a device, from shared memory alone, at most 2.  Two
+  // input sets let float32 units stream in while the previous one is
+  // processed (one set when two do not fit).
+  auto per_sm_of = [&](const WtBwPlan& q) {
+    int n = wt::bw_ctas_per_sm(q, d->dtype);
+    if (n <= 0) {
+      n = (int)(kSmemPerSm / (q.smem_bytes + 1024));
+      if (n > 2) n = 2;
+    }
+    return n < 1 ? 1 : n;
+  };
+  // 16-bit activations are loaded synchronously, so they need one input set.
+  if (d->dtype != WTCONV_F32 && pl.nsets == 2) bw_layout(pl, 1);
+  const int per_sm = per_sm_of(pl);
+  // Persistent grid: every resident CTA slot, at most one CTA per unit.
+  pl.batches = d->N > 0 ? ceil_div(d->N, P) : 0;
+  const long long U = (long long)d->C * pl.batches;
+  if (U >= (1 << 24))
+    return fail(WTCONV_ERR_UNSUPPORTED, "%lld (channel, batch) units exceed the 2^24 index range", U);
+  pl.nb_div = make_div(pl.batches > 0 ? pl.batches : 1);
+  const long long slots_total = (long long)kNumSms * per_sm;
+  pl.grid = (int)(U < slots_total ? U : slots_total);
+  if (pl.grid < 1) pl.grid = 1;
+  pl.uq = (int)(U / pl.grid);
+  pl.ur = (int)(U % pl.grid);
+  pl.g_div = make_div(pl.grid);
+  pl.nrec = 0;
+  for (int i = 0; i < pl.grid && U > 0; ++i) {
+    const int ub = bw_unit_begin(pl, i), ue = bw_unit_begin(pl, i + 1);
+    const int span = (ue - 1) / pl.batches - ub / pl.batches + 1;
+    if (span > pl.nrec) pl.nrec = span;
   }
   return WTCONV_OK;
 }
@@ -323,7 +359,7 @@ void set_load_divs(Plan& pl, const wtconv_desc_t* d, int vec) {
 }
 
 size_t bw_workspace_bytes(const WtBwPlan& pl) {
-  const size_t bytes = (size_t)pl.groups * pl.C * pl.part_stride * sizeof(float);
+  const size_t bytes = (size_t)pl.grid * pl.nrec * pl.part_stride * sizeof(float);
   return (bytes + 255) / 256 * 256;
 }
 

@@ -15,14 +15,14 @@
 //   dW_base = s_b G_0, db = s_b g, ds_b = <W_base, G_0> + b g,
 //   dW_l = s_w G_l,    ds_w = <W_l, G_l>.
 //
-// One CTA owns channel c and a chunk of the batch.  Planes of x and dy are
-// read once into shared memory, both pyramids are rebuilt there
-// (unnormalised, so G_l is recovered as 4^-l times the sum), and every
-// thread accumulates the K*K correlations of its fixed 4x4 tiles in
-// registers across the chunk.  At the end the tile sums of each band are
-// reduced through shared memory into one record per (chunk, channel); a
-// second kernel adds the records of all chunks in a fixed order, so the
-// result does not depend on scheduling.
+// A persistent grid splits the (channel, batch-of-planes) units evenly and in
+// order.  Planes of x and dy are read once into shared memory, both pyramids
+// are rebuilt there (unnormalised, so G_l is recovered as 4^-l times the
+// sum), and every thread accumulates the K*K correlations of its fixed tiles
+// in registers across the units of one channel.  When a CTA leaves a channel
+// the tile sums of each band are reduced through shared memory into one
+// record per (CTA, channel); a second kernel adds the records of each channel
+// in CTA order, so the result does not depend on scheduling.
 #include "wtconv_device.cuh"
 #include "wtconv_launch.h"
 
@@ -46,36 +46,52 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
   constexpr int MI = TR == 8 ? 1 : WT_BW_MAX_ITEMS;
   constexpr int TC = 4;
   constexpr bool ASYNC = sizeof(T) == 4;
-  const int tid = threadIdx.x;
-  const int C = pl.C, L = pl.L;
-  const int c = blockIdx.x % C;
-  const int gi = blockIdx.x / C;
-  const int n_begin = gi * pl.chunk;
-  const int n_end = min(pl.N, n_begin + pl.chunk);
   constexpr int R = K / 2;
+  const int tid = threadIdx.x;
+  const int C = pl.C, L = pl.L, P = pl.P, NB = pl.batches;
+  // Persistent CTA: an even share of the C * NB (channel, batch) units, in
+  // order, so it touches one or a few consecutive channels.
+  const int u_begin = bw_unit_begin(pl, blockIdx.x);
+  const int u_end = bw_unit_begin(pl, blockIdx.x + 1);
+  const int c_first = fdiv(u_begin, pl.nb_div);
   const int XBF = pl.xbf, DBF = pl.dbf, WF = pl.wf;
   const int ipp = pl.items_per_plane;
   float* const work = sm + pl.work_off;
   const float* const xf = reinterpret_cast<const float*>(x);
   const float* const dyf = reinterpret_cast<const float*>(dy);
   // TMA path (float32, 16-byte rows): one thread issues the x and dy box
-  // copies of a batch into input slot `slot`; both complete on mbar[slot].
+  // copies of a unit into input set `s`; both complete on mbar[s].
   const bool tma = ASYNC && pl.use_tma;
+  const bool dbl = pl.nsets == 2;
   uint64_t* const mbar = reinterpret_cast<uint64_t*>(sm + pl.mb_off);
   __shared__ int s_ok;
   uint32_t parity = 0;  // thread 0: phase parity of mbar[0] (bit 0) and mbar[1] (bit 1)
-  auto issue = [&](int n0, int s) {
+  auto unit_c = [&](int u) { return fdiv(u, pl.nb_div); };
+  auto issue = [&](int u, int s) {
+    const int cc = unit_c(u);
+    const int n0 = (u - cc * NB) * P;
     float* const dst = sm + s * pl.islot;
     fence_proxy_async();  // earlier generic accesses of the set precede the copies
     mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes);
-    tma_load_4d(dst, &tmx, -4, -R, c, n0, &mbar[s]);
-    tma_load_4d(dst + pl.xr, &tmd, 0, 0, c, n0, &mbar[s]);
+    tma_load_4d(dst, &tmx, -4, -R, cc, n0, &mbar[s]);
+    tma_load_4d(dst + pl.xr, &tmd, 0, 0, cc, n0, &mbar[s]);
+  };
+  auto load_async = [&](int u, int s) {
+    const int cc = unit_c(u);
+    const int n0 = (u - cc * NB) * P;
+    const int np = min(P, pl.N - n0);
+    float* const dst = sm + s * pl.islot;
+    load_planes_async(dst, XBF, pl.xs[0], xf, n0, np, cc, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+    load_planes_async(dst + pl.xr, DBF, pl.ds[0], dyf, n0, np, cc, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w,
+                      tid, NT);
+    cp_async_commit();
   };
 
-  // Zeroed once: interiors are rewritten per batch, margins stay zero (the
-  // box copies write whole padded planes themselves).
-  if (tma) zero_smem(work, pl.P * WF, tid, NT);
-  else zero_smem(sm, pl.work_off + pl.P * WF, tid, NT);
+  // Zeroed once: interiors are rewritten per unit, margins stay zero (the box
+  // copies write whole padded planes themselves).  The work area is zeroed
+  // again after each channel's reduction, which reuses it.
+  if (tma) zero_smem(work, pl.red_floats, tid, NT);
+  else zero_smem(sm, pl.work_off + pl.red_floats, tid, NT);
 
   float acc[MI][KK];
   float gs[MI];
@@ -93,130 +109,137 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
   __syncthreads();
 
   if (tma) {
-    if (tid == 0 && n_begin < n_end) issue(n_begin, 0);
-  } else if (ASYNC && n_begin < n_end) {  // first batch
-    const int np0 = min(pl.P, n_end - n_begin);
-    load_planes_async(sm, XBF, pl.xs[0], xf, n_begin, np0, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-    load_planes_async(sm + pl.xr, DBF, pl.ds[0], dyf, n_begin, np0, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-    cp_async_commit();
+    if (tid == 0 && u_begin < u_end) issue(u_begin, 0);
+  } else if (ASYNC && dbl && u_begin < u_end) {  // first unit
+    load_async(u_begin, 0);
     cp_async_wait_all();
   }
   int slot = 0;
-  for (int nb = n_begin; nb < n_end; nb += pl.P, slot ^= 1) {
-    const int np = min(pl.P, n_end - nb);
-    float* const in_x = sm + slot * pl.islot;  // this batch's raw x planes
-    float* const in_d = in_x + pl.xr;          // ... and raw dy planes
-    if (tma) {
-      if (tid == 0) {
-        const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u);
-        parity ^= 1u << slot;
-        if (ok && nb + pl.P < n_end) issue(nb + pl.P, slot ^ 1);  // the other set was last read by batch nb-P
-        s_ok = ok;
+  for (int u = u_begin; u < u_end;) {
+    // The units of channel c held by this CTA: [u, u_stop).
+    const int c = unit_c(u);
+    const int u_stop = min(u_end, (c + 1) * NB);
+    for (; u < u_stop; ++u, slot = dbl ? slot ^ 1 : 0) {
+      const int n0 = (u - c * NB) * P;
+      const int np = min(P, pl.N - n0);
+      float* const in_x = sm + slot * pl.islot;  // this unit's raw x planes
+      float* const in_d = in_x + pl.xr;          // ... and raw dy planes
+      if (tma) {
+        if (tid == 0) {
+          const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u);
+          parity ^= 1u << slot;
+          if (ok && dbl && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
+          s_ok = ok;
+        }
+      } else if (!ASYNC || !dbl) {
+        load_planes<T>(in_x, XBF, pl.xs[0], x, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+        load_planes<T>(in_d, DBF, pl.ds[0], dy, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
+      } else if (u + 1 < u_end) {  // prefetch the next unit into the other set
+        load_async(u + 1, slot ^ 1);
       }
-    } else if (!ASYNC) {
-      load_planes<T>(in_x, XBF, pl.xs[0], x, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-      load_planes<T>(in_d, DBF, pl.ds[0], dy, nb, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-    } else if (nb + pl.P < n_end) {  // prefetch the next batch into the other slot
-      const int n1 = nb + pl.P, np1 = min(pl.P, n_end - n1);
-      float* const nxt = sm + (slot ^ 1) * pl.islot;
-      load_planes_async(nxt, XBF, pl.xs[0], xf, n1, np1, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-      load_planes_async(nxt + pl.xr, DBF, pl.ds[0], dyf, n1, np1, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
-      cp_async_commit();
-    }
-    __syncthreads();  // this batch's planes are visible
-    if (tma && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
-      if (tid == 0) {
-        atomicAdd(&g_bw_faults, 1u);
-        mbar_wait_bounded(&mbar[slot], ((parity >> slot) & 1u) ^ 1u);  // let the copy in flight land
+      __syncthreads();  // this unit's planes are visible
+      if (tma && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
+        if (tid == 0) {
+          atomicAdd(&g_bw_faults, 1u);
+          mbar_wait_bounded(&mbar[slot], ((parity >> slot) & 1u) ^ 1u);  // let the copy in flight land
+        }
+        __syncthreads();
+        return;  // records are not written: the caller sees the fault count
       }
-      __syncthreads();
-      return;  // partial sums are not written: the caller sees the fault count
-    }
 
-    // Both pyramids: levels 1+2 fused, then 3..L.
-    if (L == 1) {
-      haar_level(in_x, XBF, work, WF, np, pl.xs[0], pl.xs[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
-      haar_level(in_d, DBF, work, WF, np, pl.ds[0], pl.ds[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
-    } else {
-      haar_levels12(in_x, XBF, work, WF, np, pl.xs[0], pl.xs[1], pl.xs[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
-                    pl.an_pp[2], pl.an_w[2], tid, NT);
-      haar_levels12(in_d, DBF, work, WF, np, pl.ds[0], pl.ds[1], pl.ds[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
-                    pl.an_pp[2], pl.an_w[2], tid, NT);
-    }
-    __syncthreads();
-    for (int l = 3; l <= L; ++l) {
-      haar_level(work, WF, work, WF, np, pl.xs[l - 1], pl.xs[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
-      haar_level(work, WF, work, WF, np, pl.ds[l - 1], pl.ds[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
+      // Both pyramids: levels 1+2 fused, then 3..L.
+      if (L == 1) {
+        haar_level(in_x, XBF, work, WF, np, pl.xs[0], pl.xs[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
+        haar_level(in_d, DBF, work, WF, np, pl.ds[0], pl.ds[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
+      } else {
+        haar_levels12(in_x, XBF, work, WF, np, pl.xs[0], pl.xs[1], pl.xs[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
+                      pl.an_pp[2], pl.an_w[2], tid, NT);
+        haar_levels12(in_d, DBF, work, WF, np, pl.ds[0], pl.ds[1], pl.ds[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
+                      pl.an_pp[2], pl.an_w[2], tid, NT);
+      }
       __syncthreads();
-    }
+      for (int l = 3; l <= L; ++l) {
+        haar_level(work, WF, work, WF, np, pl.xs[l - 1], pl.xs[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
+        haar_level(work, WF, work, WF, np, pl.ds[l - 1], pl.ds[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
+        __syncthreads();
+      }
 #pragma unroll
-    for (int s = 0; s < MI; ++s) {
-      const int item = tid + s * NT;
-      if (item < pl.P * ipp) {
-        const int g = fdiv(item, pl.ipp);
-        if (g < np) {
-          const int local = item - g * ipp;
-          int l = 0;
-          while (l < L && local >= pl.item_begin[l + 1]) ++l;
-          const int tiles = pl.tr[l] * pl.tc[l];
-          const int rel = local - pl.item_begin[l];
-          const int b = fdiv(rel, pl.tiles[l]);
-          const int t = rel - b * tiles;
-          const int tp = fdiv(t, pl.tcd[l]);
-          const int p0 = tp * TR, q0 = (t - tp * pl.tc[l]) * TC;
-          const WtBuf Xb = pl.xs[l], Db = pl.ds[l];
-          float dsum;
-          if (l == 0) {  // raw planes; x's interior starts 4 floats into each row
-            const float* xw = in_x + g * XBF + Xb.off + p0 * Xb.stride + q0;
-            const float* dw = in_d + g * DBF + Db.off + p0 * Db.stride + q0;
-            dsum = corr_tile<K, TR, TC, 4 - R>(xw, Xb.stride, dw, Db.stride, acc[s]);
-            gs[s] += dsum;
-          } else {
-            const float* ps = work + g * WF;
-            dsum = corr_tile<K, TR, TC>(ps + Xb.off + b * Xb.band + p0 * Xb.stride + q0, Xb.stride,
-                                        ps + Db.off + b * Db.band + p0 * Db.stride + q0, Db.stride, acc[s]);
+      for (int s = 0; s < MI; ++s) {
+        const int item = tid + s * NT;
+        if (item < P * ipp) {
+          const int g = fdiv(item, pl.ipp);
+          if (g < np) {
+            const int local = item - g * ipp;
+            int l = 0;
+            while (l < L && local >= pl.item_begin[l + 1]) ++l;
+            const int tiles = pl.tr[l] * pl.tc[l];
+            const int rel = local - pl.item_begin[l];
+            const int b = fdiv(rel, pl.tiles[l]);
+            const int t = rel - b * tiles;
+            const int tp = fdiv(t, pl.tcd[l]);
+            const int p0 = tp * TR, q0 = (t - tp * pl.tc[l]) * TC;
+            const WtBuf Xb = pl.xs[l], Db = pl.ds[l];
+            if (l == 0) {  // raw planes; x's interior starts 4 floats into each row
+              const float* xw = in_x + g * XBF + Xb.off + p0 * Xb.stride + q0;
+              const float* dw = in_d + g * DBF + Db.off + p0 * Db.stride + q0;
+              gs[s] += corr_tile<K, TR, TC, 4 - R>(xw, Xb.stride, dw, Db.stride, acc[s]);
+            } else {
+              const float* ps = work + g * WF;
+              corr_tile<K, TR, TC>(ps + Xb.off + b * Xb.band + p0 * Xb.stride + q0, Xb.stride,
+                                   ps + Db.off + b * Db.band + p0 * Db.stride + q0, Db.stride, acc[s]);
+            }
           }
         }
       }
-    }
-    if (ASYNC && !tma) cp_async_wait_all();  // this thread's copies of the next batch have landed
-    __syncthreads();                         // ... and every read of this batch is done
-  }
+      if (ASYNC && !tma && dbl) cp_async_wait_all();  // this thread's copies of the next unit have landed
+      __syncthreads();                                // ... and every read of this unit is done
 
-  // Tile sums -> shared memory -> one record per band.
-  float* red = sm;
-  const int rs = KK + 1;
-#pragma unroll
-  for (int s = 0; s < MI; ++s) {
-    const int item = tid + s * NT;
-    if (item < pl.P * ipp) {
-#pragma unroll
-      for (int t = 0; t < KK; ++t) red[item * rs + t] = acc[s][t];
-      red[item * rs + KK] = gs[s];
+      if (tma && !dbl && tid == 0 && u + 1 < u_end) issue(u + 1, 0);  // single set: refill it now
     }
-  }
-  __syncthreads();
-  float* rec = part + ((size_t)gi * C + c) * pl.part_stride;
-  for (int qd = tid; qd < pl.nbands * rs; qd += NT) {
-    const int B = qd / rs;
-    const int t = qd - B * rs;
-    const int l = (B == 0) ? 0 : 1 + ((B - 1) >> 2);
-    const int b = (B == 0) ? 0 : ((B - 1) & 3);
-    const int tiles = pl.tr[l] * pl.tc[l];
-    const int first = pl.item_begin[l] + b * tiles;
-    float sum = 0.f;
-    if (B == 0 || t < KK) {
-      for (int g = 0; g < pl.P; ++g)
-        for (int i = 0; i < tiles; ++i) sum += red[(g * ipp + first + i) * rs + t];
+    // Leaving channel c: tile sums -> shared memory (the work area) -> one
+    // record per band -> this CTA's record slot for c.
+    float* const red = work;
+    const int rs = KK + 1;
+#pragma unroll
+    for (int s = 0; s < MI; ++s) {
+      const int item = tid + s * NT;
+      if (item < P * ipp) {
+#pragma unroll
+        for (int t = 0; t < KK; ++t) red[item * rs + t] = acc[s][t];
+        red[item * rs + KK] = gs[s];
+      }
+      gs[s] = 0.f;
+#pragma unroll
+      for (int t = 0; t < KK; ++t) acc[s][t] = 0.f;
     }
-    rec[qd] = sum;
+    __syncthreads();
+    float* rec = part + ((size_t)blockIdx.x * pl.nrec + (c - c_first)) * pl.part_stride;
+    for (int qd = tid; qd < pl.nbands * rs; qd += NT) {
+      const int B = qd / rs;
+      const int t = qd - B * rs;
+      const int l = (B == 0) ? 0 : 1 + ((B - 1) >> 2);
+      const int b = (B == 0) ? 0 : ((B - 1) & 3);
+      const int tiles = pl.tr[l] * pl.tc[l];
+      const int first = pl.item_begin[l] + b * tiles;
+      float sum = 0.f;
+      if (B == 0 || t < KK) {
+        for (int g = 0; g < P; ++g)
+          for (int i = 0; i < tiles; ++i) sum += red[(g * ipp + first + i) * rs + t];
+      }
+      rec[qd] = sum;
+    }
+    __syncthreads();
+    if (u < u_end) {
+      zero_smem(work, pl.red_floats, tid, NT);  // restore the pyramids' zero margins
+      __syncthreads();
+    }
   }
 }
 
-// Adds the records of all chunks of channel c in chunk order and unfolds the
-// scales.  One warp per (channel, band): lane t owns taps t, t+32, t+64; the
-// scale gradient <W, G> is reduced with a fixed shuffle tree, so the result
-// does not depend on scheduling.
+// Adds the records of channel c from every CTA whose units cover it, in CTA
+// order, and unfolds the scales.  One warp per (channel, band): lane t owns
+// taps t, t+32, t+64; the scale gradient <W, G> is reduced with a fixed
+// shuffle tree, so the result does not depend on scheduling.
 __global__ void bw_finalize_kernel(const __grid_constant__ WtBwPlan pl, const float* __restrict__ part,
                                    const float* __restrict__ w_base, const float* __restrict__ b_base,
                                    const float* __restrict__ w_sub, const float* __restrict__ s_base,
@@ -225,12 +248,19 @@ __global__ void bw_finalize_kernel(const __grid_constant__ WtBwPlan pl, const fl
                                    float* __restrict__ ds_base, float* __restrict__ ds_w) {
   const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
-  const int C = pl.C, K = pl.K, KK = K * K, rs = KK + 1;
+  const int C = pl.C, K = pl.K, KK = K * K, rs = KK + 1, NB = pl.batches, G = pl.grid;
   if (warp >= C * pl.nbands) return;  // whole warps exit together
   const int c = warp / pl.nbands;
   const int B = warp - c * pl.nbands;
-  const float* rec = part + (size_t)c * pl.part_stride + (size_t)B * rs;
-  const size_t gstride = (size_t)C * pl.part_stride;
+  // CTAs i0 .. i1-1 hold the units [c*NB, (c+1)*NB) of channel c: i0 holds
+  // unit c*NB, i1 is the first CTA starting at or after (c+1)*NB.
+  int i0 = (int)((long long)c * G / C);
+  while (i0 > 0 && bw_unit_begin(pl, i0) > c * NB) --i0;
+  while (bw_unit_begin(pl, i0 + 1) <= c * NB) ++i0;
+  int i1 = (int)((long long)(c + 1) * G / C);
+  if (i1 < i0 + 1) i1 = i0 + 1;
+  while (i1 > i0 + 1 && bw_unit_begin(pl, i1 - 1) >= (c + 1) * NB) --i1;
+  while (i1 < G && bw_unit_begin(pl, i1) < (c + 1) * NB) ++i1;
   int l = 0;
   size_t ch = 0;
   float scale;
@@ -247,20 +277,37 @@ __global__ void bw_finalize_kernel(const __grid_constant__ WtBwPlan pl, const fl
     w = w_sub + ch * KK;
     dw = dw_sub + ch * KK;
   }
+  // Sum the records in CTA order; lane j of each 32-CTA batch finds the
+  // record of CTA base + j, the others read it through a shuffle.
+  float Gt[3] = {0.f, 0.f, 0.f};  // taps lane, lane + 32, lane + 64 (k <= 9)
+  float gsum = 0.f;
+  for (int base = i0; base < i1; base += 32) {
+    const int i = base + lane;
+    long long off = 0;
+    if (i < i1) off = ((long long)i * pl.nrec + (c - fdiv(bw_unit_begin(pl, i), pl.nb_div))) * pl.part_stride + (long long)B * rs;
+    const int n = min(32, i1 - base);
+    for (int j = 0; j < n; ++j) {
+      const float* rec = part + __shfl_sync(0xffffffffu, off, j);
+#pragma unroll
+      for (int m = 0; m < 3; ++m)
+        if (lane + 32 * m < KK) Gt[m] += rec[lane + 32 * m];
+      if (B == 0 && lane == 0) gsum += rec[KK];
+    }
+  }
   float dot = 0.f;
-  for (int t = lane; t < KK; t += 32) {
-    float G = 0.f;
-    for (int g = 0; g < pl.groups; ++g) G += rec[g * gstride + t];
-    G = ldexpf(G, -2 * l);  // level-l sums were taken on unnormalised coefficients
-    dw[t] = scale * G;
-    dot = fmaf(w[t], G, dot);
+#pragma unroll
+  for (int m = 0; m < 3; ++m) {
+    const int t = lane + 32 * m;
+    if (t < KK) {
+      const float Gs = ldexpf(Gt[m], -2 * l);  // level-l sums were taken on unnormalised coefficients
+      dw[t] = scale * Gs;
+      dot = fmaf(w[t], Gs, dot);
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
   if (lane == 0) {
     if (B == 0) {
-      float gsum = 0.f;
-      for (int g = 0; g < pl.groups; ++g) gsum += rec[g * gstride + KK];
       if (db_base) db_base[c] = scale * gsum;
       ds_base[c] = b_base ? fmaf(b_base[c], gsum, dot) : dot;
     } else {
@@ -275,7 +322,7 @@ static cudaError_t launch_bw_t(const WtBwPlan& pl, const CUtensorMap& tmx, const
   auto kern = pl.tbr == 8 ? bw_kernel<K, T, 8> : bw_kernel<K, T, 4>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)pl.C * (unsigned)pl.groups;
+  const unsigned grid = (unsigned)pl.grid;
   kern<<<grid, WT_BW_THREADS, pl.smem_bytes, stream>>>(pl, tmx, tmd, static_cast<const T*>(x),
                                                        static_cast<const T*>(dy), part);
   return cudaGetLastError();
@@ -309,6 +356,36 @@ cudaError_t launch_bwd_weight(const WtBwPlan& pl, const CUtensorMap& tmx, const 
   bw_finalize_kernel<<<(warps * 32 + threads - 1) / threads, threads, 0, stream>>>(
       pl, part, w_base, b_base, w_sub, s_base, s_w, dw_base, db_base, dw_sub, ds_base, ds_w);
   return cudaGetLastError();
+}
+
+// Resident parameter-gradient CTAs per SM for this plan (0 if the runtime
+// cannot tell, e.g. without a device).
+int bw_ctas_per_sm(const WtBwPlan& pl, int dtype) {
+  const void* f = nullptr;
+#define WT_BW_PICK(KK, TT) f = pl.tbr == 8 ? (const void*)bw_kernel<KK, TT, 8> : (const void*)bw_kernel<KK, TT, 4>
+#define WT_BW_PICK_K(TT)          \
+  switch (pl.K) {                 \
+    case 3: WT_BW_PICK(3, TT); break; \
+    case 5: WT_BW_PICK(5, TT); break; \
+    case 7: WT_BW_PICK(7, TT); break; \
+    case 9: WT_BW_PICK(9, TT); break; \
+    default: return 0;            \
+  }
+  if (dtype == 0) { WT_BW_PICK_K(float) }
+  else if (dtype == 1) { WT_BW_PICK_K(__half) }
+  else { WT_BW_PICK_K(__nv_bfloat16) }
+#undef WT_BW_PICK_K
+#undef WT_BW_PICK
+  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, WT_BW_THREADS, pl.smem_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 unsigned int take_bw_faults() {

@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
   if (tma && tid == 0 && u_begin < u_end) issue(u_begin, 0);
   int c_prev = -1;
   int slot = 0;
-  for (int u = u_begin; u < u_end; ++u, slot ^= 1) {
+  const bool dbl = pl.nsets == 2;
+  for (int u = u_begin; u < u_end; ++u, slot = dbl ? slot ^ 1 : 0) {
     const int c = u / pl.groups;
     const int n0 = (u - c * pl.groups) * pl.P;
     const int np = min(pl.P, pl.N - n0);

@@ -27,6 +27,10 @@ cudaError_t launch_bwd_weight(const WtBwPlan& pl, const CUtensorMap& tmx, const 
                               float* dw_sub, float* ds_base, float* ds_w, float* part,
                               cudaStream_t stream);
 
+// Resident parameter-gradient CTAs per SM for a plan, from the runtime's
+// occupancy calculator (0 when it cannot tell).
+int bw_ctas_per_sm(const WtBwPlan& pl, int dtype);
+
 // Sets the thread-local message returned by wtconv_last_error().
 void set_last_error(const char* msg);
 

@@ -1,7 +1,7 @@
 // wtconv_bwd_weight_noalloc: the parameter-gradient call for callers that
 // cannot allocate device memory.
 //
-// wtconv_bwd_weight needs a caller-provided workspace for its per-chunk
+// wtconv_bwd_weight needs a caller-provided workspace for its per-CTA
 // partial sums.  Some callers have no way to obtain one: a plugin running
 // inside a host application that owns the whole device-memory budget (a
 // fixed arena or an allocator the plugin cannot reach), or a latency-bound

@@ -50,9 +50,10 @@ struct WtFwdPlan {
   int zipp;                 // band-convolution items per plane
   int ftr, ftc;             // final tiles (WT_TP x WT_TQ level-1 positions) per plane: rows, columns
   int xf;                // floats per input-plane buffer (= TMA box of one plane)
-  int xslot;             // floats per input buffer set (P planes, 128-byte multiple); two sets
+  int xslot;             // floats per input buffer set (P planes, 128-byte multiple)
+  int nsets;             // input sets: 2 (float32: the next unit streams in meanwhile) or 1
   int wf;                // floats per work area (pyramid + convolved bands; P of them)
-  int work_off;          // = 2 * xslot
+  int work_off;          // = nsets * xslot
   int w_off;             // folded weights, after the work areas
   int w_band;            // floats per folded kernel (k*k rounded up to 4)
   int mb_off;            // two mbarriers (8-byte aligned), after the weights
@@ -67,16 +68,21 @@ struct WtFwdPlan {
   WtDiv f_pp, f_c;                              // final tiles per plane, per row
 };
 
-// Parameter-gradient pass.  One CTA owns channel c and the planes
-// n in [gi*chunk, min(N, (gi+1)*chunk)), P at a time (the next P are
-// prefetched into a second set of input slots while the current ones are
-// correlated).  "Bands" B number the
-// correlations: B = 0 base path, B = 1 + 4*(l-1) + b for level l, band b.
+// Parameter-gradient pass.  The work is C * batches units (channel c, batch
+// of P planes), split evenly and in order over a persistent grid; a CTA
+// correlates one unit at a time (the next unit's planes stream in meanwhile
+// when there are two input sets) and writes one record per channel it
+// touched.  "Bands" B number the correlations: B = 0 base path,
+// B = 1 + 4*(l-1) + b for level l, band b.
 struct WtBwPlan {
   int N, C, H, W, L, K;
-  int P;                 // planes resident at once
-  int chunk;             // planes per CTA
-  int groups;            // ceil(N / chunk); grid = C * groups
+  int P;                 // planes per unit
+  int batches;           // units per channel = ceil(N / P)
+  WtDiv nb_div;          // divides by batches
+  int grid;              // persistent CTAs G; CTA i starts at unit floor(U*i/G) = uq*i + (ur*i)/G
+  int uq, ur;            // U = C * batches = uq*G + ur
+  WtDiv g_div;           // divides by G (exact: ur*i < G^2 < 2^24)
+  int nrec;              // record slots per CTA (most channels one CTA touches)
   int Hs[WT_MAXL + 1];
   int Ws[WT_MAXL + 1];
   int tbr;               // tile rows: 8 (one tile per thread) or 4 (up to two per thread)
@@ -89,9 +95,11 @@ struct WtBwPlan {
   WtBuf ds[WT_MAXL + 1];  // unshifted operand: dy (l = 0, pad 0) and its level-l bands, pad 0
   int xbf, dbf;          // floats per raw x plane / raw dy plane (= one TMA box row set of one plane)
   int xr;                // offset of the dy planes within an input set (128-byte multiple)
-  int islot;             // floats per input set (P x planes, then P dy planes); two sets
+  int islot;             // floats per input set (P x planes, then P dy planes)
+  int nsets;             // input sets: 2 (the next batch streams in meanwhile) or 1
   int wf;                // floats per work area (both pyramids; P of them)
-  int work_off;          // = 2 * islot
+  int work_off;          // = nsets * islot
+  int red_floats;        // work area = max(P work areas, end-of-channel reduction), floats
   int mb_off;            // two mbarriers (8-byte aligned), after everything else
   int smem_bytes;
   int use_tma;           // input planes arrive by TMA box copies (float32, 16-byte rows)
@@ -113,3 +121,15 @@ struct WtBwPlan {
 #define WT_TQ 2
 #define WT_ZT 4            // band-convolution tile: ZT x ZT coefficient positions
 #define WT_BT 4            // parameter-gradient tile: WT_BT x WT_BT positions
+
+// Division helpers shared by the host planner and the kernels.
+#ifdef __CUDACC__
+#define WT_HD __host__ __device__ __forceinline__
+#else
+#define WT_HD inline
+#endif
+WT_HD int wt_fdiv(int n, WtDiv d) {
+  return (int)(((uint32_t)(((uint64_t)(uint32_t)n * d.mul) >> 32) + (uint32_t)n) >> d.shift);
+}
+// First (channel, batch) unit of persistent CTA i: floor(U*i/G).
+WT_HD int bw_unit_begin(const WtBwPlan& pl, int i) { return pl.uq * i + wt_fdiv(pl.ur * i, pl.g_div); }
