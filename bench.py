@@ -192,6 +192,168 @@ def time_oracle(inp, n_images):
     return time.perf_counter() - t0
 
 
+def unfused_torch_layer(x, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k):
+    """WTConv2d with one PyTorch library op per stage, the way the pages describe
+    the reference implementation (technical summary, "Problem statement"): a
+    grouped stride-2 convolution with the four Haar filters writes the
+    subbands of each level, a depthwise convolution per subband, the wavelet
+    scale as its own elementwise pass, a grouped transposed convolution per
+    level for the synthesis (the previous reconstruction added to the
+    low-pass band first), and the scaled base depthwise convolution.  Autograd
+    differentiates it.  A comparison arm only: nothing calls it on the path.
+    """
+    import torch
+    import torch.nn.functional as F
+
+    N, C = x.shape[:2]
+    r = k // 2
+    haar = 0.5 * torch.tensor([[[1, 1], [1, 1]], [[1, 1], [-1, -1]], [[1, -1], [1, -1]], [[1, -1], [-1, 1]]],
+                              dtype=x.dtype, device=x.device)
+    filt = haar.unsqueeze(1).repeat(C, 1, 1, 1)  # [4C, 1, 2, 2]: subband channel 4c+b
+    cur, zs, sizes = x, [], []
+    for lev in range(levels):
+        h, w = cur.shape[-2:]
+        sizes.append((h, w))
+        Y = F.conv2d(F.pad(cur, (0, w % 2, 0, h % 2)), filt, stride=2, groups=C)
+        Z = F.conv2d(Y, w_sub[lev].unsqueeze(1), padding=r, groups=4 * C)
+        zs.append(Z * wavelet_scale[lev].view(1, -1, 1, 1))
+        cur = Y.view(N, C, 4, *Y.shape[-2:])[:, :, 0]
+    nxt = None
+    for lev in reversed(range(levels)):
+        Z = zs[lev]
+        if nxt is not None:
+            Zv = Z.view(N, C, 4, *Z.shape[-2:])
+            Z = torch.cat([Zv[:, :, :1] + nxt.unsqueeze(2), Zv[:, :, 1:]], dim=2).view(Z.shape)
+        h, w = sizes[lev]
+        nxt = F.conv_transpose2d(Z, filt, stride=2, groups=C)[..., :h, :w]
+    base = F.conv2d(x, w_base.unsqueeze(1), b_base, padding=r, groups=C) * base_scale.view(1, -1, 1, 1)
+    return base + nxt
+
+
+def compare_arms(inp, dev, reps=10):
+    """Training step (fwd + autograd bwd) and inference (fwd) of the fused
+    layer, the unfused PyTorch composition and a cuDNN depthwise 7x7
+    convolution on the same x, plus the peak extra device memory of one
+    training step.  Comparison figures only."""
+    import torch
+    import torch.nn.functional as F
+
+    from memory_bound_cnn_wtconv2d_gb300 import layer, wtconv
+
+    dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[inp.dtype]
+    L, k, C = inp.levels, inp.k, inp.C
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > L2
+    f32 = lambda a: None if a is None else torch.tensor(a, dtype=torch.float32, device=dev)
+    p32 = [f32(a) for a in (inp.w_base, inp.b_base, inp.w_sub, inp.base_scale, inp.wavelet_scale)]
+    pdt = [a.to(dt) for a in p32]
+    w7 = (0.05 * torch.randn(C, 1, 7, 7, generator=torch.Generator().manual_seed(7))).to(dev, dt)
+    x = torch.tensor(inp.x, dtype=dt, device=dev)
+    dy = torch.tensor(inp.dy, dtype=dt, device=dev)
+
+    def leaves(ps):
+        return [p.detach().clone().requires_grad_(True) for p in ps]
+
+    def train_fused():
+        xg = x.detach().requires_grad_(True)
+        y = layer.WTConv2dFunction.apply(xg, *leaves(p32), L, k)
+        y.backward(dy)
+
+    def train_unfused():
+        xg = x.detach().requires_grad_(True)
+        y = unfused_torch_layer(xg, *leaves(pdt), L, k)
+        y.backward(dy)
+
+    def train_dw7():
+        xg = x.detach().requires_grad_(True)
+        wg = w7.detach().requires_grad_(True)
+        F.conv2d(xg, wg, padding=3, groups=C).backward(dy)
+
+    def infer_fused():
+        wtconv.wtconv_fwd(x, *p32, L, k)
+
+    def infer_unfused():
+        with torch.no_grad():
+            unfused_torch_layer(x, *pdt, L, k)
+
+    def infer_dw7():
+        with torch.no_grad():
+            F.conv2d(x, w7, padding=3, groups=C)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return round(statistics.median(ts), 4)
+
+    def peak(fn):
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        fn()
+        torch.cuda.synchronize()
+        return int(torch.cuda.max_memory_allocated(dev) - base)
+
+    train = {"fused": timed(train_fused), "unfused_torch": timed(train_unfused), "dw7x7_cudnn": timed(train_dw7)}
+    infer = {"fused": timed(infer_fused), "unfused_torch": timed(infer_unfused), "dw7x7_cudnn": timed(infer_dw7)}
+    mem = {"fused": peak(train_fused), "unfused_torch": peak(train_unfused), "dw7x7_cudnn": peak(train_dw7)}
+    del flush
+    return {
+        "workload": workload_config(inp)["workload"], "dtype": inp.dtype,
+        "train_ms": train, "infer_ms": infer, "train_peak_extra_bytes": mem,
+        "train_speedup_vs_unfused": round(train["unfused_torch"] / train["fused"], 3),
+        "train_speedup_vs_dw7x7": round(train["dw7x7_cudnn"] / train["fused"], 3),
+        "infer_speedup_vs_unfused": round(infer["unfused_torch"] / infer["fused"], 3),
+        "infer_speedup_vs_dw7x7": round(infer["dw7x7_cudnn"] / infer["fused"], 3),
+        "train_peak_mem_reduction_vs_unfused": round(mem["unfused_torch"] / max(mem["fused"], 1), 3),
+    }
+
+
+def run_arm_only(args):
+    """One arm's training step on the bench workload, for a profiler's launch
+    list (its per-kernel DRAM bytes give the bytes moved per element)."""
+    import torch
+    import torch.nn.functional as F
+
+    from memory_bound_cnn_wtconv2d_gb300 import build, layer
+
+    build.build()
+    dev = torch.device("cuda:0")
+    inp = synth.workload(WORKLOAD)
+    dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[inp.dtype]
+    f32 = lambda a: None if a is None else torch.tensor(a, dtype=torch.float32, device=dev, requires_grad=True)
+    ps = [f32(a) for a in (inp.w_base, inp.b_base, inp.w_sub, inp.base_scale, inp.wavelet_scale)]
+    x = torch.tensor(inp.x, dtype=dt, device=dev, requires_grad=True)
+    dy = torch.tensor(inp.dy, dtype=dt, device=dev)
+    w7 = torch.zeros(inp.C, 1, 7, 7, dtype=dt, device=dev, requires_grad=True)
+    arm = args.arm_only.replace("_infer", "")
+    train = not args.arm_only.endswith("_infer")
+    for _ in range(args.warmup + args.steps):
+        with torch.set_grad_enabled(train):
+            if arm == "fused":
+                y = layer.WTConv2dFunction.apply(x, *ps, inp.levels, inp.k)
+            elif arm == "unfused":
+                y = unfused_torch_layer(x, *ps, inp.levels, inp.k)
+            else:
+                y = F.conv2d(x, w7, padding=3, groups=inp.C)
+        if train:
+            y.backward(dy)
+    torch.cuda.synchronize()
+
+
+PAGES_CONTEXT = ("pages (RTX A6000, context only): training 3.71-4.35x fp32 / 2.68-3.09x fp16 faster than "
+                 "the reference, 1.83-2.31x less peak memory, 1.27-1.50x (fp32) / 1.40-1.76x (fp16) faster "
+                 "than a depthwise 7x7; inference 3.67-4.37x fp32 / 3.38-3.60x fp16 vs the reference")
+
+
 def run_reference(args, world, rank):
     """The oracle on the host cores, each step a bounded sample of the workload."""
     if rank != 0:
@@ -362,6 +524,15 @@ def run_ours(args, world, rank, local):
                                 "kind": "oracle",
                                 "sample": f"one fwd+bwd of the float64 oracle over {n_img} of {inp.N} images "
                                           f"(single thread)"}
+    if world == 1 and not args.no_compare:
+        comps = []
+        for name, dtype in ((WORKLOAD, None), (WORKLOAD, "f16")):
+            try:
+                w_inp = synth.workload(name, **({"dtype": dtype} if dtype else {}))
+                comps.append(compare_arms(w_inp, dev))
+            except Exception as exc:  # a comparison arm must not sink the bench line
+                comps.append({"workload": name, "dtype": dtype, "error": repr(exc)[:200]})
+        line["comparisons"] = {"arms": comps, "context": PAGES_CONTEXT}
     print(json.dumps(line), flush=True)
     return line
 
@@ -374,10 +545,18 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-compare", action="store_true",
+                    help="skip the unfused-PyTorch and depthwise-7x7 comparison arms")
+    ap.add_argument("--arm-only", default=None,
+                    choices=["fused", "unfused", "dw7x7", "fused_infer", "unfused_infer", "dw7x7_infer"],
+                    help="run only this arm's training step or forward (steps + warmup times, no JSON); "
+                         "for profilers")
     ap.add_argument("--cpu-dist", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     world, rank, local = setup_dist(args)
-    if args.impl == "reference":
+    if args.arm_only:
+        run_arm_only(args)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_ours(args, world, rank, local)

@@ -324,3 +324,23 @@ def test_rejects_even_kernel():
     inp.k = 4
     with pytest.raises(ValueError):
         oracle.fwd(inp)
+
+
+# ------------------------------------------- comparison arm of the bench --
+
+@pytest.mark.parametrize("shape", [(2, 3, 9, 7, 2, 5), (1, 2, 13, 10, 3, 3), (1, 2, 8, 8, 1, 5)])
+def test_bench_unfused_arm_equals_oracle(shape):
+    """bench.py's unfused PyTorch composition (a timing comparison arm) computes
+    the same layer and gradients as the oracle, so its timings compare like with
+    like."""
+    import bench
+    inp = synth.make_inputs(*shape, seed=sum(shape) + 5)
+    t = lambda a: torch.tensor(np.asarray(a, np.float64), requires_grad=True)
+    leaves = [t(a) for a in (inp.x, inp.w_base, inp.b_base, inp.w_sub, inp.base_scale, inp.wavelet_scale)]
+    y = bench.unfused_torch_layer(*leaves, inp.levels, inp.k)
+    assert rel(oracle.fwd(inp), y.detach().numpy()) < 1e-13
+    (y * torch.tensor(inp.dy, dtype=torch.float64)).sum().backward()
+    got = oracle.bwd(inp)
+    assert rel(got["dx"], leaves[0].grad.numpy()) < 1e-12
+    assert rel(got["dw_sub"], leaves[3].grad.numpy()) < 1e-12
+    assert rel(got["dwavelet_scale"], leaves[5].grad.numpy()) < 1e-12
