@@ -349,6 +349,123 @@ def run_arm_only(args):
     torch.cuda.synchronize()
 
 
+def time_events(fn, flush, reps):
+    """Median CUDA-event time (ms) of fn over reps runs, L2 flushed before each."""
+    import torch
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def run_suite(args):
+    """The shape/level sweep (WTConvNeXt-T stage shapes x levels 1-5, N=128, fp32
+    and fp16, a cuDNN depthwise 7x7 timed on the same x) or the 18 WTConv layers
+    of WTConvNeXt-T at batch 128 in fp16 (summed fwd+bwd time and peak device
+    memory, fused vs the unfused PyTorch composition).  One JSON line."""
+    import torch
+    import torch.nn.functional as F
+
+    from memory_bound_cnn_wtconv2d_gb300 import build, layer, wtconv
+
+    build.build()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+    reps = max(args.steps, 5)
+
+    def fused_step(x, dy, ps, L, k, out):
+        def run():
+            wtconv.wtconv_fwd(x, *ps, L, k, y=out["y"])
+            wtconv.wtconv_bwd_data(dy, ps[0], ps[2], ps[3], ps[4], L, k, dx=out["dx"])
+            wtconv.wtconv_bwd_weight(x, dy, *ps, L, k, grads=out["g"], workspace=out["ws"])
+        return run
+
+    def buffers(x, ps, L, k):
+        desc = wtconv.desc_for(x, L, k)
+        return {"y": torch.empty_like(x), "dx": torch.empty_like(x),
+                "g": dict(dw_base=torch.empty_like(ps[0]), db_base=torch.empty_like(ps[1]),
+                          dw_sub=torch.empty_like(ps[2]), dbase_scale=torch.empty_like(ps[3]),
+                          dwavelet_scale=torch.empty_like(ps[4])),
+                "ws": torch.empty(max(wtconv.wtconv_workspace_size(desc, wtconv.OP_BWD_WEIGHT), 256),
+                                  dtype=torch.uint8, device=dev)}
+
+    rows = []
+    if args.suite == "sweep":
+        N = 128
+        for dtype in ("f32", "f16"):
+            for C, H in synth.SWEEP_SHAPES:
+                base = synth.make_inputs(N, C, H, H, 1, 5, dtype=dtype, seed=3000 + C)
+                x = torch.tensor(base.x, dtype=tdt[dtype], device=dev)
+                dy = torch.tensor(base.dy, dtype=tdt[dtype], device=dev)
+                w7 = torch.zeros(C, 1, 7, 7, dtype=tdt[dtype], device=dev, requires_grad=True)
+
+                def dw7():
+                    xg = x.detach().requires_grad_(True)
+                    F.conv2d(xg, w7, padding=3, groups=C).backward(dy)
+                t7 = time_events(dw7, flush, reps)
+                for L in synth.SWEEP_LEVELS:
+                    pin = synth.make_inputs(1, C, 1, 1, L, 5, dtype=dtype, seed=3000 + 10 * C + L)
+                    ps = [torch.tensor(a, dtype=torch.float32, device=dev) for a in
+                          (pin.w_base, pin.b_base, pin.w_sub, pin.base_scale, pin.wavelet_scale)]
+                    t = time_events(fused_step(x, dy, ps, L, 5, buffers(x, ps, L, 5)), flush, reps)
+                    ne = x.numel()
+                    rows.append({"C": C, "H": H, "L": L, "dtype": dtype, "fused_fwd_bwd_ms": round(t, 4),
+                                 "dw7x7_cudnn_fwd_bwd_ms": round(t7, 4), "speedup_vs_dw7x7": round(t7 / t, 3),
+                                 "hbm_tbs": round(6 * ne * x.element_size() / (t * 1e-3) / 1e12, 3)})
+                del x, dy
+        line = {"suite": "sweep", "metric": "fwd+bwd ms per layer", "n": N, "rows": rows}
+    else:
+        N, dtype = 128, "f16"
+        tot_fused = tot_unf = 0.0
+        peak = {"fused": 0, "unfused_torch": 0}
+        for C, H, depth, L in synth.NETWORK_STAGES:
+            inp = synth.make_inputs(N, C, H, H, L, 5, dtype=dtype, seed=4000 + C)
+            x = torch.tensor(inp.x, dtype=tdt[dtype], device=dev)
+            dy = torch.tensor(inp.dy, dtype=tdt[dtype], device=dev)
+            ps = [torch.tensor(a, dtype=torch.float32, device=dev) for a in
+                  (inp.w_base, inp.b_base, inp.w_sub, inp.base_scale, inp.wavelet_scale)]
+            pdt = [p.to(tdt[dtype]) for p in ps]
+            t = time_events(fused_step(x, dy, ps, L, 5, buffers(x, ps, L, 5)), flush, reps)
+
+            def unf():
+                xg = x.detach().requires_grad_(True)
+                leaves = [p.detach().clone().requires_grad_(True) for p in pdt]
+                unfused_torch_layer(xg, *leaves, L, 5).backward(dy)
+
+            def fus():
+                xg = x.detach().requires_grad_(True)
+                leaves = [p.detach().clone().requires_grad_(True) for p in ps]
+                layer.WTConv2dFunction.apply(xg, *leaves, L, 5).backward(dy)
+            tu = time_events(unf, flush, reps)
+            for name, fn in (("fused", fus), ("unfused_torch", unf)):
+                torch.cuda.synchronize()
+                torch.cuda.empty_cache()
+                torch.cuda.reset_peak_memory_stats(dev)
+                fn()
+                torch.cuda.synchronize()
+                peak[name] = max(peak[name], int(torch.cuda.max_memory_allocated(dev)))
+            rows.append({"C": C, "H": H, "depth": depth, "L": L, "fused_fwd_bwd_ms": round(t, 4),
+                         "unfused_torch_fwd_bwd_ms": round(tu, 4)})
+            tot_fused += depth * t
+            tot_unf += depth * tu
+            del x, dy
+        line = {"suite": "network", "metric": "summed fwd+bwd ms of the 18 WTConv layers (batch 128, fp16)",
+                "fused_ms": round(tot_fused, 3), "unfused_torch_ms": round(tot_unf, 3),
+                "speedup": round(tot_unf / tot_fused, 3), "peak_device_bytes": peak,
+                "peak_mem_reduction": round(peak["unfused_torch"] / max(peak["fused"], 1), 3), "rows": rows}
+    print(json.dumps(line), flush=True)
+
+
 PAGES_CONTEXT = ("pages (RTX A6000, context only): training 3.71-4.35x fp32 / 2.68-3.09x fp16 faster than "
                  "the reference, 1.83-2.31x less peak memory, 1.27-1.50x (fp32) / 1.40-1.76x (fp16) faster "
                  "than a depthwise 7x7; inference 3.67-4.37x fp32 / 3.38-3.60x fp16 vs the reference")
@@ -547,6 +664,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the unfused-PyTorch and depthwise-7x7 comparison arms")
+    ap.add_argument("--suite", choices=["sweep", "network"], default=None,
+                    help="time the shape/level sweep or the 18-layer network instead of the bench step")
     ap.add_argument("--arm-only", default=None,
                     choices=["fused", "unfused", "dw7x7", "fused_infer", "unfused_infer", "dw7x7_infer"],
                     help="run only this arm's training step or forward (steps + warmup times, no JSON); "
@@ -554,7 +673,9 @@ def main(argv=None):
     ap.add_argument("--cpu-dist", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     world, rank, local = setup_dist(args)
-    if args.arm_only:
+    if args.suite:
+        run_suite(args)
+    elif args.arm_only:
         run_arm_only(args)
     elif args.impl == "reference":
         run_reference(args, world, rank)

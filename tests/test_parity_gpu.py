@@ -186,3 +186,44 @@ def test_level_sweep_shapes(wt, C, H, L):
     # the sweep's (C, H=W, L) shapes at a reduced batch (every plane is
     # independent, so the batch size does not change the per-plane path)
     check_all(wt, synth.make_inputs(3, C // 8, H, H, L, 5, seed=C + H + L))
+
+
+# The largest planes each pass of this build handles (shared memory per CTA for
+# the forward / input-gradient pass; register-resident gradient tiles for the
+# parameter-gradient pass), and the deepest pyramids (L = 8: the coarse levels
+# are 1x1 planes of zero-padded blocks).
+@pytest.mark.parametrize("N,C,H,W,L,k", [(1, 2, 104, 104, 3, 3), (1, 2, 96, 96, 5, 9), (1, 2, 100, 100, 8, 3),
+                                         (1, 2, 3, 512, 1, 5), (2, 3, 92, 92, 8, 9)])
+def test_forward_and_input_gradient_at_maximum_plane(wt, N, C, H, W, L, k):
+    inp = synth.make_inputs(N, C, H, W, L, k, seed=H + W + L + k)
+    d = to_dev(inp)
+    y = wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], L, k)
+    dx = wt.wtconv_bwd_data(d["dy"], d["w_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], L, k)
+    torch.cuda.synchronize()
+    assert wt.wtconv_device_faults() == 0
+    compare("y", y.cpu().numpy(), oracle.fwd(inp), "f32", False)
+    compare("dx", dx.cpu().numpy(), oracle.bwd(inp)["dx"], "f32", False)
+
+
+@pytest.mark.parametrize("N,C,H,W,L,k", [(1, 2, 56, 56, 8, 9), (2, 2, 64, 64, 1, 5), (1, 3, 3, 256, 3, 5),
+                                         (2, 2, 56, 55, 5, 7)])
+def test_all_passes_at_maximum_gradient_plane(wt, N, C, H, W, L, k):
+    check_all(wt, synth.make_inputs(N, C, H, W, L, k, seed=H + W + L + k))
+
+
+def test_planes_beyond_the_limits_are_refused(wt):
+    inp = synth.make_inputs(1, 2, 113, 113, 1, 5, seed=1)
+    d = to_dev(inp)
+    with pytest.raises(wt.WtconvError) as e:
+        wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 1, 5)
+    assert e.value.status == wt.WTCONV_ERR_UNSUPPORTED
+    inp = synth.make_inputs(1, 2, 57, 57, 3, 5, seed=2)
+    d = to_dev(inp)
+    with pytest.raises(wt.WtconvError) as e:
+        wt.wtconv_bwd_weight(d["x"], d["dy"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"],
+                             d["wavelet_scale"], 3, 5)
+    assert e.value.status == wt.WTCONV_ERR_UNSUPPORTED
+    # the refusals launched nothing and left the context usable
+    y = wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 3, 5)
+    torch.cuda.synchronize()
+    compare("y", y.cpu().numpy(), oracle.fwd(inp), "f32", False)
