@@ -358,6 +358,20 @@ void set_load_divs(Plan& pl, const wtconv_desc_t* d, int vec) {
   pl.ld_w = make_div(per_row);
 }
 
+// 16-bit planes stream in by one bulk copy each when a plane is a whole
+// number of 16-byte chunks and the tensor is 16-byte aligned.
+template <typename Plan>
+void set_bulk(Plan& pl, const wtconv_desc_t* d, const void* src, long capacity_bytes) {
+  const long plane = 2L * d->H * d->W;
+  pl.use_bulk = d->dtype != WTCONV_F32 && plane % 16 == 0 && aligned(src, 16) &&
+                plane * pl.P <= capacity_bytes && plane * pl.P < (1L << 20);
+  pl.bulk_bytes = (uint32_t)plane;
+  pl.wd_vec = d->W % 4 == 0;
+  const int per_row = pl.wd_vec ? d->W / 4 : d->W;
+  pl.wd_pp = make_div(d->H * per_row);
+  pl.wd_w = make_div(per_row);
+}
+
 size_t bw_workspace_bytes(const WtBwPlan& pl) {
   const size_t bytes = (size_t)pl.grid * pl.nrec * pl.part_stride * sizeof(float);
   return (bytes + 255) / 256 * 256;
@@ -406,6 +420,7 @@ wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float
   alignas(64) CUtensorMap tmx;
   memset(&tmx, 0, sizeof(tmx));
   pl.use_tma = encode_plane_map(&tmx, x, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
+  set_bulk(pl, desc, x, pl.nsets == 2 ? 4L * pl.xslot : 0);
   cudaError_t e = wt::launch_fwd(pl, tmx, desc->dtype, false, x, w_base, b_base, w_sub, base_scale,
                                  wavelet_scale, y, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_fwd: %s", cudaGetErrorString(e));
@@ -432,6 +447,7 @@ wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const
   alignas(64) CUtensorMap tmx;
   memset(&tmx, 0, sizeof(tmx));
   pl.use_tma = encode_plane_map(&tmx, dy, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
+  set_bulk(pl, desc, dy, pl.nsets == 2 ? 4L * pl.xslot : 0);
   cudaError_t e = wt::launch_fwd(pl, tmx, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale,
                                  wavelet_scale, dx, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_data: %s", cudaGetErrorString(e));

@@ -323,6 +323,39 @@ __device__ __forceinline__ void haar_levels12(const float* sbase, int sps, float
   }
 }
 
+// Widen np raw 16-bit planes (H*W elements each, consecutive in `src`, as the
+// bulk copies leave them) into the float32 interiors of buffer B of each
+// plane slot.  `vec`: W % 4 == 0, 4 elements per item (8-byte loads, 16-byte
+// stores: B.pcol and B.stride are multiples of 4); else one element per item.
+template <typename T>
+__device__ __forceinline__ void widen_planes(float* dbase, int dps, const WtBuf B, const T* src, int np, int H,
+                                             int W, bool vec, const WtDiv& dpp, const WtDiv& dw, int tid,
+                                             int nthreads) {
+  const int HW = H * W;
+  if (vec) {
+    const int Wv = W >> 2;
+    const int per_plane = H * Wv;
+    for (int it = tid; it < np * per_plane; it += nthreads) {
+      const int g = fdiv(it, dpp);
+      const int rem = it - g * per_plane;
+      const int i = fdiv(rem, dw);
+      const int j = (rem - i * Wv) << 2;
+      const uint2 raw = *reinterpret_cast<const uint2*>(src + g * HW + i * W + j);
+      const T* h = reinterpret_cast<const T*>(&raw);
+      *reinterpret_cast<float4*>(dbase + g * dps + B.off + (i + B.prow) * B.stride + j + B.pcol) =
+          make_float4(to_f32(h[0]), to_f32(h[1]), to_f32(h[2]), to_f32(h[3]));
+    }
+  } else {
+    for (int it = tid; it < np * HW; it += nthreads) {
+      const int g = fdiv(it, dpp);
+      const int rem = it - g * HW;
+      const int i = fdiv(rem, dw);
+      const int j = rem - i * W;
+      dbase[g * dps + B.off + (i + B.prow) * B.stride + j + B.pcol] = to_f32(src[it]);
+    }
+  }
+}
+
 // Copy planes n0 .. n0+np-1 of channel c from global memory into the
 // interiors of buffer B of each plane slot.
 template <typename T>
@@ -467,6 +500,14 @@ __device__ __forceinline__ void tma_load_4d(float* dst, const CUtensorMap* map, 
       " [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(mbar))
       : "memory");
+}
+
+// Contiguous global -> shared bulk copy (both addresses 16-byte aligned, size
+// a multiple of 16); completes `bytes` of transaction on mbar.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+               ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(mbar))
+               : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* mbar, uint32_t parity) {

@@ -117,21 +117,38 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes);
     tma_load_4d(sm + s * pl.xslot, &tmx, -4, -R, cc, nn, &mbar[s]);
   };
+  // 16-bit bulk path: the raw planes of a unit land, one bulk copy per plane,
+  // in the second input set (unused by 16-bit units); they are widened into
+  // the first set at the start of the unit, after which the next unit's copy
+  // is issued.  One mbarrier (mbar[0]).
+  const bool bulk = !ASYNC && pl.use_bulk;
+  T* const stage = reinterpret_cast<T*>(sm + pl.xslot);
+  const int HWp = pl.H * pl.W;
+  auto issue_bulk = [&](int uu) {
+    const int cc = uu / pl.groups;
+    const int nn = (uu - cc * pl.groups) * pl.P;
+    const int npp = min(pl.P, pl.N - nn);
+    fence_proxy_async();  // the widening reads of the staging area precede the copies
+    mbar_arrive_expect_tx(&mbar[0], (uint32_t)npp * pl.bulk_bytes);
+    for (int g = 0; g < npp; ++g)
+      bulk_load(stage + g * HWp, x + ((size_t)(nn + g) * C + cc) * HWp, pl.bulk_bytes, &mbar[0]);
+  };
 
   // Zero margins once (the box copies write whole padded planes themselves).
   if (tma) zero_smem(sm + pl.work_off, pl.w_off - pl.work_off, tid, NT);
   else zero_smem(sm, pl.w_off, tid, NT);
-  if (tma && tid == 0) {
+  if ((tma || bulk) && tid == 0) {
     mbar_init(&mbar[0], 1);
     mbar_init(&mbar[1], 1);
     fence_mbar_init();
   }
   __syncthreads();  // the zero fill and barrier init land before any plane copy
   if (tma && tid == 0 && u_begin < u_end) issue(u_begin, 0);
+  if (bulk && tid == 0 && u_begin < u_end) issue_bulk(u_begin);
   int c_prev = -1;
   int slot = 0;
   const bool dbl = pl.nsets == 2;
-  for (int u = u_begin; u < u_end; ++u, slot = dbl ? slot ^ 1 : 0) {
+  for (int u = u_begin; u < u_end; ++u, slot = (dbl && !bulk) ? slot ^ 1 : 0) {
     const int c = u / pl.groups;
     const int n0 = (u - c * pl.groups) * pl.P;
     const int np = min(pl.P, pl.N - n0);
@@ -146,6 +163,11 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
         parity ^= 1u << slot;
         if (ok && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
         s_ok = ok;
+      }
+    } else if (bulk) {
+      if (tid == 0) {
+        s_ok = mbar_wait_bounded(&mbar[0], parity & 1u);
+        parity ^= 1u;
       }
     } else if (!ASYNC) {
       load_planes<T>(xs, XF, pl.lev[0], x, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
@@ -166,13 +188,19 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     }
     const float bias = (!ROT && b_base != nullptr) ? s_base[c] * b_base[c] : 0.f;
     __syncthreads();  // planes of unit u and the weights are visible
-    if (tma && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
+    if ((tma || bulk) && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
+      const int mb = bulk ? 0 : slot;
       if (tid == 0) {
         atomicAdd(&g_fwd_faults, 1u);
-        mbar_wait_bounded(&mbar[slot], ((parity >> slot) & 1u) ^ 1u);  // let the copy in flight land
+        mbar_wait_bounded(&mbar[mb], ((parity >> mb) & 1u) ^ 1u);  // let the copy in flight land
       }
       __syncthreads();
       break;
+    }
+    if (bulk) {  // widen the raw planes, then start the next unit's copy
+      widen_planes<T>(xs, XF, pl.lev[0], stage, np, pl.H, pl.W, pl.wd_vec != 0, pl.wd_pp, pl.wd_w, tid, NT);
+      __syncthreads();
+      if (tid == 0 && u + 1 < u_end) issue_bulk(u + 1);
     }
 
     // (1) Haar pyramid on chip.

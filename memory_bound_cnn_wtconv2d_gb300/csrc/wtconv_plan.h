@@ -61,6 +61,10 @@ struct WtFwdPlan {
   int vec_ok;            // rows can use 16-byte global accesses (W % elems-per-16B == 0)
   int use_tma;           // input planes arrive by TMA box copies (float32, 16-byte rows)
   uint32_t tma_bytes;    // bytes of one box (P planes)
+  int use_bulk;          // 16-bit planes arrive by bulk copies into the second input set, then widen
+  uint32_t bulk_bytes;   // bytes of one raw 16-bit plane (H*W*2, a multiple of 16)
+  int wd_vec;            // widening works on 4-element items (W % 4 == 0)
+  WtDiv wd_pp, wd_w;     // widening: items per plane, items per row
   WtDiv ld_pp, ld_w;     // plane load: items per plane, items per row
   WtDiv an_pp[WT_MAXL + 1], an_w[WT_MAXL + 1];  // analysis at level l (l = 2: the fused 1+2 pass)
   WtDiv z_ipp;                                  // band-convolution items per plane
