@@ -180,12 +180,18 @@ void bw_tiles(const wtconv_desc_t* d, WtBwPlan& pl, int tbr) {
 // Shared-memory layout of the parameter-gradient pass for `nsets` input sets:
 // [input sets][P work areas, or the end-of-channel reduction if larger]
 // [mbarriers].  TMA destinations are 128-byte aligned.
-void bw_layout(WtBwPlan& pl, int nsets) {
+void bw_layout(WtBwPlan& pl, int nsets, bool staging) {
   const int P = pl.P, KK = pl.K * pl.K;
   pl.nsets = nsets;
   pl.xr = round_up(P * pl.xbf, 32);
   pl.islot = pl.xr + round_up(P * pl.dbf, 32);
-  pl.work_off = nsets * pl.islot;
+  pl.stage_off = 0;
+  int off = nsets * pl.islot;
+  if (staging) {  // raw 16-bit x and dy planes of one unit: P * H * W * 2 halves = P * H * W floats
+    pl.stage_off = off;
+    off += round_up(P * pl.H * pl.W, 32);
+  }
+  pl.work_off = off;
   long region = (long)P * pl.wf;
   const long red = (long)P * pl.items_per_plane * (KK + 1);  // end-of-channel reduction (reuses the work area)
   if (red > region) region = red;
@@ -237,9 +243,13 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
   if (d->N > 0 && P > d->N) P = d->N;
   if (P < 1) P = 1;
   pl.P = P;
-  bw_layout(pl, 2);
+  // 16-bit planes that are whole 16-byte chunks get a staging area for bulk
+  // copies (used when the tensors are 16-byte aligned).
+  const bool staging = d->dtype != WTCONV_F32 && (2L * d->H * d->W) % 16 == 0 &&
+                       2L * d->H * d->W * P * 2 < (1L << 20);
+  bw_layout(pl, 2, false);
   if (pl.smem_bytes > kMaxSmemPerBlock) {
-    bw_layout(pl, 1);
+    bw_layout(pl, 1, false);
     if (pl.smem_bytes > kMaxSmemPerBlock)
       return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %d B of shared memory (max %d)",
                   d->H, d->W, L, pl.smem_bytes, kMaxSmemPerBlock);
@@ -268,7 +278,10 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
     return n < 1 ? 1 : n;
   };
   // 16-bit activations are loaded synchronously, so they need one input set.
-  if (d->dtype != WTCONV_F32 && pl.nsets == 2) bw_layout(pl, 1);
+  if (d->dtype != WTCONV_F32) {
+    bw_layout(pl, 1, staging);
+    if (pl.smem_bytes > kMaxSmemPerBlock) bw_layout(pl, 1, false);
+  }
   const int per_sm = per_sm_of(pl);
   // Persistent grid: every resident CTA slot, at most one CTA per unit.
   pl.batches = d->N > 0 ? ceil_div(d->N, P) : 0;
@@ -490,6 +503,7 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
     return fail(WTCONV_ERR_WORKSPACE, "workspace of %zu B given, %zu B needed", ws ? ws_bytes : 0, need);
   if (!aligned(ws, 256)) return fail(WTCONV_ERR_MISALIGNED, "workspace is not 256-byte aligned");
   set_load_divs(pl, desc, vec_ok(desc, x, dy));
+  set_bulk(pl, desc, x, pl.stage_off > 0 && aligned(dy, 16) ? 4L * (pl.work_off - pl.stage_off) / 2 : 0);
   alignas(64) CUtensorMap tmx, tmd;
   memset(&tmx, 0, sizeof(tmx));
   memset(&tmd, 0, sizeof(tmd));

@@ -76,6 +76,25 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
     tma_load_4d(dst, &tmx, -4, -R, cc, n0, &mbar[s]);
     tma_load_4d(dst + pl.xr, &tmd, 0, 0, cc, n0, &mbar[s]);
   };
+  // 16-bit bulk path: a unit's raw x and dy planes land in the staging area
+  // (one bulk copy per plane) on mbar[0]; the unit widens them into its input
+  // set, after which the next unit's copies are issued.
+  const bool bulk = !ASYNC && pl.use_bulk;
+  const int HWp = pl.H * pl.W;
+  T* const stage_x = reinterpret_cast<T*>(sm + pl.stage_off);
+  T* const stage_d = stage_x + P * HWp;
+  auto issue_bulk = [&](int u) {
+    const int cc = unit_c(u);
+    const int n0 = (u - cc * NB) * P;
+    const int npp = min(P, pl.N - n0);
+    fence_proxy_async();  // the widening reads of the staging area precede the copies
+    mbar_arrive_expect_tx(&mbar[0], 2u * (uint32_t)npp * pl.bulk_bytes);
+    for (int g = 0; g < npp; ++g) {
+      const size_t src = ((size_t)(n0 + g) * C + cc) * HWp;
+      bulk_load(stage_x + g * HWp, x + src, pl.bulk_bytes, &mbar[0]);
+      bulk_load(stage_d + g * HWp, dy + src, pl.bulk_bytes, &mbar[0]);
+    }
+  };
   auto load_async = [&](int u, int s) {
     const int cc = unit_c(u);
     const int n0 = (u - cc * NB) * P;
@@ -101,7 +120,7 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
 #pragma unroll
     for (int t = 0; t < KK; ++t) acc[s][t] = 0.f;
   }
-  if (tma && tid == 0) {
+  if ((tma || bulk) && tid == 0) {
     mbar_init(&mbar[0], 1);
     mbar_init(&mbar[1], 1);
     fence_mbar_init();
@@ -110,6 +129,8 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
 
   if (tma) {
     if (tid == 0 && u_begin < u_end) issue(u_begin, 0);
+  } else if (bulk) {
+    if (tid == 0 && u_begin < u_end) issue_bulk(u_begin);
   } else if (ASYNC && dbl && u_begin < u_end) {  // first unit
     load_async(u_begin, 0);
     cp_async_wait_all();
@@ -131,6 +152,11 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
           if (ok && dbl && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
           s_ok = ok;
         }
+      } else if (bulk) {
+        if (tid == 0) {
+          s_ok = mbar_wait_bounded(&mbar[0], parity & 1u);
+          parity ^= 1u;
+        }
       } else if (!ASYNC || !dbl) {
         load_planes<T>(in_x, XBF, pl.xs[0], x, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
         load_planes<T>(in_d, DBF, pl.ds[0], dy, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
@@ -138,13 +164,20 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
         load_async(u + 1, slot ^ 1);
       }
       __syncthreads();  // this unit's planes are visible
-      if (tma && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
+      if ((tma || bulk) && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
+        const int mb = bulk ? 0 : slot;
         if (tid == 0) {
           atomicAdd(&g_bw_faults, 1u);
-          mbar_wait_bounded(&mbar[slot], ((parity >> slot) & 1u) ^ 1u);  // let the copy in flight land
+          mbar_wait_bounded(&mbar[mb], ((parity >> mb) & 1u) ^ 1u);  // let the copy in flight land
         }
         __syncthreads();
         return;  // records are not written: the caller sees the fault count
+      }
+      if (bulk) {  // widen the raw planes, then start the next unit's copies
+        widen_planes<T>(in_x, XBF, pl.xs[0], stage_x, np, pl.H, pl.W, pl.wd_vec != 0, pl.wd_pp, pl.wd_w, tid, NT);
+        widen_planes<T>(in_d, DBF, pl.ds[0], stage_d, np, pl.H, pl.W, pl.wd_vec != 0, pl.wd_pp, pl.wd_w, tid, NT);
+        __syncthreads();
+        if (tid == 0 && u + 1 < u_end) issue_bulk(u + 1);
       }
 
       // Both pyramids: levels 1+2 fused, then 3..L.

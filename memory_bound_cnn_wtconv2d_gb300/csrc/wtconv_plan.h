@@ -108,6 +108,11 @@ struct WtBwPlan {
   int smem_bytes;
   int use_tma;           // input planes arrive by TMA box copies (float32, 16-byte rows)
   uint32_t tma_bytes;    // bytes of one input set (x and dy boxes)
+  int stage_off;         // 16-bit staging area (raw x planes, then raw dy planes), floats; 0 = none
+  int use_bulk;          // 16-bit planes arrive by bulk copies into the staging area, then widen
+  uint32_t bulk_bytes;   // bytes of one raw 16-bit plane (H*W*2, a multiple of 16)
+  int wd_vec;            // widening works on 4-element items (W % 4 == 0)
+  WtDiv wd_pp, wd_w;     // widening: items per plane, items per row
   int nbands;            // 1 + 4L
   int part_stride;       // floats per (group, channel) partial record = nbands*(k*k+1)
   int vec_ok;
