@@ -110,11 +110,11 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   }
   pl.zipp = pl.zbegin[L + 1];
   for (int l = 1; l <= L; ++l) {
-    // Z^l: written on the band-convolution grid, read by the final tiles at
-    // (p >> (l-1), q >> (l-1)) for every level-1 position of the tile grid.
-    const int zr = WT_ZT * pl.ztr[l], zc = WT_ZT * pl.ztc[l];
+    // Z^l: written at the valid positions (p < H_l, q < W_l) only, read by
+    // the final tiles at (p >> (l-1), q >> (l-1)) for every level-1 position
+    // of the tile grid; rows/columns read but never written stay zero.
     const int fr = ((WT_TP * pl.ftr - 1) >> (l - 1)) + 1, fc = ((WT_TQ * pl.ftc - 1) >> (l - 1)) + 1;
-    off = place(pl.zb[l], off, zr > fr ? zr : fr, zc > fc ? zc : fc, 0, 0, 4);
+    off = place(pl.zb[l], off, pl.Hs[l] > fr ? pl.Hs[l] : fr, pl.Ws[l] > fc ? pl.Ws[l] : fc, 0, 0, 4);
   }
   pl.wf = round_up(off, 4);
   pl.w_band = round_up(KK, 4);
