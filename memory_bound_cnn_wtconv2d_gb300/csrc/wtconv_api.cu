@@ -88,18 +88,17 @@ int place(WtBuf& b, int off, int er, int ec, int prow, int pcol, int nb, int min
   return off + nb * b.band;
 }
 
-wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
-  memset(&pl, 0, sizeof(pl));
-  pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
-  const int R = d->k / 2, L = d->levels, KK = d->k * d->k;
-  level_sizes(d, pl.Hs, pl.Ws);
-  pl.ftr = ceil_div(pl.Hs[1], WT_TP);
+// Buffer geometry of the forward pass for final tiles of tp x WT_TQ level-1
+// positions (2tp x 2WT_TQ outputs).
+void fwd_geometry(const wtconv_desc_t* d, WtFwdPlan& pl, int tp) {
+  const int R = d->k / 2, L = d->levels;
+  pl.ftp = tp;
+  pl.ftr = ceil_div(pl.Hs[1], tp);
   pl.ftc = ceil_div(pl.Ws[1], WT_TQ);
   // Input plane (own buffer): R zero rows above, a 4-float (16-byte) left
   // margin so its interior rows are 16-byte aligned.  Rows cover the final
-  // tiles' windows (4*ftr + 2R) and row length covers their reads.
-  pl.xf = round_up(place(pl.lev[0], 0, 2 * WT_TP * pl.ftr, 2 * WT_TQ * pl.ftc, R, 4, 1,
-                        2 * WT_TQ * pl.ftc + 8), 4);
+  // tiles' windows (2*tp*ftr + 2R) and row length covers their reads.
+  pl.xf = round_up(place(pl.lev[0], 0, 2 * tp * pl.ftr, 2 * WT_TQ * pl.ftc, R, 4, 1, 2 * WT_TQ * pl.ftc + 8), 4);
   int off = 0;  // work area: pyramid levels 1..L, then convolved bands
   pl.zbegin[1] = 0;
   for (int l = 1; l <= L; ++l) {
@@ -113,10 +112,18 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
     // Z^l: written at the valid positions (p < H_l, q < W_l) only, read by
     // the final tiles at (p >> (l-1), q >> (l-1)) for every level-1 position
     // of the tile grid; rows/columns read but never written stay zero.
-    const int fr = ((WT_TP * pl.ftr - 1) >> (l - 1)) + 1, fc = ((WT_TQ * pl.ftc - 1) >> (l - 1)) + 1;
+    const int fr = ((tp * pl.ftr - 1) >> (l - 1)) + 1, fc = ((WT_TQ * pl.ftc - 1) >> (l - 1)) + 1;
     off = place(pl.zb[l], off, pl.Hs[l] > fr ? pl.Hs[l] : fr, pl.Ws[l] > fc ? pl.Ws[l] : fc, 0, 0, 4);
   }
   pl.wf = round_up(off, 4);
+}
+
+wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
+  memset(&pl, 0, sizeof(pl));
+  pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
+  const int L = d->levels, KK = d->k * d->k;
+  level_sizes(d, pl.Hs, pl.Ws);
+  fwd_geometry(d, pl, WT_TP);
   pl.w_band = round_up(KK, 4);
   const int wfloats = (1 + 4 * L) * pl.w_band;
   // Two input sets: float32 planes stream into one while the other is
@@ -133,6 +140,10 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   const int fit = (int)((kFwdBudget - 4L * wfloats) / plane_bytes);
   if (P > fit) P = fit < 1 ? 1 : fit;
   if (d->N > 0 && P > d->N) P = d->N;
+  // Final tiles of half the height when the full ones would leave more than
+  // half of the CTA's threads without a tile (small planes): twice the items,
+  // each half as long.  Never larger in shared memory.
+  if ((long)P * items * 2 <= WT_FWD_THREADS) fwd_geometry(d, pl, WT_TP / 2);
   pl.P = P;
   pl.groups = d->N > 0 ? ceil_div(d->N, P) : 0;
   pl.xslot = round_up(P * pl.xf, 32);  // 128-byte aligned buffer sets (TMA destinations)

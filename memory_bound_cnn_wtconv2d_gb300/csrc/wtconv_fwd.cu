@@ -80,6 +80,116 @@ __device__ __forceinline__ void stage_weights(float* wsm, int wb, int L, int C, 
 // while the current unit is computed, for float32), one work area per plane
 // (pyramid + convolved bands) and the weights.  It is zeroed once; later
 // writes touch interiors only, so every margin stays zero.
+// Final tiles of one unit: each thread takes TP x TQ level-1 positions =
+// 2TP x 2TQ output pixels (the tile height is a plan choice: TP = 4, or 2
+// for small planes), gathers the coarse levels and the level-1 butterflies
+// of the synthesis, accumulates the base convolution on top and stores y.
+template <int K, typename T, int TP>
+__device__ __forceinline__ void final_tiles(const WtFwdPlan& pl, const float* work, const float* xs, const float* wsm,
+                                            float bias, T* __restrict__ y, int n0, int c, int np, int tid) {
+  constexpr int R = K / 2;
+  constexpr int TQ = WT_TQ;
+  constexpr int NT = WT_FWD_THREADS;
+  const int XF = pl.xf, WF = pl.wf;
+  const WtBuf X = pl.lev[0];
+  const int H = pl.H, W = pl.W, L = pl.L, C = pl.C;
+  const size_t HW = (size_t)H * W;
+  const int per_plane = pl.ftr * pl.ftc;
+  for (int it = tid; it < np * per_plane; it += NT) {
+    const int g = fdiv(it, pl.f_pp);
+    const int rem = it - g * per_plane;
+    const int tp = fdiv(rem, pl.f_c);
+    const int p0 = tp * TP, q0 = (rem - tp * pl.ftc) * TQ;
+    const float* ps = work + g * WF;
+    const float* px = xs + g * XF;
+
+    // Coarse levels 2..L, gathered per level-1 position (p0 + o, q0 + j):
+    // level l contributes the parity value (bit l-2 of p, bit l-2 of q) of
+    // its coefficients at (p >> (l-1), q >> (l-1)).
+    float cc[TP][TQ];
+#pragma unroll
+    for (int o = 0; o < TP; ++o)
+#pragma unroll
+      for (int j = 0; j < TQ; ++j) cc[o][j] = bias;
+    if (L >= 2) {
+      // level 2: rows p0/2 .. p0/2 + TP/2 - 1, column q0/2; parity (o & 1, j)
+      const WtBuf Z2 = pl.zb[2];
+      const float* z2 = ps + Z2.off + (p0 >> 1) * Z2.stride + (q0 >> 1);
+#pragma unroll
+      for (int k = 0; k < TP / 2; ++k) {
+        const float* zk = z2 + k * Z2.stride;
+        float par[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        add_parities(zk[0], zk[Z2.band], zk[2 * Z2.band], zk[3 * Z2.band], par);
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int j = 0; j < TQ; ++j) cc[2 * k + u][j] += par[u][j];
+      }
+    }
+    for (int l = 3; l <= L; ++l) {
+      // one coarse position per tile; column parity fixed, row parity from bit l-2 of p0 + o
+      const WtBuf Zl = pl.zb[l];
+      const float* zl = ps + Zl.off + (p0 >> (l - 1)) * Zl.stride + (q0 >> (l - 1));
+      float par[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      add_parities(zl[0], zl[Zl.band], zl[2 * Zl.band], zl[3 * Zl.band], par);
+      const int v = (q0 >> (l - 2)) & 1;
+#pragma unroll
+      for (int o = 0; o < TP; ++o) {
+        const int u = ((p0 + o) >> (l - 2)) & 1;
+        const float add = u ? (v ? par[1][1] : par[1][0]) : (v ? par[0][1] : par[0][0]);
+#pragma unroll
+        for (int j = 0; j < TQ; ++j) cc[o][j] += add;
+      }
+    }
+
+    // Level 1 per output parity, plus the coarse sum.
+    float out[2 * TP][2 * TQ];
+    const WtBuf Z1 = pl.zb[1];
+#pragma unroll
+    for (int o = 0; o < TP; ++o) {
+      const float* z1 = ps + Z1.off + (p0 + o) * Z1.stride + q0;
+      float2 zr[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) zr[b] = *reinterpret_cast<const float2*>(z1 + b * Z1.band);
+#pragma unroll
+      for (int j = 0; j < TQ; ++j) {
+        float par[2][2] = {{cc[o][j], cc[o][j]}, {cc[o][j], cc[o][j]}};
+        if (j == 0) add_parities(zr[0].x, zr[1].x, zr[2].x, zr[3].x, par);
+        else add_parities(zr[0].y, zr[1].y, zr[2].y, zr[3].y, par);
+        out[2 * o][2 * j] = par[0][0];
+        out[2 * o][2 * j + 1] = par[0][1];
+        out[2 * o + 1][2 * j] = par[1][0];
+        out[2 * o + 1][2 * j + 1] = par[1][1];
+      }
+    }
+
+    // Base convolution from the input plane (interior column 0 sits 4 floats
+    // into each row, so the window starts 4 - r floats after a 16-byte boundary).
+    conv_tile_off<K, 2 * TP, 2 * TQ, 4 - R>(px + X.off + 2 * p0 * X.stride + 2 * q0, X.stride, wsm, out);
+
+    T* plane = y + ((size_t)(n0 + g) * C + c) * HW;
+    const int j0 = 2 * q0;
+    // One 2TQ-wide store per row: 16 bytes (float32) or 8 bytes (16-bit).
+    // Rows start on that boundary when vec_ok (W*sizeof(T) % 16 == 0, base
+    // 16-byte aligned) since j0*sizeof(T) = tile column * 2TQ*sizeof(T).
+    const bool full_row = pl.vec_ok && (j0 + 2 * TQ <= W);
+#pragma unroll
+    for (int oo = 0; oo < 2 * TP; ++oo) {
+      const int i = 2 * p0 + oo;
+      if (i < H) {
+        T* dst = plane + (size_t)i * W + j0;
+        if (full_row) {
+          stg_row<T, 2 * TQ>(dst, out[oo]);
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 2 * TQ; ++jj)
+            if (j0 + jj < W) dst[jj] = from_f32<T>(out[oo][jj]);
+        }
+      }
+    }
+  }
+}
+
 template <int K, typename T, bool ROT>
 __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     fwd_kernel(const __grid_constant__ WtFwdPlan pl, const __grid_constant__ CUtensorMap tmx,
@@ -91,7 +201,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
   float* const sm = align_smem128(sm_raw);  // TMA box destinations need 128-byte alignment
   constexpr int R = K / 2;
   constexpr int NT = WT_FWD_THREADS;
-  constexpr int TP = WT_TP, TQ = WT_TQ, ZT = WT_ZT;
+  constexpr int ZT = WT_ZT;
   constexpr bool ASYNC = sizeof(T) == 4;
   const int tid = threadIdx.x;
   const int C = pl.C, L = pl.L;
@@ -254,104 +364,9 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     }
     __syncthreads();
 
-    // (2) final tiles: TP x TQ level-1 positions = 2TP x 2TQ outputs.
-    const WtBuf X = pl.lev[0];
-    const int H = pl.H, W = pl.W;
-    const size_t HW = (size_t)H * W;
-    const int per_plane = pl.ftr * pl.ftc;
-    for (int it = tid; it < np * per_plane; it += NT) {
-      const int g = fdiv(it, pl.f_pp);
-      const int rem = it - g * per_plane;
-      const int tp = fdiv(rem, pl.f_c);
-      const int p0 = tp * TP, q0 = (rem - tp * pl.ftc) * TQ;
-      const float* ps = work + g * WF;
-      const float* px = xs + g * XF;
-
-      // Coarse levels 2..L, gathered per level-1 position (p0 + o, q0 + j):
-      // level l contributes the parity value (bit l-2 of p, bit l-2 of q) of
-      // its coefficients at (p >> (l-1), q >> (l-1)).
-      float cc[TP][TQ];
-#pragma unroll
-      for (int o = 0; o < TP; ++o)
-#pragma unroll
-        for (int j = 0; j < TQ; ++j) cc[o][j] = bias;
-      if (L >= 2) {
-        // level 2: rows p0/2 and p0/2 + 1, column q0/2; parity (o & 1, j)
-        const WtBuf Z2 = pl.zb[2];
-        const float* z2 = ps + Z2.off + (p0 >> 1) * Z2.stride + (q0 >> 1);
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float* zk = z2 + k * Z2.stride;
-          float par[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-          add_parities(zk[0], zk[Z2.band], zk[2 * Z2.band], zk[3 * Z2.band], par);
-#pragma unroll
-          for (int u = 0; u < 2; ++u)
-#pragma unroll
-            for (int j = 0; j < TQ; ++j) cc[2 * k + u][j] += par[u][j];
-        }
-      }
-      for (int l = 3; l <= L; ++l) {
-        // one coarse position per tile; column parity fixed, row parity from bit l-2 of p0 + o
-        const WtBuf Zl = pl.zb[l];
-        const float* zl = ps + Zl.off + (p0 >> (l - 1)) * Zl.stride + (q0 >> (l - 1));
-        float par[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        add_parities(zl[0], zl[Zl.band], zl[2 * Zl.band], zl[3 * Zl.band], par);
-        const int v = (q0 >> (l - 2)) & 1;
-#pragma unroll
-        for (int o = 0; o < TP; ++o) {
-          const int u = ((p0 + o) >> (l - 2)) & 1;
-          const float add = u ? (v ? par[1][1] : par[1][0]) : (v ? par[0][1] : par[0][0]);
-#pragma unroll
-          for (int j = 0; j < TQ; ++j) cc[o][j] += add;
-        }
-      }
-
-      // Level 1 per output parity, plus the coarse sum.
-      float out[2 * TP][2 * TQ];
-      const WtBuf Z1 = pl.zb[1];
-#pragma unroll
-      for (int o = 0; o < TP; ++o) {
-        const float* z1 = ps + Z1.off + (p0 + o) * Z1.stride + q0;
-        float2 zr[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) zr[b] = *reinterpret_cast<const float2*>(z1 + b * Z1.band);
-#pragma unroll
-        for (int j = 0; j < TQ; ++j) {
-          float par[2][2] = {{cc[o][j], cc[o][j]}, {cc[o][j], cc[o][j]}};
-          if (j == 0) add_parities(zr[0].x, zr[1].x, zr[2].x, zr[3].x, par);
-          else add_parities(zr[0].y, zr[1].y, zr[2].y, zr[3].y, par);
-          out[2 * o][2 * j] = par[0][0];
-          out[2 * o][2 * j + 1] = par[0][1];
-          out[2 * o + 1][2 * j] = par[1][0];
-          out[2 * o + 1][2 * j + 1] = par[1][1];
-        }
-      }
-
-      // Base convolution from the input plane (interior column 0 sits 4 floats
-      // into each row, so the window starts 4 - r floats after a 16-byte boundary).
-      conv_tile_off<K, 2 * TP, 2 * TQ, 4 - R>(px + X.off + 2 * p0 * X.stride + 2 * q0, X.stride, wsm, out);
-
-      T* plane = y + ((size_t)(n0 + g) * C + c) * HW;
-      const int j0 = 2 * q0;
-      // One 2TQ-wide store per row: 16 bytes (float32) or 8 bytes (16-bit).
-      // Rows start on that boundary when vec_ok (W*sizeof(T) % 16 == 0, base
-      // 16-byte aligned) since j0*sizeof(T) = tile column * 2TQ*sizeof(T).
-      const bool full_row = pl.vec_ok && (j0 + 2 * TQ <= W);
-#pragma unroll
-      for (int oo = 0; oo < 2 * TP; ++oo) {
-        const int i = 2 * p0 + oo;
-        if (i < H) {
-          T* dst = plane + (size_t)i * W + j0;
-          if (full_row) {
-            stg_row<T, 2 * TQ>(dst, out[oo]);
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < 2 * TQ; ++jj)
-              if (j0 + jj < W) dst[jj] = from_f32<T>(out[oo][jj]);
-          }
-        }
-      }
-    }
+    // (2) final tiles: base convolution + synthesis + store.
+    if (pl.ftp == WT_TP) final_tiles<K, T, WT_TP>(pl, work, xs, wsm, bias, y, n0, c, np, tid);
+    else final_tiles<K, T, WT_TP / 2>(pl, work, xs, wsm, bias, y, n0, c, np, tid);
     if (ASYNC && !tma) cp_async_wait_all();  // this thread's copies of the next unit have landed
     __syncthreads();                 // ... and all reads of unit u are done
   }  // unit loop

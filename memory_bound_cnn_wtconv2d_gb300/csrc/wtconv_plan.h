@@ -48,7 +48,8 @@ struct WtFwdPlan {
   int ztc[WT_MAXL + 1];
   int zbegin[WT_MAXL + 2];  // first (band, tile) item of level l within a plane; [L+1] = total
   int zipp;                 // band-convolution items per plane
-  int ftr, ftc;             // final tiles (WT_TP x WT_TQ level-1 positions) per plane: rows, columns
+  int ftp;                  // level-1 rows per final tile: WT_TP, or WT_TP / 2 for small planes
+  int ftr, ftc;             // final tiles (ftp x WT_TQ level-1 positions) per plane: rows, columns
   int xf;                // floats per input-plane buffer (= TMA box of one plane)
   int xslot;             // floats per input buffer set (P planes, 128-byte multiple)
   int nsets;             // input sets: 2 (float32: the next unit streams in meanwhile) or 1
