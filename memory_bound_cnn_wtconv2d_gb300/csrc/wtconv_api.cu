@@ -35,6 +35,7 @@ wtconv_status_t ok() {
 constexpr int kMaxSmemPerBlock = 232448;  // 227 KiB opt-in shared memory per CTA on sm_103
 constexpr int kSmemPerSm = 233472;        // 228 KiB shared memory per SM
 constexpr int kNumSms = 152;              // GB300; only a grid-shaping heuristic
+constexpr int kStaticSmem = 16;            // static shared memory of the kernels (a flag word)
 constexpr int kFwdBudget = 72 * 1024;     // preferred forward CTA footprint (>= 3 CTAs / SM)
 constexpr int kBwBudget = 112 * 1024;     // preferred gradient CTA footprint (>= 2 CTAs / SM)
 
@@ -147,7 +148,25 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   pl.P = P;
   pl.groups = d->N > 0 ? ceil_div(d->N, P) : 0;
   pl.xslot = round_up(P * pl.xf, 32);  // 128-byte aligned buffer sets (TMA destinations)
-  pl.work_off = pl.nsets * pl.xslot;
+  // One float32 input set when the second would cost a CTA per SM (3 fit by
+  // registers): the next unit is then requested as soon as this one is done
+  // with its planes, and the other resident CTAs cover the latency.
+  // 16-bit planes: the second region holds the raw planes for the bulk
+  // copies; it shrinks to just that staging area (one float32 set) on the
+  // same condition.
+  int region1 = pl.xslot;
+  {
+    const long two = 4L * (2 * pl.xslot + (long)P * pl.wf + wfloats) + 16 + WT_SMEM_SLACK;
+    const long per3 = kSmemPerSm / 3 - 1024 - kStaticSmem;
+    const int staging = round_up((P * d->H * d->W + 1) / 2, 32);  // P raw 16-bit planes, in floats
+    const int alt = d->dtype == WTCONV_F32 ? 0 : staging;
+    if (two > per3 && two - 4L * (pl.xslot - alt) <= per3) {
+      pl.nsets = 1;
+      region1 = alt;
+    }
+  }
+  pl.stage_off = pl.xslot;
+  pl.work_off = pl.xslot + region1;
   pl.w_off = pl.work_off + P * pl.wf;
   pl.mb_off = round_up(pl.w_off + wfloats, 2);
   pl.smem_bytes = 4 * pl.mb_off + 16 + WT_SMEM_SLACK;
@@ -444,7 +463,7 @@ wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float
   alignas(64) CUtensorMap tmx;
   memset(&tmx, 0, sizeof(tmx));
   pl.use_tma = encode_plane_map(&tmx, x, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
-  set_bulk(pl, desc, x, pl.nsets == 2 ? 4L * pl.xslot : 0);
+  set_bulk(pl, desc, x, 4L * (pl.work_off - pl.stage_off));
   cudaError_t e = wt::launch_fwd(pl, tmx, desc->dtype, false, x, w_base, b_base, w_sub, base_scale,
                                  wavelet_scale, y, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_fwd: %s", cudaGetErrorString(e));
@@ -471,7 +490,7 @@ wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const
   alignas(64) CUtensorMap tmx;
   memset(&tmx, 0, sizeof(tmx));
   pl.use_tma = encode_plane_map(&tmx, dy, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
-  set_bulk(pl, desc, dy, pl.nsets == 2 ? 4L * pl.xslot : 0);
+  set_bulk(pl, desc, dy, 4L * (pl.work_off - pl.stage_off));
   cudaError_t e = wt::launch_fwd(pl, tmx, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale,
                                  wavelet_scale, dx, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_data: %s", cudaGetErrorString(e));

@@ -228,11 +228,11 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     tma_load_4d(sm + s * pl.xslot, &tmx, -4, -R, cc, nn, &mbar[s]);
   };
   // 16-bit bulk path: the raw planes of a unit land, one bulk copy per plane,
-  // in the second input set (unused by 16-bit units); they are widened into
-  // the first set at the start of the unit, after which the next unit's copy
-  // is issued.  One mbarrier (mbar[0]).
+  // in the staging area after the first input set; they are widened into the
+  // first set at the start of the unit, after which the next unit's copy is
+  // issued.  One mbarrier (mbar[0]).
   const bool bulk = !ASYNC && pl.use_bulk;
-  T* const stage = reinterpret_cast<T*>(sm + pl.xslot);
+  T* const stage = reinterpret_cast<T*>(sm + pl.stage_off);
   const int HWp = pl.H * pl.W;
   auto issue_bulk = [&](int uu) {
     const int cc = uu / pl.groups;
@@ -269,9 +269,10 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     }
     if (tma) {
       if (tid == 0) {
+        if (!dbl && u != u_begin) issue(u, 0);  // single set: the previous unit is done with it
         const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u);
         parity ^= 1u << slot;
-        if (ok && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
+        if (ok && dbl && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
         s_ok = ok;
       }
     } else if (bulk) {
@@ -282,13 +283,13 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     } else if (!ASYNC) {
       load_planes<T>(xs, XF, pl.lev[0], x, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
     } else {
-      if (u == u_begin) {
+      if (u == u_begin || !dbl) {  // first unit, or single set: load now
         load_planes_async(xs, XF, pl.lev[0], reinterpret_cast<const float*>(x), n0, np, c, C, pl.H, pl.W,
                           pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
         cp_async_commit();
         cp_async_wait_all();
       }
-      if (u + 1 < u_end) {  // prefetch the next unit into the other buffer set
+      if (dbl && u + 1 < u_end) {  // prefetch the next unit into the other buffer set
         const int c1 = (u + 1) / pl.groups;
         const int n1 = (u + 1 - c1 * pl.groups) * pl.P;
         load_planes_async(sm + (slot ^ 1) * pl.xslot, XF, pl.lev[0], reinterpret_cast<const float*>(x), n1,
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     // (2) final tiles: base convolution + synthesis + store.
     if (pl.ftp == WT_TP) final_tiles<K, T, WT_TP>(pl, work, xs, wsm, bias, y, n0, c, np, tid);
     else final_tiles<K, T, WT_TP / 2>(pl, work, xs, wsm, bias, y, n0, c, np, tid);
-    if (ASYNC && !tma) cp_async_wait_all();  // this thread's copies of the next unit have landed
+    if (ASYNC && !tma && dbl) cp_async_wait_all();  // this thread's copies of the next unit have landed
     __syncthreads();                 // ... and all reads of unit u are done
   }  // unit loop
 }

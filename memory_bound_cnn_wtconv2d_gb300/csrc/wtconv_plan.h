@@ -52,9 +52,10 @@ struct WtFwdPlan {
   int ftr, ftc;             // final tiles (ftp x WT_TQ level-1 positions) per plane: rows, columns
   int xf;                // floats per input-plane buffer (= TMA box of one plane)
   int xslot;             // floats per input buffer set (P planes, 128-byte multiple)
-  int nsets;             // input sets: 2 (float32: the next unit streams in meanwhile) or 1
+  int nsets;             // input sets: 2 (the next unit streams in meanwhile) or 1
+  int stage_off;         // = xslot: second set, or (16-bit) the staging area of the raw planes
   int wf;                // floats per work area (pyramid + convolved bands; P of them)
-  int work_off;          // = nsets * xslot
+  int work_off;          // after the input sets / staging area
   int w_off;             // folded weights, after the work areas
   int w_band;            // floats per folded kernel (k*k rounded up to 4)
   int mb_off;            // two mbarriers (8-byte aligned), after the weights
