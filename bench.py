@@ -56,9 +56,9 @@ def fma_per_plane(H, W, L, k):
 # kernel, from one ncu capture of the stage-1 layer (profiles/ncu_full_stage1_f32.md),
 # valid only for the kernel sources they were taken on (hash below).
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "8e13c6a1d3194ec875e038bdce258726c891f8dc80ce663fbbba9a3f3ad842d9",
+    "csrc_sha256": "041a3995697b3b77b737e9cb77c1f4bda2260449613a2289763ef92d2914902f",
     "workload": "stage1",
-    "bytes": {"fwd": 108_307_456, "bwd_data": 108_124_416, "bwd_weight": 157_428_736},
+    "bytes": {"fwd": 108_224_768, "bwd_data": 108_350_208, "bwd_weight": 157_412_608},
 }
 
 
