@@ -185,15 +185,13 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
         haar_level(in_x, XBF, work, WF, np, pl.xs[0], pl.xs[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
         haar_level(in_d, DBF, work, WF, np, pl.ds[0], pl.ds[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
       } else {
-        haar_levels12(in_x, XBF, work, WF, np, pl.xs[0], pl.xs[1], pl.xs[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
-                      pl.an_pp[2], pl.an_w[2], tid, NT);
-        haar_levels12(in_d, DBF, work, WF, np, pl.ds[0], pl.ds[1], pl.ds[2], pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2],
-                      pl.an_pp[2], pl.an_w[2], tid, NT);
+        haar_levels12_pair(in_x, XBF, pl.xs[0], pl.xs[1], pl.xs[2], in_d, DBF, pl.ds[0], pl.ds[1], pl.ds[2], work,
+                           WF, np, pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2], pl.an_pp[2], pl.an_w[2], tid, NT);
       }
       __syncthreads();
       for (int l = 3; l <= L; ++l) {
-        haar_level(work, WF, work, WF, np, pl.xs[l - 1], pl.xs[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
-        haar_level(work, WF, work, WF, np, pl.ds[l - 1], pl.ds[l], pl.Hs[l], pl.Ws[l], pl.an_pp[l], pl.an_w[l], tid, NT);
+        haar_level_pair(work, WF, work, WF, np, pl.xs[l - 1], pl.xs[l], pl.ds[l - 1], pl.ds[l], pl.Hs[l], pl.Ws[l],
+                        pl.an_pp[l], pl.an_w[l], tid, NT);
         __syncthreads();
       }
 #pragma unroll

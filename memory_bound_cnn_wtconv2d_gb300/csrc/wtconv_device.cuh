@@ -252,12 +252,7 @@ __device__ __forceinline__ void haar_level(const float* sbase, int sps, float* d
   }
 }
 
-// Haar levels 1 and 2 in one pass: each item reads a 4x4 block of the input
-// plane and writes the 2x2 level-1 positions of all four bands and the one
-// level-2 position built from their low-pass values (same unnormalised
-// butterflies as haar_level).  Items cover the level-2 grid H2 x W2; level-1
-// positions past H1 x W1 are skipped (they lie in the zero margin, and the
-// input rows/columns they read there are zero).
+// Unnormalised 2x2 Haar butterfly of (a b / c d): LL, row-high, column-high, diagonal.
 __device__ __forceinline__ void butterfly4(float a, float b, float c, float d, float (&o)[4]) {
   const float s0 = a + b, d0 = a - b, s1 = c + d, d1 = c - d;
   o[0] = s0 + s1;
@@ -266,6 +261,63 @@ __device__ __forceinline__ void butterfly4(float a, float b, float c, float d, f
   o[3] = d0 - d1;
 }
 
+// Loads the 4x4 input block at level-2 position (P, Q) of source buffer S.
+__device__ __forceinline__ void load_block4(const float* s, const WtBuf S, float (&x)[4][4]) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const float* r = s + a * S.stride;
+    if ((S.pcol & 3) == 0) {
+      const float4 t = *reinterpret_cast<const float4*>(r);
+      x[a][0] = t.x; x[a][1] = t.y; x[a][2] = t.z; x[a][3] = t.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[a][e] = r[e];
+    }
+  }
+}
+
+// Levels 1 and 2 of one 4x4 block (butterflies of haar_levels12) stored at
+// level-2 position (P, Q) of the destination buffers D1, D2 of plane base ps.
+__device__ __forceinline__ void store_block12(const float (&x)[4][4], float* ps, const WtBuf D1, const WtBuf D2,
+                                              int P, int Q, int H1, int W1) {
+  float ll[2][2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    float o[2][4];
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+      butterfly4(x[2 * u][2 * v], x[2 * u][2 * v + 1], x[2 * u + 1][2 * v], x[2 * u + 1][2 * v + 1], o[v]);
+      ll[u][v] = o[v][0];
+    }
+    const int p = 2 * P + u, q = 2 * Q;
+    if (p < H1) {
+      float* d = ps + D1.off + (p + D1.prow) * D1.stride + q + D1.pcol;
+      if (q + 1 < W1 && (D1.pcol & 1) == 0) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) *reinterpret_cast<float2*>(d + b * D1.band) = make_float2(o[0][b], o[1][b]);
+      } else {
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+          if (q + v < W1) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) d[b * D1.band + v] = o[v][b];
+          }
+      }
+    }
+  }
+  float o2[4];
+  butterfly4(ll[0][0], ll[0][1], ll[1][0], ll[1][1], o2);
+  float* d = ps + D2.off + (P + D2.prow) * D2.stride + Q + D2.pcol;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) d[b * D2.band] = o2[b];
+}
+
+// Haar levels 1 and 2 in one pass: each item reads a 4x4 block of the input
+// plane and writes the 2x2 level-1 positions of all four bands and the one
+// level-2 position built from their low-pass values (same unnormalised
+// butterflies as haar_level).  Items cover the level-2 grid H2 x W2; level-1
+// positions past H1 x W1 are skipped (they lie in the zero margin, and the
+// input rows/columns they read there are zero).
 __device__ __forceinline__ void haar_levels12(const float* sbase, int sps, float* dbase, int dps, int np,
                                               const WtBuf S, const WtBuf D1, const WtBuf D2, int H1, int W1,
                                               int H2, int W2, const WtDiv& dpp, const WtDiv& dw, int tid,
@@ -276,50 +328,9 @@ __device__ __forceinline__ void haar_levels12(const float* sbase, int sps, float
     const int rem = it - g * per_plane;
     const int P = fdiv(rem, dw);
     const int Q = rem - P * W2;
-    float* ps = dbase + g * dps;
-    const float* s = sbase + g * sps + S.off + (4 * P + S.prow) * S.stride + 4 * Q + S.pcol;
     float x[4][4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const float* r = s + a * S.stride;
-      if ((S.pcol & 3) == 0) {
-        const float4 t = *reinterpret_cast<const float4*>(r);
-        x[a][0] = t.x; x[a][1] = t.y; x[a][2] = t.z; x[a][3] = t.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[a][e] = r[e];
-      }
-    }
-    float ll[2][2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      float o[2][4];
-#pragma unroll
-      for (int v = 0; v < 2; ++v) {
-        butterfly4(x[2 * u][2 * v], x[2 * u][2 * v + 1], x[2 * u + 1][2 * v], x[2 * u + 1][2 * v + 1], o[v]);
-        ll[u][v] = o[v][0];
-      }
-      const int p = 2 * P + u, q = 2 * Q;
-      if (p < H1) {
-        float* d = ps + D1.off + (p + D1.prow) * D1.stride + q + D1.pcol;
-        if (q + 1 < W1 && (D1.pcol & 1) == 0) {  // both columns valid, 8-byte aligned pair
-#pragma unroll
-          for (int b = 0; b < 4; ++b) *reinterpret_cast<float2*>(d + b * D1.band) = make_float2(o[0][b], o[1][b]);
-        } else {
-#pragma unroll
-          for (int v = 0; v < 2; ++v)
-            if (q + v < W1) {
-#pragma unroll
-              for (int b = 0; b < 4; ++b) d[b * D1.band + v] = o[v][b];
-            }
-        }
-      }
-    }
-    float o2[4];
-    butterfly4(ll[0][0], ll[0][1], ll[1][0], ll[1][1], o2);
-    float* d = ps + D2.off + (P + D2.prow) * D2.stride + Q + D2.pcol;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) d[b * D2.band] = o2[b];
+    load_block4(sbase + g * sps + S.off + (4 * P + S.prow) * S.stride + 4 * Q + S.pcol, S, x);
+    store_block12(x, dbase + g * dps, D1, D2, P, Q, H1, W1);
   }
 }
 
@@ -353,6 +364,57 @@ __device__ __forceinline__ void widen_planes(float* dbase, int dps, const WtBuf 
       const int j = rem - i * W;
       dbase[g * dps + B.off + (i + B.prow) * B.stride + j + B.pcol] = to_f32(src[it]);
     }
+  }
+}
+
+// haar_levels12 for two same-sized pyramids at once (x and dy of the
+// parameter-gradient pass): each item loads the block of both sources before
+// any store, so the two butterfly chains overlap, and shares the indexing.
+__device__ __forceinline__ void haar_levels12_pair(const float* sa, int spa, const WtBuf SA, const WtBuf DA1,
+                                                   const WtBuf DA2, const float* sb, int spb, const WtBuf SB,
+                                                   const WtBuf DB1, const WtBuf DB2, float* dbase, int dps,
+                                                   int np, int H1, int W1, int H2, int W2, const WtDiv& dpp,
+                                                   const WtDiv& dw, int tid, int nthreads) {
+  const int per_plane = H2 * W2;
+  for (int it = tid; it < np * per_plane; it += nthreads) {
+    const int g = fdiv(it, dpp);
+    const int rem = it - g * per_plane;
+    const int P = fdiv(rem, dw);
+    const int Q = rem - P * W2;
+    float xa[4][4], xb[4][4];
+    load_block4(sa + g * spa + SA.off + (4 * P + SA.prow) * SA.stride + 4 * Q + SA.pcol, SA, xa);
+    load_block4(sb + g * spb + SB.off + (4 * P + SB.prow) * SB.stride + 4 * Q + SB.pcol, SB, xb);
+    float* ps = dbase + g * dps;
+    store_block12(xa, ps, DA1, DA2, P, Q, H1, W1);
+    store_block12(xb, ps, DB1, DB2, P, Q, H1, W1);
+  }
+}
+
+// haar_level for two same-sized pyramids at once (both sources read before
+// any store).
+__device__ __forceinline__ void haar_level_pair(const float* sbase, int sps, float* dbase, int dps, int np,
+                                                const WtBuf SA, const WtBuf DA, const WtBuf SB, const WtBuf DB,
+                                                int Hl, int Wl, const WtDiv& dpp, const WtDiv& dw, int tid,
+                                                int nthreads) {
+  const int per_plane = Hl * Wl;
+  for (int it = tid; it < np * per_plane; it += nthreads) {
+    const int g = fdiv(it, dpp);
+    const int rem = it - g * per_plane;
+    const int p = fdiv(rem, dw);
+    const int q = rem - p * Wl;
+    const float* s1 = sbase + g * sps + SA.off + (2 * p + SA.prow) * SA.stride + 2 * q + SA.pcol;
+    const float* s2 = sbase + g * sps + SB.off + (2 * p + SB.prow) * SB.stride + 2 * q + SB.pcol;
+    const float a1 = s1[0], b1 = s1[1], c1 = s1[SA.stride], d1 = s1[SA.stride + 1];
+    const float a2 = s2[0], b2 = s2[1], c2 = s2[SB.stride], d2 = s2[SB.stride + 1];
+    float o1[4], o2[4];
+    butterfly4(a1, b1, c1, d1, o1);
+    butterfly4(a2, b2, c2, d2, o2);
+    float* t1 = dbase + g * dps + DA.off + (p + DA.prow) * DA.stride + q + DA.pcol;
+    float* t2 = dbase + g * dps + DB.off + (p + DB.prow) * DB.stride + q + DB.pcol;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) t1[b * DA.band] = o1[b];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) t2[b * DB.band] = o2[b];
   }
 }
 
