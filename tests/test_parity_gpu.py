@@ -182,10 +182,12 @@ def test_full_size_workloads(wt, name):
 
 @pytest.mark.parametrize("C,H", synth.SWEEP_SHAPES)
 @pytest.mark.parametrize("L", synth.SWEEP_LEVELS)
-def test_level_sweep_shapes(wt, C, H, L):
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_level_sweep_shapes(wt, C, H, L, dtype):
     # the sweep's (C, H=W, L) shapes at a reduced batch (every plane is
-    # independent, so the batch size does not change the per-plane path)
-    check_all(wt, synth.make_inputs(3, C // 8, H, H, L, 5, seed=C + H + L))
+    # independent, so the batch size does not change the per-plane path);
+    # covers both input-set layouts, 16-bit staging and both final-tile heights
+    check_all(wt, synth.make_inputs(3, C // 8, H, H, L, 5, dtype=dtype, seed=C + H + L))
 
 
 # The largest planes each pass of this build handles (shared memory per CTA for
