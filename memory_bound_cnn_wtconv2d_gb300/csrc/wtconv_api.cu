@@ -273,10 +273,9 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
   if (d->N > 0 && P > d->N) P = d->N;
   if (P < 1) P = 1;
   pl.P = P;
-  // 16-bit planes that are whole 16-byte chunks get a staging area for bulk
-  // copies (used when the tensors are 16-byte aligned).
-  const bool staging = d->dtype != WTCONV_F32 && (2L * d->H * d->W) % 16 == 0 &&
-                       2L * d->H * d->W * P * 2 < (1L << 20);
+  // 16-bit planes that are whole 8-byte chunks get a staging area for their
+  // raw planes (used when the tensors are aligned enough; see set_bulk).
+  const bool staging = d->dtype != WTCONV_F32 && (2L * d->H * d->W) % 8 == 0;
   bw_layout(pl, 2, false);
   if (pl.smem_bytes > kMaxSmemPerBlock) {
     bw_layout(pl, 1, false);
@@ -401,14 +400,20 @@ void set_load_divs(Plan& pl, const wtconv_desc_t* d, int vec) {
   pl.ld_w = make_div(per_row);
 }
 
-// 16-bit planes stream in by one bulk copy each when a plane is a whole
-// number of 16-byte chunks and the tensor is 16-byte aligned.
+// 16-bit planes are staged raw and widened in shared memory: by one bulk copy
+// per plane when a plane is a whole number of 16-byte chunks and the tensor is
+// 16-byte aligned (mode 1), else by 8-byte cp.async chunks when a plane is a
+// whole number of 8-byte chunks and the tensor is 8-byte aligned (mode 2).
 template <typename Plan>
 void set_bulk(Plan& pl, const wtconv_desc_t* d, const void* src, long capacity_bytes) {
   const long plane = 2L * d->H * d->W;
-  pl.use_bulk = d->dtype != WTCONV_F32 && plane % 16 == 0 && aligned(src, 16) &&
-                plane * pl.P <= capacity_bytes && plane * pl.P < (1L << 20);
+  pl.use_bulk = 0;
+  if (d->dtype != WTCONV_F32 && plane * pl.P <= capacity_bytes) {
+    if (plane % 16 == 0 && aligned(src, 16) && plane * pl.P < (1L << 20)) pl.use_bulk = 1;
+    else if (plane % 8 == 0 && aligned(src, 8)) pl.use_bulk = 2;
+  }
   pl.bulk_bytes = (uint32_t)plane;
+  pl.cp_pp = make_div((int)(plane / 8 > 0 ? plane / 8 : 1));
   pl.wd_vec = d->W % 4 == 0;
   const int per_row = pl.wd_vec ? d->W / 4 : d->W;
   pl.wd_pp = make_div(d->H * per_row);
@@ -533,7 +538,9 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
     return fail(WTCONV_ERR_WORKSPACE, "workspace of %zu B given, %zu B needed", ws ? ws_bytes : 0, need);
   if (!aligned(ws, 256)) return fail(WTCONV_ERR_MISALIGNED, "workspace is not 256-byte aligned");
   set_load_divs(pl, desc, vec_ok(desc, x, dy));
-  set_bulk(pl, desc, x, pl.stage_off > 0 && aligned(dy, 16) ? 4L * (pl.work_off - pl.stage_off) / 2 : 0);
+  set_bulk(pl, desc, x, pl.stage_off > 0 ? 4L * (pl.work_off - pl.stage_off) / 2 : 0);
+  if (pl.use_bulk == 1 && !(aligned(dy, 16) && 2L * pl.P * pl.bulk_bytes < (1L << 20))) pl.use_bulk = 2;
+  if (pl.use_bulk == 2 && !aligned(dy, 8)) pl.use_bulk = 0;
   alignas(64) CUtensorMap tmx, tmd;
   memset(&tmx, 0, sizeof(tmx));
   memset(&tmd, 0, sizeof(tmd));

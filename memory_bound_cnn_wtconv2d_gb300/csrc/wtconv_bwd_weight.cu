@@ -76,10 +76,13 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
     tma_load_4d(dst, &tmx, -4, -R, cc, n0, &mbar[s]);
     tma_load_4d(dst + pl.xr, &tmd, 0, 0, cc, n0, &mbar[s]);
   };
-  // 16-bit bulk path: a unit's raw x and dy planes land in the staging area
-  // (one bulk copy per plane) on mbar[0]; the unit widens them into its input
-  // set, after which the next unit's copies are issued.
-  const bool bulk = !ASYNC && pl.use_bulk;
+  // 16-bit staged path: a unit's raw x and dy planes land in the staging area
+  // (one bulk copy per plane on mbar[0], or 8-byte cp.async chunks from every
+  // thread); the unit widens them into its input set, after which the next
+  // unit's copies are issued.
+  const bool bulk = !ASYNC && pl.use_bulk == 1;
+  const bool cpa = !ASYNC && pl.use_bulk == 2;  // same staging, filled by every thread's 8-byte cp.async
+  const bool staged = bulk || cpa;
   const int HWp = pl.H * pl.W;
   T* const stage_x = reinterpret_cast<T*>(sm + pl.stage_off);
   T* const stage_d = stage_x + P * HWp;
@@ -94,6 +97,20 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
       bulk_load(stage_x + g * HWp, x + src, pl.bulk_bytes, &mbar[0]);
       bulk_load(stage_d + g * HWp, dy + src, pl.bulk_bytes, &mbar[0]);
     }
+  };
+  auto issue_cpa = [&](int u) {
+    const int cc = unit_c(u);
+    const int n0 = (u - cc * NB) * P;
+    const int chunks = HWp >> 2;  // 8-byte chunks (4 elements) per plane
+    const int total = min(P, pl.N - n0) * chunks;
+    for (int i = tid; i < total; i += NT) {
+      const int g = fdiv(i, pl.cp_pp);
+      const int o = (i - g * chunks) << 2;
+      const size_t src = ((size_t)(n0 + g) * C + cc) * HWp + o;
+      cp_async8(reinterpret_cast<float*>(stage_x + g * HWp + o), reinterpret_cast<const float*>(x + src));
+      cp_async8(reinterpret_cast<float*>(stage_d + g * HWp + o), reinterpret_cast<const float*>(dy + src));
+    }
+    cp_async_commit();
   };
   auto load_async = [&](int u, int s) {
     const int cc = unit_c(u);
@@ -131,6 +148,8 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
     if (tid == 0 && u_begin < u_end) issue(u_begin, 0);
   } else if (bulk) {
     if (tid == 0 && u_begin < u_end) issue_bulk(u_begin);
+  } else if (cpa) {
+    if (u_begin < u_end) issue_cpa(u_begin);
   } else if (ASYNC && dbl && u_begin < u_end) {  // first unit
     load_async(u_begin, 0);
     cp_async_wait_all();
@@ -157,6 +176,8 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
           s_ok = mbar_wait_bounded(&mbar[0], parity & 1u);
           parity ^= 1u;
         }
+      } else if (cpa) {
+        cp_async_wait_all();  // this thread's copies of unit u; the barrier below publishes all
       } else if (!ASYNC || !dbl) {
         load_planes<T>(in_x, XBF, pl.xs[0], x, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
         load_planes<T>(in_d, DBF, pl.ds[0], dy, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
@@ -173,11 +194,12 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
         __syncthreads();
         return;  // records are not written: the caller sees the fault count
       }
-      if (bulk) {  // widen the raw planes, then start the next unit's copies
+      if (staged) {  // widen the raw planes, then start the next unit's copies
         widen_planes<T>(in_x, XBF, pl.xs[0], stage_x, np, pl.H, pl.W, pl.wd_vec != 0, pl.wd_pp, pl.wd_w, tid, NT);
         widen_planes<T>(in_d, DBF, pl.ds[0], stage_d, np, pl.H, pl.W, pl.wd_vec != 0, pl.wd_pp, pl.wd_w, tid, NT);
         __syncthreads();
-        if (tid == 0 && u + 1 < u_end) issue_bulk(u + 1);
+        if (bulk && tid == 0 && u + 1 < u_end) issue_bulk(u + 1);
+        if (cpa && u + 1 < u_end) issue_cpa(u + 1);
       }
 
       // Both pyramids: levels 1+2 fused, then 3..L.

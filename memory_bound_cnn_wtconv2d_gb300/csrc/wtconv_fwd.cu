@@ -227,11 +227,13 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes);
     tma_load_4d(sm + s * pl.xslot, &tmx, -4, -R, cc, nn, &mbar[s]);
   };
-  // 16-bit bulk path: the raw planes of a unit land, one bulk copy per plane,
-  // in the staging area after the first input set; they are widened into the
-  // first set at the start of the unit, after which the next unit's copy is
-  // issued.  One mbarrier (mbar[0]).
-  const bool bulk = !ASYNC && pl.use_bulk;
+  // 16-bit staged path: the raw planes of a unit land in the staging area
+  // after the first input set (one bulk copy per plane on mbar[0], or 8-byte
+  // cp.async chunks from every thread); they are widened into the first set at
+  // the start of the unit, after which the next unit's copies are issued.
+  const bool bulk = !ASYNC && pl.use_bulk == 1;
+  const bool cpa = !ASYNC && pl.use_bulk == 2;  // same staging, filled by every thread's 8-byte cp.async
+  const bool staged = bulk || cpa;
   T* const stage = reinterpret_cast<T*>(sm + pl.stage_off);
   const int HWp = pl.H * pl.W;
   auto issue_bulk = [&](int uu) {
@@ -242,6 +244,19 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     mbar_arrive_expect_tx(&mbar[0], (uint32_t)npp * pl.bulk_bytes);
     for (int g = 0; g < npp; ++g)
       bulk_load(stage + g * HWp, x + ((size_t)(nn + g) * C + cc) * HWp, pl.bulk_bytes, &mbar[0]);
+  };
+  auto issue_cpa = [&](int uu) {
+    const int cc = uu / pl.groups;
+    const int nn = (uu - cc * pl.groups) * pl.P;
+    const int chunks = HWp >> 2;  // 8-byte chunks (4 elements) per plane
+    const int total = min(pl.P, pl.N - nn) * chunks;
+    for (int i = tid; i < total; i += NT) {
+      const int g = fdiv(i, pl.cp_pp);
+      const int o = (i - g * chunks) << 2;
+      cp_async8(reinterpret_cast<float*>(stage + g * HWp + o),
+                reinterpret_cast<const float*>(x + ((size_t)(nn + g) * C + cc) * HWp + o));
+    }
+    cp_async_commit();
   };
 
   // Zero margins once (the box copies write whole padded planes themselves).
@@ -255,10 +270,11 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
   __syncthreads();  // the zero fill and barrier init land before any plane copy
   if (tma && tid == 0 && u_begin < u_end) issue(u_begin, 0);
   if (bulk && tid == 0 && u_begin < u_end) issue_bulk(u_begin);
+  if (cpa && u_begin < u_end) issue_cpa(u_begin);
   int c_prev = -1;
   int slot = 0;
   const bool dbl = pl.nsets == 2;
-  for (int u = u_begin; u < u_end; ++u, slot = (dbl && !bulk) ? slot ^ 1 : 0) {
+  for (int u = u_begin; u < u_end; ++u, slot = (dbl && !staged) ? slot ^ 1 : 0) {
     const int c = u / pl.groups;
     const int n0 = (u - c * pl.groups) * pl.P;
     const int np = min(pl.P, pl.N - n0);
@@ -280,6 +296,8 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
         s_ok = mbar_wait_bounded(&mbar[0], parity & 1u);
         parity ^= 1u;
       }
+    } else if (cpa) {
+      cp_async_wait_all();  // this thread's copies of unit u; the barrier below publishes all
     } else if (!ASYNC) {
       load_planes<T>(xs, XF, pl.lev[0], x, n0, np, c, C, pl.H, pl.W, pl.vec_ok != 0, pl.ld_pp, pl.ld_w, tid, NT);
     } else {
@@ -308,10 +326,11 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
       __syncthreads();
       break;
     }
-    if (bulk) {  // widen the raw planes, then start the next unit's copy
+    if (staged) {  // widen the raw planes, then start the next unit's copy
       widen_planes<T>(xs, XF, pl.lev[0], stage, np, pl.H, pl.W, pl.wd_vec != 0, pl.wd_pp, pl.wd_w, tid, NT);
       __syncthreads();
-      if (tid == 0 && u + 1 < u_end) issue_bulk(u + 1);
+      if (bulk && tid == 0 && u + 1 < u_end) issue_bulk(u + 1);
+      if (cpa && u + 1 < u_end) issue_cpa(u + 1);
     }
 
     // (1) Haar pyramid on chip.

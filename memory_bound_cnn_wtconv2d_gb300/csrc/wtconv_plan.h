@@ -63,8 +63,9 @@ struct WtFwdPlan {
   int vec_ok;            // rows can use 16-byte global accesses (W % elems-per-16B == 0)
   int use_tma;           // input planes arrive by TMA box copies (float32, 16-byte rows)
   uint32_t tma_bytes;    // bytes of one box (P planes)
-  int use_bulk;          // 16-bit planes arrive by bulk copies into the second input set, then widen
-  uint32_t bulk_bytes;   // bytes of one raw 16-bit plane (H*W*2, a multiple of 16)
+  int use_bulk;          // 16-bit planes are staged raw, then widened: 1 = bulk copies, 2 = 8-byte cp.async
+  uint32_t bulk_bytes;   // bytes of one raw 16-bit plane (H*W*2: a multiple of 16, or of 8 for cp.async)
+  WtDiv cp_pp;           // 8-byte chunks per raw plane (H*W/4), for the cp.async staging
   int wd_vec;            // widening works on 4-element items (W % 4 == 0)
   WtDiv wd_pp, wd_w;     // widening: items per plane, items per row
   WtDiv ld_pp, ld_w;     // plane load: items per plane, items per row
@@ -111,8 +112,9 @@ struct WtBwPlan {
   int use_tma;           // input planes arrive by TMA box copies (float32, 16-byte rows)
   uint32_t tma_bytes;    // bytes of one input set (x and dy boxes)
   int stage_off;         // 16-bit staging area (raw x planes, then raw dy planes), floats; 0 = none
-  int use_bulk;          // 16-bit planes arrive by bulk copies into the staging area, then widen
-  uint32_t bulk_bytes;   // bytes of one raw 16-bit plane (H*W*2, a multiple of 16)
+  int use_bulk;          // 16-bit planes are staged raw, then widened: 1 = bulk copies, 2 = 8-byte cp.async
+  uint32_t bulk_bytes;   // bytes of one raw 16-bit plane (H*W*2: a multiple of 16, or of 8 for cp.async)
+  WtDiv cp_pp;           // 8-byte chunks per raw plane (H*W/4), for the cp.async staging
   int wd_vec;            // widening works on 4-element items (W % 4 == 0)
   WtDiv wd_pp, wd_w;     // widening: items per plane, items per row
   int nbands;            // 1 + 4L
