@@ -56,9 +56,9 @@ def fma_per_plane(H, W, L, k):
 # kernel, from one ncu capture of the stage-1 layer (profiles/ncu_full_stage1_f32.md),
 # valid only for the kernel sources they were taken on (hash below).
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "041a3995697b3b77b737e9cb77c1f4bda2260449613a2289763ef92d2914902f",
+    "csrc_sha256": "acdd78634dc07eba67e19c71a1e14ee57c101218a9d24d17fec7aa9d29c50341",
     "workload": "stage1",
-    "bytes": {"fwd": 108_224_768, "bwd_data": 108_350_208, "bwd_weight": 157_412_608},
+    "bytes": {"fwd": 108_781_824, "bwd_data": 108_309_760, "bwd_weight": 157_504_256},
 }
 
 
