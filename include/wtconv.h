@@ -44,10 +44,13 @@
  *     CUDA launch error it returns WTCONV_ERR_CUDA.  wtconv_last_error()
  *     returns a thread-local message describing the last failure.
  *   - Limits: 3 <= k <= 9, k odd; 1 <= levels <= 8; N >= 0; C, H, W >= 1;
- *     every plane (with its on-chip pyramid) must fit in one SM's shared
- *     memory (about H, W <= 128 for the forward calls and H, W <= 88 for the
- *     parameter-gradient call; larger planes return WTCONV_ERR_UNSUPPORTED).
- *     N = 0 is a valid empty batch.
+ *     every plane (with its on-chip pyramid) must fit one CTA's shared
+ *     memory: square planes up to 92..112 px for wtconv_fwd and
+ *     wtconv_bwd_data (depending on k and levels), up to 56 px (64 px at
+ *     levels = 1) for wtconv_bwd_weight, whose per-thread gradient tiles
+ *     must also fit in registers; larger planes return
+ *     WTCONV_ERR_UNSUPPORTED before anything is launched.  N = 0 is a valid
+ *     empty batch.
  *   - Pointers must be aligned to their element size (WTCONV_ERR_MISALIGNED
  *     otherwise); 16-byte alignment enables vector loads and stores.
  */
@@ -85,9 +88,11 @@ typedef struct {
   int dtype;       /* wtconv_dtype_t of x / y / dy / dx                     */
 } wtconv_desc_t;
 
-/* Bytes of device workspace `op` needs for `desc` (0 if none, or if desc is
- * invalid).  The workspace must be 256-byte aligned; its contents need not
- * be initialised and are garbage after the call. */
+/* Bytes of device workspace `op` needs for `desc` on the current device (0 if
+ * none, or if desc is invalid; the parameter-gradient grid, and with it the
+ * size, follows the device's occupancy).  The workspace must be 256-byte
+ * aligned; its contents need not be initialised and are garbage after the
+ * call. */
 size_t wtconv_workspace_size(const wtconv_desc_t* desc, int op);
 
 /* Forward: y = WTConv2d(x).  b_base may be NULL (no bias).
@@ -154,7 +159,7 @@ const char* wtconv_last_error(void);
 
 /* Number of in-kernel waits on the current device that gave up since the
  * previous call, then resets the count.  The kernels wait for their own
- * asynchronous (TMA) plane copies with a time limit of about a second; a
+ * asynchronous (TMA and bulk) plane copies with a time limit of about a second; a
  * wait that runs out records itself here and the kernel stops early (its
  * outputs are then invalid).  0 in normal operation.  Synchronises the
  * current device. */

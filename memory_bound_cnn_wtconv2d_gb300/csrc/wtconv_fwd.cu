@@ -1,10 +1,10 @@
 // Fused WTConv2d forward pass and input-gradient pass (sm_103a).
 //
-// One CTA owns P planes of one channel.  The planes cross HBM once: they are
-// read into shared memory, the Haar pyramid is rebuilt there, every band of
-// every level is convolved with scale-folded weights, and the final tiles
-// add the base convolution and the synthesis of all levels in registers and
-// write the output directly.
+// A persistent grid walks units of P planes of one channel.  The planes
+// cross HBM once: they are read into shared memory, the Haar pyramid is
+// rebuilt there, every band of every level is convolved with scale-folded
+// weights, and the final tiles add the base convolution and the synthesis of
+// all levels in registers and write the output directly.
 //
 // Paper: "Fast and Memory-Efficient Wavelet Convolutions via I/O-Aware
 // Reformulation" (arXiv 2608.10805), technical summary, "Methodology":
@@ -18,9 +18,11 @@
 // The 2^-l normalisations of analysis and synthesis (4^-l in total) are also
 // folded into the level-l weights, so every butterfly is a pure add.
 //
-// Phases per group of planes (one CTA barrier after each):
-//   load -> Haar levels 1+2 (fused) -> Haar levels 3..L -> band convolutions
-//   of all levels (Z buffers) -> final tiles (base conv + (2), stored to HBM).
+// Phases per unit (one CTA barrier after each):
+//   load (TMA / bulk / cp.async, the next unit prefetched where the layout
+//   allows) -> Haar levels 1+2 (fused) -> Haar levels 3..L -> band
+//   convolutions of all levels (Z buffers) -> final tiles (base conv + (2),
+//   stored to HBM).
 //
 // The input-gradient pass is the same kernel with every kernel rotated by
 // 180 degrees and no bias: the layer map is A = s_b*Conv_b + sum_l F_l^T K_l F_l

@@ -32,14 +32,15 @@ struct WtBuf {
   int band;    // floats between consecutive bands
 };
 
-// Forward / input-gradient pass.  One CTA owns P planes of one channel c
-// (n = gi*P .. gi*P+P-1) and runs: load -> Haar analysis (levels 1 and 2
-// fused, then 3..L) -> band convolutions of every level into Z buffers ->
-// final tiles (base conv + bit-indexed synthesis) -> store.
+// Forward / input-gradient pass.  A persistent grid walks the C * groups
+// units (channel c, planes n = gi*P .. gi*P+P-1) in order; per unit a CTA
+// runs: load -> Haar analysis (levels 1 and 2 fused, then 3..L) -> band
+// convolutions of every level into Z buffers -> final tiles (base conv +
+// bit-indexed synthesis) -> store.
 struct WtFwdPlan {
   int N, C, H, W, L, K;
   int P;                 // planes per CTA
-  int groups;            // ceil(N / P); grid = C * groups
+  int groups;            // units per channel: ceil(N / P)
   int Hs[WT_MAXL + 1];   // level sizes, Hs[0] = H, Hs[l] = ceil(Hs[l-1] / 2)
   int Ws[WT_MAXL + 1];
   WtBuf lev[WT_MAXL + 1];  // lev[0] = input plane (pcol 4), lev[l] = 4 coefficient bands (pad r)
