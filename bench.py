@@ -56,7 +56,7 @@ def fma_per_plane(H, W, L, k):
 # kernel, from one ncu capture of the stage-1 layer (profiles/ncu_full_stage1_f32.md),
 # valid only for the kernel sources they were taken on (hash below).
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "acdd78634dc07eba67e19c71a1e14ee57c101218a9d24d17fec7aa9d29c50341",
+    "csrc_sha256": "a49be7bc59651c8ec5987c546e8708add4197045fa23eed4e7dc1855b4f65073",
     "workload": "stage1",
     "bytes": {"fwd": 108_781_824, "bwd_data": 108_309_760, "bwd_weight": 157_504_256},
 }
