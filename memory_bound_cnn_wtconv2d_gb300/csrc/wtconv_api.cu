@@ -135,16 +135,40 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   if (plane_bytes + 4L * wfloats > kMaxSmemPerBlock)
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %ld B of shared memory (max %d)",
                 d->H, d->W, L, plane_bytes + 4L * wfloats, kMaxSmemPerBlock);
-  const int items = pl.ftr * pl.ftc;
-  int P = ceil_div(WT_FWD_THREADS, items);
-  P = P < 1 ? 1 : P;
-  const int fit = (int)((kFwdBudget - 4L * wfloats) / plane_bytes);
-  if (P > fit) P = fit < 1 ? 1 : fit;
-  if (d->N > 0 && P > d->N) P = d->N;
-  // Final tiles of half the height when the full ones would leave more than
-  // half of the CTA's threads without a tile (small planes): twice the items,
-  // each half as long.  Never larger in shared memory.
-  if ((long)P * items * 2 <= WT_FWD_THREADS) fwd_geometry(d, pl, WT_TP / 2);
+  // Planes per unit P and final-tile height: the pair with the least modelled
+  // time per plane.  Each phase of a unit costs (rounds of its items over the
+  // CTA's threads) x (the latency of one item, in issue slots measured on the
+  // stage shapes), plus a fixed cost per unit (barriers, copy wait); P is
+  // bounded by the shared-memory budget (3 CTAs per SM).  Half-height final
+  // tiles never need more shared memory.
+  int fit = (int)((kFwdBudget - 4L * wfloats) / plane_bytes);
+  if (fit < 1) fit = 1;
+  if (d->N > 0 && fit > d->N) fit = d->N;
+  int P = 1, tp = WT_TP;
+  {
+    const int T = WT_FWD_THREADS;
+    const long n12 = L >= 2 ? (long)pl.Hs[2] * pl.Ws[2] : (long)pl.Hs[1] * pl.Ws[1];
+    // per unit: 400, plus 200 for every level past the second (its own
+    // analysis pass behind a CTA barrier)
+    const long c12 = 100, c3 = 30, cz = 16L * KK + 130, cunit = 400 + 200L * (L > 2 ? L - 2 : 0);
+    double best = -1.0;
+    for (int q = 1; q <= fit && q <= 64; ++q) {
+      for (int t = WT_TP; t >= WT_TP / 2; t /= 2) {
+        const long nf = (long)ceil_div(pl.Hs[1], t) * ceil_div(pl.Ws[1], WT_TQ);
+        const long cf = 8L * t * KK + (t == WT_TP ? 400 : 300);  // 2t x 2TQ outputs, k*k FMAs each
+        long cost = ceil_div((int)(q * n12), T) * c12 + ceil_div((int)(q * pl.zipp), T) * cz +
+                    ceil_div((int)(q * nf), T) * cf + cunit;
+        for (int l = 3; l <= L; ++l) cost += ceil_div(q * pl.Hs[l] * pl.Ws[l], T) * c3;
+        const double per_plane = (double)cost / q;
+        if (best < 0 || per_plane < best * (1 - 1e-9)) {
+          best = per_plane;
+          P = q;
+          tp = t;
+        }
+      }
+    }
+  }
+  if (tp != WT_TP) fwd_geometry(d, pl, tp);
   pl.P = P;
   pl.groups = d->N > 0 ? ceil_div(d->N, P) : 0;
   pl.xslot = round_up(P * pl.xf, 32);  // 128-byte aligned buffer sets (TMA destinations)
