@@ -192,6 +192,35 @@ def time_oracle(inp, n_images):
     return time.perf_counter() - t0
 
 
+def time_oracle_parallel(inp, workers):
+    """fwd+bwd of the float64 oracle over the whole batch, the images split into
+    `workers` slices run by that many threads (the oracle's C calls release the
+    interpreter lock); seconds.  The same work as time_oracle over all images."""
+    import concurrent.futures
+    import oracle
+    oracle.fwd(synth.LayerInputs(N=1, C=inp.C, H=inp.H, W=inp.W, levels=inp.levels, k=inp.k, dtype=inp.dtype,
+                                 x=inp.x[:1], dy=inp.dy[:1], w_base=inp.w_base, b_base=inp.b_base,
+                                 w_sub=inp.w_sub, base_scale=inp.base_scale,
+                                 wavelet_scale=inp.wavelet_scale))  # load the library first
+    bounds = [inp.N * i // workers for i in range(workers + 1)]
+
+    def run(i):
+        a, b = bounds[i], bounds[i + 1]
+        if b <= a:
+            return
+        part = synth.LayerInputs(N=b - a, C=inp.C, H=inp.H, W=inp.W, levels=inp.levels, k=inp.k,
+                                 dtype=inp.dtype, x=inp.x[a:b], dy=inp.dy[a:b], w_base=inp.w_base,
+                                 b_base=inp.b_base, w_sub=inp.w_sub, base_scale=inp.base_scale,
+                                 wavelet_scale=inp.wavelet_scale)
+        oracle.fwd(part)
+        oracle.bwd(part)
+
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(run, range(workers)))
+    return time.perf_counter() - t0
+
+
 def unfused_torch_layer(x, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k):
     """WTConv2d with one PyTorch library op per stage, the way the pages describe
     the reference implementation (technical summary, "Problem statement"): a
@@ -368,9 +397,11 @@ def time_events(fn, flush, reps):
 
 def run_suite(args):
     """The shape/level sweep (WTConvNeXt-T stage shapes x levels 1-5, N=128, fp32
-    and fp16, a cuDNN depthwise 7x7 timed on the same x) or the 18 WTConv layers
+    and fp16, a cuDNN depthwise 7x7 timed on the same x), the 18 WTConv layers
     of WTConvNeXt-T at batch 128 in fp16 (summed fwd+bwd time and peak device
-    memory, fused vs the unfused PyTorch composition).  One JSON line."""
+    memory, fused vs the unfused PyTorch composition), or every workload (tiny,
+    stage 1, stage 2 in fp16 and bf16, one layer of each network stage) with
+    the float64 oracle timed on one and on all host cores.  One JSON line."""
     import torch
     import torch.nn.functional as F
 
@@ -424,6 +455,27 @@ def run_suite(args):
                                  "hbm_tbs": round(6 * ne * x.element_size() / (t * 1e-3) / 1e12, 3)})
                 del x, dy
         line = {"suite": "sweep", "metric": "fwd+bwd ms per layer", "n": N, "rows": rows}
+    elif args.suite == "configs":
+        cases = [("tiny", synth.workload("tiny")), ("stage1", synth.workload("stage1")),
+                 ("stage2_f16", synth.workload("stage2_f16")), ("stage2_bf16", synth.workload("stage2_bf16"))]
+        cases += [(f"network C{C} H{H} L{L}", synth.make_inputs(128, C, H, H, L, 5, dtype="f16", seed=4000 + C))
+                  for C, H, _, L in synth.NETWORK_STAGES]
+        workers = os.cpu_count() or 1
+        for name, inp in cases:
+            x = torch.tensor(inp.x, dtype=tdt[inp.dtype], device=dev)
+            dy = torch.tensor(inp.dy, dtype=tdt[inp.dtype], device=dev)
+            ps = [torch.tensor(a, dtype=torch.float32, device=dev) for a in
+                  (inp.w_base, inp.b_base, inp.w_sub, inp.base_scale, inp.wavelet_scale)]
+            t = time_events(fused_step(x, dy, ps, inp.levels, inp.k, buffers(x, ps, inp.levels, inp.k)), flush, reps)
+            t1 = time_oracle(inp, inp.N)
+            tn = time_oracle_parallel(inp, max(1, min(workers, inp.N)))
+            rows.append({"config": name, "shape": [inp.N, inp.C, inp.H, inp.W], "levels": inp.levels,
+                         "dtype": inp.dtype, "fused_fwd_bwd_ms": round(t, 4),
+                         "hbm_tbs": round(6 * x.numel() * x.element_size() / (t * 1e-3) / 1e12, 3),
+                         "oracle_1core_s": round(t1, 3), "oracle_all_cores_s": round(tn, 3),
+                         "oracle_cores": max(1, min(workers, inp.N))})
+            del x, dy
+        line = {"suite": "configs", "metric": "fwd+bwd ms per layer; oracle seconds per layer", "rows": rows}
     else:
         N, dtype = 128, "f16"
         tot_fused = tot_unf = 0.0
@@ -670,6 +722,12 @@ def run_ours(args, world, rank, local):
                                 "kind": "oracle",
                                 "sample": f"one fwd+bwd of the float64 oracle over {n_img} of {inp.N} images "
                                           f"(single thread)"}
+        workers = max(1, min(os.cpu_count() or 1, inp.N))
+        tp = time_oracle_parallel(inp, workers)
+        line["cpu_baseline_all_cores"] = {"value": round(1e3 * tp, 1), "unit": "ms/layer", "cores": workers,
+                                          "kind": "oracle",
+                                          "sample": f"the same fwd+bwd over all {inp.N} images, split over "
+                                                    f"{workers} threads"}
     if world == 1 and not args.no_compare:
         comps = []
         for name, dtype in ((WORKLOAD, None), (WORKLOAD, "f16")):
@@ -693,8 +751,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the unfused-PyTorch and depthwise-7x7 comparison arms")
-    ap.add_argument("--suite", choices=["sweep", "network"], default=None,
-                    help="time the shape/level sweep or the 18-layer network instead of the bench step")
+    ap.add_argument("--suite", choices=["sweep", "network", "configs"], default=None,
+                    help="time the shape/level sweep, the 18-layer network, or every workload with the "
+                         "oracle beside it, instead of the bench step")
     ap.add_argument("--arm-only", default=None,
                     choices=["fused", "unfused", "dw7x7", "fused_infer", "unfused_infer", "dw7x7_infer"],
                     help="run only this arm's training step or forward (steps + warmup times, no JSON); "
