@@ -399,9 +399,11 @@ def run_suite(args):
     """The shape/level sweep (WTConvNeXt-T stage shapes x levels 1-5, N=128, fp32
     and fp16, a cuDNN depthwise 7x7 timed on the same x), the 18 WTConv layers
     of WTConvNeXt-T at batch 128 in fp16 (summed fwd+bwd time and peak device
-    memory, fused vs the unfused PyTorch composition), or every workload (tiny,
+    memory, fused vs the unfused PyTorch composition), every workload (tiny,
     stage 1, stage 2 in fp16 and bf16, one layer of each network stage) with
-    the float64 oracle timed on one and on all host cores.  One JSON line."""
+    the float64 oracle timed on one and on all host cores, or the planes
+    larger than one CTA (forward and input gradient, tiled with a halo).
+    One JSON line."""
     import torch
     import torch.nn.functional as F
 
@@ -476,6 +478,44 @@ def run_suite(args):
                          "oracle_cores": max(1, min(workers, inp.N))})
             del x, dy
         line = {"suite": "configs", "metric": "fwd+bwd ms per layer; oracle seconds per layer", "rows": rows}
+    elif args.suite == "large":
+        # Planes beyond one CTA: the windowed forward and input gradient
+        # against the unfused PyTorch composition (forward, and forward +
+        # autograd input gradient) and a cuDNN depthwise 7x7 on the same x.
+        for N, C, H, W, L, k, dtype in synth.LARGE_PLANES:
+            pin = synth.make_inputs(1, C, 1, 1, L, k, dtype=dtype, seed=5000 + C + L)
+            ps = [torch.tensor(a, dtype=torch.float32, device=dev) for a in
+                  (pin.w_base, pin.b_base, pin.w_sub, pin.base_scale, pin.wavelet_scale)]
+            pdt = [p.to(tdt[dtype]) for p in ps]
+            g = torch.Generator(device=dev).manual_seed(5000 + H + L)
+            x = torch.randn(N, C, H, W, generator=g, device=dev).to(tdt[dtype])
+            dy = torch.randn(N, C, H, W, generator=g, device=dev).to(tdt[dtype])
+            y, dx = torch.empty_like(x), torch.empty_like(x)
+            w7 = torch.zeros(C, 1, 7, 7, dtype=tdt[dtype], device=dev)
+            tf = time_events(lambda: wtconv.wtconv_fwd(x, *ps, L, k, y=y), flush, reps)
+            tb = time_events(lambda: wtconv.wtconv_bwd_data(dy, ps[0], ps[2], ps[3], ps[4], L, k, dx=dx), flush, reps)
+            with torch.no_grad():
+                tu = time_events(lambda: unfused_torch_layer(x, *pdt, L, k), flush, reps)
+                t7 = time_events(lambda: F.conv2d(x, w7, padding=3, groups=C), flush, reps)
+
+            def unf_dx():
+                xg = x.detach().requires_grad_(True)
+                unfused_torch_layer(xg, *pdt, L, k).backward(dy)
+            tud = time_events(unf_dx, flush, reps)
+            assert wtconv.wtconv_device_faults() == 0
+            ne = x.numel()
+            rows.append({"shape": [N, C, H, W], "levels": L, "k": k, "dtype": dtype,
+                         "fwd_ms": round(tf, 4), "bwd_data_ms": round(tb, 4),
+                         "fwd_gbs": round(2 * ne * x.element_size() / (tf * 1e-3) / 1e9, 1),
+                         "ps_per_element_fwd": round(tf * 1e9 / ne, 3),
+                         "unfused_torch_fwd_ms": round(tu, 4), "unfused_torch_fwd_dx_ms": round(tud, 4),
+                         "dw7x7_cudnn_fwd_ms": round(t7, 4),
+                         "speedup_fwd_vs_unfused": round(tu / tf, 3),
+                         "speedup_fwd_dx_vs_unfused": round(tud / (tf + tb), 3),
+                         "speedup_fwd_vs_dw7x7": round(t7 / tf, 3)})
+            del x, dy, y, dx
+        line = {"suite": "large", "metric": "ms per call on planes beyond one CTA (tiled with a halo)",
+                "rows": rows}
     else:
         N, dtype = 128, "f16"
         tot_fused = tot_unf = 0.0
@@ -751,9 +791,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the unfused-PyTorch and depthwise-7x7 comparison arms")
-    ap.add_argument("--suite", choices=["sweep", "network", "configs"], default=None,
-                    help="time the shape/level sweep, the 18-layer network, or every workload with the "
-                         "oracle beside it, instead of the bench step")
+    ap.add_argument("--suite", choices=["sweep", "network", "configs", "large"], default=None,
+                    help="time the shape/level sweep, the 18-layer network, every workload with the "
+                         "oracle beside it, or the planes larger than one CTA, instead of the bench step")
     ap.add_argument("--arm-only", default=None,
                     choices=["fused", "unfused", "dw7x7", "fused_infer", "unfused_infer", "dw7x7_infer"],
                     help="run only this arm's training step or forward (steps + warmup times, no JSON); "

@@ -8,6 +8,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/wtconv.h"
@@ -119,6 +120,29 @@ void fwd_geometry(const wtconv_desc_t* d, WtFwdPlan& pl, int tp) {
   pl.wf = round_up(off, 4);
 }
 
+// Loop divisors of the analysis, band-convolution and final-tile phases.
+void fwd_divs(WtFwdPlan& pl) {
+  const int L = pl.L;
+  if (L == 1) {
+    pl.an_pp[1] = make_div(pl.Hs[1] * pl.Ws[1]);
+    pl.an_w[1] = make_div(pl.Ws[1]);
+  } else {
+    pl.an_pp[2] = make_div(pl.Hs[2] * pl.Ws[2]);
+    pl.an_w[2] = make_div(pl.Ws[2]);
+  }
+  for (int l = 3; l <= L; ++l) {
+    pl.an_pp[l] = make_div(pl.Hs[l] * pl.Ws[l]);
+    pl.an_w[l] = make_div(pl.Ws[l]);
+  }
+  pl.z_ipp = make_div(pl.zipp);
+  for (int l = 1; l <= L; ++l) {
+    pl.z_tiles[l] = make_div(pl.ztr[l] * pl.ztc[l]);
+    pl.z_tc[l] = make_div(pl.ztc[l]);
+  }
+  pl.f_pp = make_div(pl.ftr * pl.ftc);
+  pl.f_c = make_div(pl.ftc);
+}
+
 wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
   memset(&pl, 0, sizeof(pl));
   pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
@@ -198,24 +222,153 @@ wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %d B of shared memory (max %d)",
                 d->H, d->W, L, pl.smem_bytes, kMaxSmemPerBlock);
   pl.tma_bytes = (uint32_t)(4L * P * pl.xf);
-  if (L == 1) {
-    pl.an_pp[1] = make_div(pl.Hs[1] * pl.Ws[1]);
-    pl.an_w[1] = make_div(pl.Ws[1]);
-  } else {
-    pl.an_pp[2] = make_div(pl.Hs[2] * pl.Ws[2]);
-    pl.an_w[2] = make_div(pl.Ws[2]);
-  }
-  for (int l = 3; l <= L; ++l) {
-    pl.an_pp[l] = make_div(pl.Hs[l] * pl.Ws[l]);
-    pl.an_w[l] = make_div(pl.Ws[l]);
-  }
-  pl.z_ipp = make_div(pl.zipp);
+  fwd_divs(pl);
+  return WTCONV_OK;
+}
+
+// Windowed forward geometry for th x tw output tiles (multiples of
+// max(2^L, 8)) and final tiles of tp x WT_TQ level-1 positions; pl.halo set.
+// Window: Hv x Wv = (th + 2h) x (tw + 2h) pixels, level l exactly
+// (Hv >> l) x (Wv >> l) coefficients.  Input buffer: the window with r zero
+// rows above and below and a 4-float margin left and right (the float32 box
+// copy fills exactly this).  Level buffers: no top margin (the tile's
+// convolution windows start zo - r >= 0 rows into the window), a column
+// margin pcol = (r - zo) mod 4 that puts every convolution window's first
+// column on a 16-byte boundary, and room for the rows and float4 columns
+// the last band-convolution tiles read past the window.  Z buffers hold the
+// tile's coefficients only.
+void win_geometry(const wtconv_desc_t* d, WtFwdPlan& pl, int th, int tw, int tp) {
+  const int R = d->k / 2, L = d->levels, h = pl.halo;
+  const int NV = (WT_ZT + d->k - 1 + 3) / 4;  // float4s per row of a band-convolution window
+  pl.th = th;
+  pl.tw = tw;
+  pl.Hs[0] = th + 2 * h;
+  pl.Ws[0] = tw + 2 * h;
   for (int l = 1; l <= L; ++l) {
-    pl.z_tiles[l] = make_div(pl.ztr[l] * pl.ztc[l]);
-    pl.z_tc[l] = make_div(pl.ztc[l]);
+    pl.Hs[l] = pl.Hs[0] >> l;
+    pl.Ws[l] = pl.Ws[0] >> l;
   }
-  pl.f_pp = make_div(pl.ftr * pl.ftc);
-  pl.f_c = make_div(pl.ftc);
+  pl.ftp = tp;
+  pl.ftr = th / 2 / tp;
+  pl.ftc = tw / 2 / WT_TQ;
+  pl.xf = place(pl.lev[0], 0, pl.Hs[0], pl.Ws[0], R, 4, 1);
+  int off = 0;
+  pl.zbegin[1] = 0;
+  for (int l = 1; l <= L; ++l) {
+    const int zo = h >> l;
+    pl.zo[l] = zo;
+    pl.ztr[l] = ceil_div(th >> l, WT_ZT);
+    pl.ztc[l] = ceil_div(tw >> l, WT_ZT);
+    WtBuf& b = pl.lev[l];
+    b.off = off;
+    b.prow = 0;
+    b.pcol = ((R - zo) % 4 + 4) % 4;
+    const int rows = std::max(pl.Hs[l], zo + WT_ZT * pl.ztr[l] + R);
+    const int cols = std::max(b.pcol + pl.Ws[l], zo + WT_ZT * (pl.ztc[l] - 1) - R + b.pcol + 4 * NV);
+    b.stride = round_up(cols, 4);
+    b.band = rows * b.stride;
+    off += 4 * b.band;
+    pl.zbegin[l + 1] = pl.zbegin[l] + 4 * pl.ztr[l] * pl.ztc[l];
+  }
+  pl.zipp = pl.zbegin[L + 1];
+  for (int l = 1; l <= L; ++l) off = place(pl.zb[l], off, th >> l, tw >> l, 0, 0, 4);
+  pl.wf = round_up(off, 4);
+}
+
+// Shared memory of a windowed plan with P planes per unit and `nsets` input
+// sets: [input sets][16-bit staging][P work areas][weights][2 mbarriers].
+long win_smem_bytes(const WtFwdPlan& pl, int P, int nsets, int load, int wfloats) {
+  const long xslot = round_up(P * pl.xf, 32);
+  const long stage = load == 2 ? round_up((P * pl.Hs[0] * pl.Ws[0] + 1) / 2, 32) : 0;
+  const long mb = (nsets * xslot + stage + (long)P * pl.wf + wfloats + 1) / 2 * 2;
+  return 4 * mb + 16 + WT_SMEM_SLACK;
+}
+
+// Windowed plan for planes too large for plan_fwd.  `load`: 0 = plain loads,
+// 1 = float32 box copies, 2 = 16-bit box copies (see WtFwdPlan::win_load).
+// Tile size, final-tile height, input sets and planes per unit minimise the
+// modelled time of the whole call: the phase-round cost of one unit (as in
+// plan_fwd, with the pyramid over the whole window) times the number of units
+// (edge tiles count whole), weighted by how many CTAs fit an SM: fewer
+// resident CTAs hide less latency, which also makes full-height final tiles
+// (fewer, longer items) cost more.  The weights were fitted to a sweep of
+// forced tilings on a GB300 (224 x 224 planes at levels 1-4 and k = 3, 5, 7;
+// 128 x 128 and 512 x 512 planes; float32 and float16), where the model's
+// choice came within 2% of the fastest tiling measured.
+wtconv_status_t plan_win(const wtconv_desc_t* d, WtFwdPlan& pl, int load) {
+  memset(&pl, 0, sizeof(pl));
+  pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
+  const int R = d->k / 2, L = d->levels, KK = d->k * d->k, S = 1 << L;
+  pl.win = 1;
+  pl.win_load = load;
+  pl.halo = round_up(R * S, 8);
+  const int h = pl.halo, A = S > 8 ? S : 8;
+  pl.w_band = round_up(KK, 4);
+  const int wfloats = (1 + 4 * L) * pl.w_band;
+  const int thmax = round_up(d->H, A), twmax = round_up(d->W, A);
+  const int NT = WT_FWD_THREADS;
+  const long c12 = 100, c3 = 30, cz = 16L * KK + 130, cunit = 400 + 200L * (L > 2 ? L - 2 : 0);
+  const int Pmax = d->N < 1 ? 1 : (d->N < 8 ? d->N : 8);
+  double best = -1.0;
+  int bth = 0, btw = 0, btp = 0, bP = 0, bns = 0;
+  for (int T = A;; T += A) {
+    const int th = T < thmax ? T : thmax, tw = T < twmax ? T : twmax;
+    // one box copy per window and plane: at most 256 elements per dimension
+    if (tw + 2 * h + 8 > 256 || th + 2 * h + 2 * R > 256) break;
+    for (int t = WT_TP; t >= WT_TP / 2; t /= 2) {
+      win_geometry(d, pl, th, tw, t);
+      const int n12 = L >= 2 ? pl.Hs[2] * pl.Ws[2] : pl.Hs[1] * pl.Ws[1];
+      const int nf = pl.ftr * pl.ftc;
+      const long cf = 8L * t * KK + (t == WT_TP ? 400 : 300);
+      for (int q = 1; q <= Pmax; ++q) {
+        for (int ns = (load == 1 ? 2 : 1); ns >= 1; --ns) {
+          const long smem = win_smem_bytes(pl, q, ns, load, wfloats);
+          if (smem > kMaxSmemPerBlock) continue;
+          long ctas = kSmemPerSm / (smem + 1024);
+          if (ctas > 3) ctas = 3;
+          const long cft = cf + (t == WT_TP ? 150 * (3 - ctas) : 0);
+          long cost = ceil_div(q * n12, NT) * c12 + ceil_div(q * pl.zipp, NT) * cz + ceil_div(q * nf, NT) * cft + cunit;
+          for (int l = 3; l <= L; ++l) cost += ceil_div(q * pl.Hs[l] * pl.Ws[l], NT) * c3;
+          if (load == 0) cost += ceil_div(q * pl.Hs[0] * pl.Ws[0] / 4, NT) * 60;  // plain loads stall the unit
+          const double units = (double)ceil_div(d->N > 0 ? d->N : 1, q) * ceil_div(d->H, th) * ceil_div(d->W, tw);
+          const double occ = ctas >= 3 ? 1.0 : ctas == 2 ? 1.25 : 2.0;
+          const double one_set = (load == 1 && ns == 1) ? 1.05 : 1.0;
+          const double total = (double)cost * units * occ * one_set;
+          if (best < 0 || total < best * (1 - 1e-9)) {
+            best = total;
+            bth = th; btw = tw; btp = t; bP = q; bns = ns;
+          }
+        }
+      }
+    }
+    if (th == thmax && tw == twmax) break;
+  }
+  if (best < 0)
+    return fail(WTCONV_ERR_UNSUPPORTED,
+                "plane %dx%d does not fit one CTA, and neither does the smallest %dx%d tile with its %d-pixel halo "
+                "(levels %d, k %d)", d->H, d->W, A, A, h, L, d->k);
+  win_geometry(d, pl, bth, btw, btp);
+  const int P = bP;
+  pl.P = P;
+  pl.nsets = bns;
+  pl.groups = d->N > 0 ? ceil_div(d->N, P) : 0;
+  pl.nty = ceil_div(d->H, bth);
+  pl.ntx = ceil_div(d->W, btw);
+  if ((long long)d->C * pl.groups * pl.nty * pl.ntx >= INT32_MAX)
+    return fail(WTCONV_ERR_UNSUPPORTED, "%lld tile units exceed the 32-bit unit index",
+                (long long)d->C * pl.groups * pl.nty * pl.ntx);
+  pl.xslot = round_up(P * pl.xf, 32);
+  const int stage = load == 2 ? round_up((P * pl.Hs[0] * pl.Ws[0] + 1) / 2, 32) : 0;
+  pl.stage_off = pl.nsets * pl.xslot;
+  pl.work_off = pl.stage_off + stage;
+  pl.w_off = pl.work_off + P * pl.wf;
+  pl.mb_off = round_up(pl.w_off + wfloats, 2);
+  pl.smem_bytes = 4 * pl.mb_off + 16 + WT_SMEM_SLACK;
+  pl.tma_bytes = load == 1 ? (uint32_t)(4L * P * pl.xf) : load == 2 ? (uint32_t)(2L * P * pl.Hs[0] * pl.Ws[0]) : 0u;
+  pl.wd_vec = 1;
+  pl.wd_pp = make_div(pl.Hs[0] * pl.Ws[0] / 4);
+  pl.wd_w = make_div(pl.Ws[0] / 4);
+  fwd_divs(pl);
   return WTCONV_OK;
 }
 
@@ -397,6 +550,41 @@ bool encode_plane_map(CUtensorMap* m, const void* base, const wtconv_desc_t* d, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map over a 16-bit NCHW tensor for the windowed pass: box
+// (box_w, box_h, 1, P) elements, landing as P consecutive raw windows.
+// Rows must be whole 16-byte chunks (W % 8 == 0) and box_w a multiple of 8.
+bool encode_map16(CUtensorMap* m, const void* base, const wtconv_desc_t* d, int box_w, int box_h, int P) {
+  if (d->dtype == WTCONV_F32 || (d->W % 8) != 0 || !aligned(base, 16)) return false;
+  if (box_w > 256 || box_h > 256 || P > 256 || (box_w % 8) != 0) return false;
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)d->W, (cuuint64_t)d->H, (cuuint64_t)d->C, (cuuint64_t)d->N};
+  const cuuint64_t strides[3] = {2ull * d->W, 2ull * d->W * d->H, 2ull * d->W * d->H * d->C};
+  const cuuint32_t box[4] = {(cuuint32_t)box_w, (cuuint32_t)box_h, 1u, (cuuint32_t)P};
+  const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+  const CUtensorMapDataType t =
+      d->dtype == WTCONV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return fn(m, t, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Window load mode for source `src`: box copies when its rows are whole
+// 16-byte chunks and it is 16-byte aligned, else plain loads.
+int win_load_mode(const wtconv_desc_t* d, const void* src) {
+  if (!aligned(src, 16)) return 0;
+  if (d->dtype == WTCONV_F32) return d->W % 4 == 0 ? 1 : 0;
+  return d->W % 8 == 0 ? 2 : 0;
+}
+
+// Plan of the forward / input-gradient pass: whole planes when a plane and
+// its pyramid fit one CTA, else output tiles with a halo.
+wtconv_status_t plan_any(const wtconv_desc_t* d, WtFwdPlan& pl, const void* src) {
+  const wtconv_status_t st = plan_fwd(d, pl);
+  if (st != WTCONV_ERR_UNSUPPORTED) return st;
+  return plan_win(d, pl, win_load_mode(d, src));
+}
+
 wtconv_status_t check_act(const void* p, const char* name, const wtconv_desc_t* d) {
   if (!p) return fail(WTCONV_ERR_INVALID_ARG, "%s is NULL", name);
   if (!aligned(p, elem_size(d->dtype)))
@@ -455,6 +643,24 @@ size_t bw_workspace_bytes(const WtBwPlan& pl) {
     if (st_ != WTCONV_OK) return st_; \
   } while (0)
 
+// Pointer-dependent parts of a windowed plan: the box tensor map (re-planned
+// for plain loads if it cannot be encoded) and the plain-load divisors.
+wtconv_status_t prepare_win(const wtconv_desc_t* d, WtFwdPlan& pl, CUtensorMap* m, const void* src,
+                            const void* dst) {
+  bool boxed = true;
+  if (pl.win_load == 1)
+    boxed = encode_plane_map(m, src, d, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
+  else if (pl.win_load == 2)
+    boxed = encode_map16(m, src, d, pl.Ws[0], pl.Hs[0], pl.P);
+  if (!boxed) WT_TRY(plan_win(d, pl, 0));
+  pl.vec_ok = vec_ok(d, src, dst);
+  const int per_row = pl.vec_ok ? pl.Ws[0] / (int)(16 / elem_size(d->dtype)) : pl.Ws[0];
+  pl.ld_pp = make_div(pl.Hs[0] * per_row);
+  pl.ld_w = make_div(per_row);
+  return WTCONV_OK;
+}
+
+
 }  // namespace
 
 namespace wt {
@@ -484,17 +690,24 @@ wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float
   WT_TRY(check_param(base_scale, "base_scale", false));
   WT_TRY(check_param(wavelet_scale, "wavelet_scale", false));
   WtFwdPlan pl;
-  WT_TRY(plan_fwd(desc, pl));
+  WT_TRY(plan_any(desc, pl, x));
   if (desc->N == 0) return ok();
   WT_TRY(check_act(x, "x", desc));
   WT_TRY(check_act(y, "y", desc));
-  set_load_divs(pl, desc, vec_ok(desc, x, y));
   alignas(64) CUtensorMap tmx;
   memset(&tmx, 0, sizeof(tmx));
-  pl.use_tma = encode_plane_map(&tmx, x, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
-  set_bulk(pl, desc, x, 4L * (pl.work_off - pl.stage_off));
-  cudaError_t e = wt::launch_fwd(pl, tmx, desc->dtype, false, x, w_base, b_base, w_sub, base_scale,
-                                 wavelet_scale, y, (cudaStream_t)stream);
+  cudaError_t e;
+  if (pl.win) {
+    WT_TRY(prepare_win(desc, pl, &tmx, x, y));
+    e = wt::launch_fwd_win(pl, tmx, desc->dtype, false, x, w_base, b_base, w_sub, base_scale, wavelet_scale, y,
+                           (cudaStream_t)stream);
+  } else {
+    set_load_divs(pl, desc, vec_ok(desc, x, y));
+    pl.use_tma = encode_plane_map(&tmx, x, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
+    set_bulk(pl, desc, x, 4L * (pl.work_off - pl.stage_off));
+    e = wt::launch_fwd(pl, tmx, desc->dtype, false, x, w_base, b_base, w_sub, base_scale, wavelet_scale, y,
+                       (cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_fwd: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -511,17 +724,24 @@ wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const
   WT_TRY(check_param(base_scale, "base_scale", false));
   WT_TRY(check_param(wavelet_scale, "wavelet_scale", false));
   WtFwdPlan pl;
-  WT_TRY(plan_fwd(desc, pl));
+  WT_TRY(plan_any(desc, pl, dy));
   if (desc->N == 0) return ok();
   WT_TRY(check_act(dy, "dy", desc));
   WT_TRY(check_act(dx, "dx", desc));
-  set_load_divs(pl, desc, vec_ok(desc, dy, dx));
   alignas(64) CUtensorMap tmx;
   memset(&tmx, 0, sizeof(tmx));
-  pl.use_tma = encode_plane_map(&tmx, dy, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
-  set_bulk(pl, desc, dy, 4L * (pl.work_off - pl.stage_off));
-  cudaError_t e = wt::launch_fwd(pl, tmx, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale,
-                                 wavelet_scale, dx, (cudaStream_t)stream);
+  cudaError_t e;
+  if (pl.win) {
+    WT_TRY(prepare_win(desc, pl, &tmx, dy, dx));
+    e = wt::launch_fwd_win(pl, tmx, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale, wavelet_scale,
+                           dx, (cudaStream_t)stream);
+  } else {
+    set_load_divs(pl, desc, vec_ok(desc, dy, dx));
+    pl.use_tma = encode_plane_map(&tmx, dy, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
+    set_bulk(pl, desc, dy, 4L * (pl.work_off - pl.stage_off));
+    e = wt::launch_fwd(pl, tmx, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale, wavelet_scale, dx,
+                       (cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_data: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -593,7 +813,7 @@ const char* wtconv_last_error(void) { return g_last_error; }
 
 unsigned int wtconv_device_faults(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return 0;
-  return wt::take_fwd_faults() + wt::take_bw_faults();
+  return wt::take_fwd_faults() + wt::take_win_faults() + wt::take_bw_faults();
 }
 
 }  // extern "C"

@@ -14,9 +14,16 @@ cudaError_t launch_fwd(const WtFwdPlan& pl, const CUtensorMap& tmx, int dtype, b
                        const float* w_base, const float* b_base, const float* w_sub, const float* s_base,
                        const float* s_w, void* y, cudaStream_t stream);
 
+// The same passes for planes too large for one CTA, tile by tile with a halo
+// (pl.win = 1); tmx describes x for the box copies (pl.win_load = 1 or 2).
+cudaError_t launch_fwd_win(const WtFwdPlan& pl, const CUtensorMap& tmx, int dtype, bool rotate, const void* x,
+                           const float* w_base, const float* b_base, const float* w_sub, const float* s_base,
+                           const float* s_w, void* y, cudaStream_t stream);
+
 // Number of bounded in-kernel waits that gave up since the last call
 // (reads and clears a device counter; synchronises the device).
 unsigned int take_fwd_faults();
+unsigned int take_win_faults();
 unsigned int take_bw_faults();
 
 // Parameter gradients: correlation kernel into `part`, then the finalize kernel.

@@ -74,6 +74,20 @@ struct WtFwdPlan {
   WtDiv z_ipp;                                  // band-convolution items per plane
   WtDiv z_tiles[WT_MAXL + 1], z_tc[WT_MAXL + 1];  // ztr*ztc and ztc per level
   WtDiv f_pp, f_c;                              // final tiles per plane, per row
+  // Windowed mode, for planes whose pyramid does not fit one CTA: a unit is
+  // one th x tw output tile of P planes of one channel.  The CTA loads the
+  // tile's window, the tile plus `halo` pixels on every side (zero outside
+  // the H x W plane), builds the Haar pyramid of the whole window, and
+  // convolves the bands and runs the final tiles on the tile only.  Hs/Ws and
+  // lev[] then describe the window (Hs[0] x Ws[0] pixels), ztr/ztc, zb[] and
+  // ftr/ftc the tile; H and W stay the plane's.
+  int win;               // 1 = windowed mode
+  int halo;              // h: 2^L * r rounded up to 8 (a multiple of 2^L, and of 8 for 16-byte rows)
+  int th, tw;            // output tile, multiples of max(2^L, 8)
+  int nty, ntx;          // tiles per plane
+  int zo[WT_MAXL + 1];   // h >> l: the tile's first level-l coefficient row / column in the window
+  int win_load;          // 0 = plain loads, 1 = float32 box copy (margins included), 2 = 16-bit box copy into
+                         // the staging area, widened per unit
 };
 
 // Parameter-gradient pass.  The work is C * batches units (channel c, batch

@@ -114,6 +114,12 @@ SWEEP_SHAPES = ((96, 56), (192, 28), (384, 14), (768, 7))
 SWEEP_LEVELS = (1, 2, 3, 4, 5)
 # All WTConv layers of WTConvNeXt-T at 224x224 input: (C, H=W, depth, levels).
 NETWORK_STAGES = ((96, 56, 3, 5), (192, 28, 3, 4), (384, 14, 9, 3), (768, 7, 3, 2))
+# Planes larger than one CTA holds (run tile by tile with a halo): a WTConv
+# layer at the stem resolution of a 224x224 image for levels 1-4, and larger
+# maps.  (N, C, H, W, levels, k, dtype); every tensor is larger than the L2.
+LARGE_PLANES = ((16, 64, 224, 224, 1, 5, "f32"), (16, 64, 224, 224, 2, 5, "f32"), (16, 64, 224, 224, 3, 5, "f32"),
+                (16, 64, 224, 224, 4, 5, "f32"), (32, 64, 224, 224, 3, 5, "f16"), (32, 96, 128, 128, 3, 5, "f32"),
+                (16, 32, 384, 384, 2, 5, "f32"), (8, 32, 512, 512, 2, 5, "f16"))
 
 
 def workload(name: str, **overrides) -> LayerInputs:
