@@ -479,9 +479,10 @@ def run_suite(args):
             del x, dy
         line = {"suite": "configs", "metric": "fwd+bwd ms per layer; oracle seconds per layer", "rows": rows}
     elif args.suite == "large":
-        # Planes beyond one CTA: the windowed forward and input gradient
-        # against the unfused PyTorch composition (forward, and forward +
-        # autograd input gradient) and a cuDNN depthwise 7x7 on the same x.
+        # Planes beyond one CTA (tiled with a halo): each call of the fused
+        # layer, and the training step (all three calls) against the unfused
+        # PyTorch composition with autograd and a cuDNN depthwise 7x7, forward
+        # alone and forward + backward, on the same x.
         for N, C, H, W, L, k, dtype in synth.LARGE_PLANES:
             pin = synth.make_inputs(1, C, 1, 1, L, k, dtype=dtype, seed=5000 + C + L)
             ps = [torch.tensor(a, dtype=torch.float32, device=dev) for a in
@@ -490,31 +491,43 @@ def run_suite(args):
             g = torch.Generator(device=dev).manual_seed(5000 + H + L)
             x = torch.randn(N, C, H, W, generator=g, device=dev).to(tdt[dtype])
             dy = torch.randn(N, C, H, W, generator=g, device=dev).to(tdt[dtype])
-            y, dx = torch.empty_like(x), torch.empty_like(x)
-            w7 = torch.zeros(C, 1, 7, 7, dtype=tdt[dtype], device=dev)
-            tf = time_events(lambda: wtconv.wtconv_fwd(x, *ps, L, k, y=y), flush, reps)
-            tb = time_events(lambda: wtconv.wtconv_bwd_data(dy, ps[0], ps[2], ps[3], ps[4], L, k, dx=dx), flush, reps)
+            out = buffers(x, ps, L, k)
+            w7 = torch.zeros(C, 1, 7, 7, dtype=tdt[dtype], device=dev, requires_grad=True)
+            tf = time_events(lambda: wtconv.wtconv_fwd(x, *ps, L, k, y=out["y"]), flush, reps)
+            tb = time_events(lambda: wtconv.wtconv_bwd_data(dy, ps[0], ps[2], ps[3], ps[4], L, k, dx=out["dx"]),
+                             flush, reps)
+            tw = time_events(lambda: wtconv.wtconv_bwd_weight(x, dy, *ps, L, k, grads=out["g"], workspace=out["ws"]),
+                             flush, reps)
+            tt = time_events(fused_step(x, dy, ps, L, k, out), flush, reps)
             with torch.no_grad():
                 tu = time_events(lambda: unfused_torch_layer(x, *pdt, L, k), flush, reps)
                 t7 = time_events(lambda: F.conv2d(x, w7, padding=3, groups=C), flush, reps)
 
-            def unf_dx():
+            def unf_train():
                 xg = x.detach().requires_grad_(True)
-                unfused_torch_layer(xg, *pdt, L, k).backward(dy)
-            tud = time_events(unf_dx, flush, reps)
+                leaves = [p.detach().clone().requires_grad_(True) for p in pdt]
+                unfused_torch_layer(xg, *leaves, L, k).backward(dy)
+
+            def dw7_train():
+                xg = x.detach().requires_grad_(True)
+                F.conv2d(xg, w7, padding=3, groups=C).backward(dy)
+            tut = time_events(unf_train, flush, reps)
+            t7t = time_events(dw7_train, flush, reps)
             assert wtconv.wtconv_device_faults() == 0
             ne = x.numel()
             rows.append({"shape": [N, C, H, W], "levels": L, "k": k, "dtype": dtype,
-                         "fwd_ms": round(tf, 4), "bwd_data_ms": round(tb, 4),
-                         "fwd_gbs": round(2 * ne * x.element_size() / (tf * 1e-3) / 1e9, 1),
+                         "fwd_ms": round(tf, 4), "bwd_data_ms": round(tb, 4), "bwd_weight_ms": round(tw, 4),
+                         "fused_fwd_bwd_ms": round(tt, 4),
                          "ps_per_element_fwd": round(tf * 1e9 / ne, 3),
-                         "unfused_torch_fwd_ms": round(tu, 4), "unfused_torch_fwd_dx_ms": round(tud, 4),
-                         "dw7x7_cudnn_fwd_ms": round(t7, 4),
+                         "hbm_tbs_fwd_bwd": round(6 * ne * x.element_size() / (tt * 1e-3) / 1e12, 3),
+                         "unfused_torch_fwd_ms": round(tu, 4), "unfused_torch_fwd_bwd_ms": round(tut, 4),
+                         "dw7x7_cudnn_fwd_ms": round(t7, 4), "dw7x7_cudnn_fwd_bwd_ms": round(t7t, 4),
                          "speedup_fwd_vs_unfused": round(tu / tf, 3),
-                         "speedup_fwd_dx_vs_unfused": round(tud / (tf + tb), 3),
-                         "speedup_fwd_vs_dw7x7": round(t7 / tf, 3)})
-            del x, dy, y, dx
-        line = {"suite": "large", "metric": "ms per call on planes beyond one CTA (tiled with a halo)",
+                         "speedup_fwd_bwd_vs_unfused": round(tut / tt, 3),
+                         "speedup_fwd_vs_dw7x7": round(t7 / tf, 3),
+                         "speedup_fwd_bwd_vs_dw7x7": round(t7t / tt, 3)})
+            del x, dy, out
+        line = {"suite": "large", "metric": "ms per call and per fwd+bwd step on planes beyond one CTA (tiled with a halo)",
                 "rows": rows}
     else:
         N, dtype = 128, "f16"

@@ -44,16 +44,15 @@
  *     CUDA launch error it returns WTCONV_ERR_CUDA.  wtconv_last_error()
  *     returns a thread-local message describing the last failure.
  *   - Limits: 3 <= k <= 9, k odd; 1 <= levels <= 8; N >= 0; C, H, W >= 1;
- *     H * W <= 2^24.  wtconv_fwd and wtconv_bwd_data keep a whole plane and
- *     its pyramid in one CTA's shared memory when it fits (square planes up
- *     to 92..112 px, depending on k and levels); larger planes run in output
- *     tiles, each computed from a window that adds a halo of 2^levels * (k/2)
- *     pixels (rounded up to 8) on every side, which must itself fit one CTA:
- *     levels <= 4 at every k, levels = 5 at k = 3.  wtconv_bwd_weight keeps
- *     whole planes only: up to 56 px (64 px at levels = 1), since its
- *     per-thread gradient tiles must also fit in registers.  Anything beyond
- *     returns WTCONV_ERR_UNSUPPORTED before anything is launched.  N = 0 is
- *     a valid empty batch.
+ *     H * W <= 2^24.  Each call keeps whole planes and their pyramids in one
+ *     CTA's shared memory when they fit (square planes up to 92..112 px for
+ *     wtconv_fwd and wtconv_bwd_data, up to 56 px, or 64 px at levels = 1,
+ *     for wtconv_bwd_weight, depending on k and levels).  Larger planes run
+ *     in output tiles, each computed from a window of x (or dy) that adds a
+ *     halo of 2^levels * (k/2) pixels, rounded up to 8, on every side.  That
+ *     window must itself fit one CTA: levels <= 4 at every k, levels = 5 at
+ *     k = 3.  Beyond that a call returns WTCONV_ERR_UNSUPPORTED before
+ *     anything is launched.  N = 0 is a valid empty batch.
  *   - Pointers must be aligned to their element size (WTCONV_ERR_MISALIGNED
  *     otherwise); 16-byte alignment enables vector loads and stores.
  */

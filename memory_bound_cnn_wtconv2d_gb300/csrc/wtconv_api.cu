@@ -409,6 +409,28 @@ void bw_layout(WtBwPlan& pl, int nsets, bool staging) {
   pl.tma_bytes = (uint32_t)(4L * P * (pl.xbf + pl.dbf));
 }
 
+// Persistent grid and record slots of a gradient plan whose `batches` (units
+// per channel) is set; `per_sm` resident CTAs per SM.
+wtconv_status_t bw_grid(const wtconv_desc_t* d, WtBwPlan& pl, int per_sm) {
+  const long long U = (long long)d->C * pl.batches;
+  if (U >= (1 << 24))
+    return fail(WTCONV_ERR_UNSUPPORTED, "%lld gradient units exceed the 2^24 index range", U);
+  pl.nb_div = make_div(pl.batches > 0 ? pl.batches : 1);
+  const long long slots_total = (long long)kNumSms * per_sm;
+  pl.grid = (int)(U < slots_total ? U : slots_total);
+  if (pl.grid < 1) pl.grid = 1;
+  pl.uq = (int)(U / pl.grid);
+  pl.ur = (int)(U % pl.grid);
+  pl.g_div = make_div(pl.grid);
+  pl.nrec = 0;
+  for (int i = 0; i < pl.grid && U > 0; ++i) {
+    const int ub = bw_unit_begin(pl, i), ue = bw_unit_begin(pl, i + 1);
+    const int span = (ue - 1) / pl.batches - ub / pl.batches + 1;
+    if (span > pl.nrec) pl.nrec = span;
+  }
+  return WTCONV_OK;
+}
+
 wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
   memset(&pl, 0, sizeof(pl));
   pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
@@ -491,23 +513,176 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
   const int per_sm = per_sm_of(pl);
   // Persistent grid: every resident CTA slot, at most one CTA per unit.
   pl.batches = d->N > 0 ? ceil_div(d->N, P) : 0;
-  const long long U = (long long)d->C * pl.batches;
-  if (U >= (1 << 24))
-    return fail(WTCONV_ERR_UNSUPPORTED, "%lld (channel, batch) units exceed the 2^24 index range", U);
-  pl.nb_div = make_div(pl.batches > 0 ? pl.batches : 1);
-  const long long slots_total = (long long)kNumSms * per_sm;
-  pl.grid = (int)(U < slots_total ? U : slots_total);
-  if (pl.grid < 1) pl.grid = 1;
-  pl.uq = (int)(U / pl.grid);
-  pl.ur = (int)(U % pl.grid);
-  pl.g_div = make_div(pl.grid);
-  pl.nrec = 0;
-  for (int i = 0; i < pl.grid && U > 0; ++i) {
-    const int ub = bw_unit_begin(pl, i), ue = bw_unit_begin(pl, i + 1);
-    const int span = (ue - 1) / pl.batches - ub / pl.batches + 1;
-    if (span > pl.nrec) pl.nrec = span;
+  return bw_grid(d, pl, per_sm);
+}
+
+// Windowed parameter-gradient geometry for th x tw tiles and tbr-row
+// correlation tiles; pl.halo set.  x window: (th + 2h) x (tw + 2h) pixels
+// with r zero rows above and below and a 4-float margin left and right (the
+// float32 box copy fills exactly this); dy tile: th x tw, no margin.  x
+// level buffers: no top margin, a column margin (r - zo) mod 4 that puts
+// every correlation window's first column on a 16-byte boundary, and room
+// for the rows and float4 columns the last correlation tiles read past the
+// window; dy level buffers: the tile's coefficients rounded up to whole
+// correlation tiles (the rounding margin stays zero).
+void bw_win_geometry(const wtconv_desc_t* d, WtBwPlan& pl, int th, int tw, int tbr) {
+  const int R = d->k / 2, L = d->levels, h = pl.halo;
+  const int NV = (4 + d->k - 1 + 3) / 4;  // float4s per row of a correlation window
+  pl.th = th;
+  pl.tw = tw;
+  pl.tbr = tbr;
+  pl.tcw = 4;
+  pl.Hs[0] = th + 2 * h;
+  pl.Ws[0] = tw + 2 * h;
+  for (int l = 0; l <= L; ++l) {
+    pl.Hs[l] = pl.Hs[0] >> l;
+    pl.Ws[l] = pl.Ws[0] >> l;
+    pl.dHs[l] = th >> l;
+    pl.dWs[l] = tw >> l;
   }
-  return WTCONV_OK;
+  pl.item_begin[0] = 0;
+  for (int l = 0; l <= L; ++l) {
+    pl.tr[l] = ceil_div(th >> l, tbr);
+    pl.tc[l] = ceil_div(tw >> l, 4);
+    pl.item_begin[l + 1] = pl.item_begin[l] + (l == 0 ? 1 : 4) * pl.tr[l] * pl.tc[l];
+  }
+  pl.items_per_plane = pl.item_begin[L + 1];
+  pl.xbf = place(pl.xs[0], 0, pl.Hs[0], pl.Ws[0], R, 4, 1);
+  pl.dbf = place(pl.ds[0], 0, th, tw, 0, 0, 1);
+  int off = 0;
+  for (int l = 1; l <= L; ++l) {
+    const int zo = h >> l;
+    pl.zo[l] = zo;
+    WtBuf& b = pl.xs[l];
+    b.off = off;
+    b.prow = 0;
+    b.pcol = ((R - zo) % 4 + 4) % 4;
+    const int rows = std::max(pl.Hs[l], zo + tbr * pl.tr[l] + R);
+    const int cols = std::max(b.pcol + pl.Ws[l], zo + 4 * (pl.tc[l] - 1) - R + b.pcol + 4 * NV);
+    b.stride = round_up(cols, 4);
+    b.band = rows * b.stride;
+    off += 4 * b.band;
+    off = place(pl.ds[l], off, tbr * pl.tr[l], 4 * pl.tc[l], 0, 0, 4);
+  }
+  pl.wf = round_up(off, 4);
+}
+
+// Shared-memory layout of a windowed gradient plan: [input sets: P x windows,
+// then P dy tiles][16-bit staging: raw x windows, then raw dy tiles][work
+// area: P pyramid pairs, or the end-of-channel reduction if larger][mbarriers].
+void bw_win_layout(WtBwPlan& pl, int P, int nsets, int load) {
+  const int KK = pl.K * pl.K;
+  pl.P = P;
+  pl.nsets = nsets;
+  pl.xr = round_up(P * pl.xbf, 32);
+  pl.islot = pl.xr + round_up(P * pl.dbf, 32);
+  int off = nsets * pl.islot;
+  pl.stage_off = off;
+  pl.stage_dx = 0;
+  if (load == 2) {
+    pl.stage_dx = round_up((P * pl.Hs[0] * pl.Ws[0] + 1) / 2, 32);
+    off += pl.stage_dx + round_up((P * pl.th * pl.tw + 1) / 2, 32);
+  }
+  pl.work_off = off;
+  long region = (long)P * pl.wf;
+  const long red = (long)P * pl.items_per_plane * (KK + 1);
+  if (red > region) region = red;
+  pl.red_floats = (int)((region + 3) / 4 * 4);
+  pl.mb_off = pl.work_off + pl.red_floats;
+  const long smem = 4L * pl.mb_off + 16 + WT_SMEM_SLACK;
+  pl.smem_bytes = smem > INT32_MAX ? INT32_MAX : (int)smem;
+  pl.tma_bytes = load == 1 ? (uint32_t)(4L * P * (pl.xbf + pl.dbf))
+                           : load == 2 ? (uint32_t)(2L * P * (pl.Hs[0] * pl.Ws[0] + pl.th * pl.tw)) : 0u;
+}
+
+// Windowed parameter-gradient plan for planes too large for plan_bw.
+// `load` as for plan_win.  Tile, correlation-tile height, planes per unit and
+// input sets minimise the modelled time of the call, as in plan_win: phase
+// rounds of the 256 threads (both pyramids, then one or two correlation
+// items per thread) times the number of units, weighted by the CTAs that fit
+// an SM (shared memory; at most 2, which the registers of 256-thread CTAs
+// allow at k <= 5).
+wtconv_status_t plan_bw_win(const wtconv_desc_t* d, WtBwPlan& pl, int load) {
+  memset(&pl, 0, sizeof(pl));
+  pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
+  const int R = d->k / 2, L = d->levels, KK = d->k * d->k, S = 1 << L;
+  pl.win = 1;
+  pl.win_load = load;
+  pl.halo = round_up(R * S, 8);
+  const int h = pl.halo, A = S > 8 ? S : 8;
+  const int thmax = round_up(d->H, A), twmax = round_up(d->W, A);
+  const int NT = WT_BW_THREADS;
+  const long c12 = 100, c3 = 30, cunit = 600 + 200L * (L > 2 ? L - 2 : 0);
+  const int Pmax = d->N < 1 ? 1 : (d->N < 8 ? d->N : 8);
+  double best = -1.0;
+  int bth = 0, btw = 0, btr = 0, bP = 0, bns = 0;
+  for (int T = A;; T += A) {
+    const int th = T < thmax ? T : thmax, tw = T < twmax ? T : twmax;
+    if (tw + 2 * h + 8 > 256 || th + 2 * h + 2 * R > 256) break;  // one box per window and plane
+    for (int tbr = 8; tbr >= 4; tbr /= 2) {
+      bw_win_geometry(d, pl, th, tw, tbr);
+      const int slots = (tbr == 8 ? 1 : WT_BW_MAX_ITEMS) * NT;
+      const int n12x = L >= 2 ? pl.Hs[2] * pl.Ws[2] : pl.Hs[1] * pl.Ws[1];
+      const int n12d = L >= 2 ? pl.dHs[2] * pl.dWs[2] : pl.dHs[1] * pl.dWs[1];
+      const long citem = 4L * tbr * KK + 200;
+      for (int q = 1; q <= Pmax && q * pl.items_per_plane <= slots; ++q) {
+        for (int ns = (load == 1 ? 2 : 1); ns >= 1; --ns) {
+          bw_win_layout(pl, q, ns, load);
+          if (pl.smem_bytes > kMaxSmemPerBlock) continue;
+          long ctas = kSmemPerSm / (pl.smem_bytes + 1024);
+          if (ctas > 2) ctas = 2;
+          long cost = ceil_div(q * n12x, NT) * c12 + ceil_div(q * n12d, NT) * c12 +
+                      ceil_div(q * pl.items_per_plane, NT) * citem + cunit;
+          for (int l = 3; l <= L; ++l)
+            cost += (ceil_div(q * pl.Hs[l] * pl.Ws[l], NT) + ceil_div(q * pl.dHs[l] * pl.dWs[l], NT)) * c3;
+          if (load == 0) cost += ceil_div(q * (pl.Hs[0] * pl.Ws[0] + th * tw) / 4, NT) * 60;
+          const double units = (double)ceil_div(d->N > 0 ? d->N : 1, q) * ceil_div(d->H, th) * ceil_div(d->W, tw);
+          const double occ = ctas >= 2 ? 1.0 : 1.6;
+          const double one_set = (load == 1 && ns == 1) ? 1.05 : 1.0;
+          const double total = (double)cost * units * occ * one_set;
+          if (best < 0 || total < best * (1 - 1e-9)) {
+            best = total;
+            bth = th; btw = tw; btr = tbr; bP = q; bns = ns;
+          }
+        }
+      }
+    }
+    if (th == thmax && tw == twmax) break;
+  }
+  if (best < 0)
+    return fail(WTCONV_ERR_UNSUPPORTED,
+                "plane %dx%d does not fit one CTA for the parameter gradient, and neither does the smallest "
+                "%dx%d tile with its %d-pixel halo (levels %d, k %d)", d->H, d->W, A, A, h, L, d->k);
+  bw_win_geometry(d, pl, bth, btw, btr);
+  bw_win_layout(pl, bP, bns, load);
+  pl.groups = d->N > 0 ? ceil_div(d->N, bP) : 0;
+  pl.nty = ceil_div(d->H, bth);
+  pl.ntx = ceil_div(d->W, btw);
+  if ((long long)pl.groups * pl.nty * pl.ntx >= (1 << 24))
+    return fail(WTCONV_ERR_UNSUPPORTED, "too many gradient tiles per channel");
+  pl.batches = pl.groups * pl.nty * pl.ntx;
+  pl.nbands = 1 + 4 * L;
+  pl.part_stride = pl.nbands * (KK + 1);
+  for (int l = 0; l <= L; ++l) {
+    pl.an_pp[l] = make_div(pl.Hs[l] * pl.Ws[l]);
+    pl.an_w[l] = make_div(pl.Ws[l]);
+    pl.dn_pp[l] = make_div(pl.dHs[l] * pl.dWs[l]);
+    pl.dn_w[l] = make_div(pl.dWs[l]);
+    pl.tiles[l] = make_div(pl.tr[l] * pl.tc[l]);
+    pl.tcd[l] = make_div(pl.tc[l]);
+  }
+  pl.ipp = make_div(pl.items_per_plane);
+  pl.wd_vec = 1;
+  pl.wd_pp = make_div(pl.Hs[0] * pl.Ws[0] / 4);
+  pl.wd_w = make_div(pl.Ws[0] / 4);
+  pl.dwd_pp = make_div(pl.th * pl.tw / 4);
+  pl.dwd_w = make_div(pl.tw / 4);
+  int per_sm = wt::bw_win_ctas_per_sm(pl, d->dtype);
+  if (per_sm <= 0) {
+    per_sm = (int)(kSmemPerSm / (pl.smem_bytes + 1024));
+    if (per_sm > 2) per_sm = 2;
+  }
+  return bw_grid(d, pl, per_sm < 1 ? 1 : per_sm);
 }
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
@@ -575,6 +750,16 @@ int win_load_mode(const wtconv_desc_t* d, const void* src) {
   if (!aligned(src, 16)) return 0;
   if (d->dtype == WTCONV_F32) return d->W % 4 == 0 ? 1 : 0;
   return d->W % 8 == 0 ? 2 : 0;
+}
+
+// Plan of the parameter-gradient pass: whole planes when both pyramids fit
+// one CTA, else tiles with a halo on x.  Box copies need x and dy 16-byte
+// aligned with 16-byte rows.
+wtconv_status_t plan_bw_any(const wtconv_desc_t* d, WtBwPlan& pl, const void* x, const void* dy) {
+  const wtconv_status_t st = plan_bw(d, pl);
+  if (st != WTCONV_ERR_UNSUPPORTED) return st;
+  const int mx = win_load_mode(d, x), md = win_load_mode(d, dy);
+  return plan_bw_win(d, pl, mx == md ? mx : 0);
 }
 
 // Plan of the forward / input-gradient pass: whole planes when a plane and
@@ -673,8 +858,18 @@ size_t wtconv_workspace_size(const wtconv_desc_t* desc, int op) {
   if (validate_desc(desc) != WTCONV_OK) return 0;
   if (op != WTCONV_OP_BWD_WEIGHT) return 0;
   WtBwPlan pl;
-  if (plan_bw(desc, pl) != WTCONV_OK) return 0;
-  return bw_workspace_bytes(pl);
+  const wtconv_status_t st = plan_bw(desc, pl);
+  if (st == WTCONV_OK) return bw_workspace_bytes(pl);
+  if (st != WTCONV_ERR_UNSUPPORTED) return 0;
+  // Windowed: the plan (and with it the grid and the record count) depends on
+  // how the tensors can be loaded, which the pointers decide at call time;
+  // the size covers every way.
+  size_t bytes = 0;
+  const int box = desc->dtype == WTCONV_F32 ? (desc->W % 4 == 0 ? 1 : 0) : (desc->W % 8 == 0 ? 2 : 0);
+  for (int load = 0; load <= box; load += box > 0 ? box : 1) {
+    if (plan_bw_win(desc, pl, load) == WTCONV_OK) bytes = std::max(bytes, bw_workspace_bytes(pl));
+  }
+  return bytes;
 }
 
 wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float* w_base,
@@ -763,7 +958,7 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
   WT_TRY(check_param(dbase_scale, "dbase_scale", false));
   WT_TRY(check_param(dwavelet_scale, "dwavelet_scale", false));
   WtBwPlan pl;
-  WT_TRY(plan_bw(desc, pl));
+  WT_TRY(plan_bw_any(desc, pl, x, dy));
   cudaStream_t st = (cudaStream_t)stream;
   const int C = desc->C, L = desc->levels, KK = desc->k * desc->k;
   if (desc->N == 0) {  // empty batch: every gradient is an empty sum
@@ -777,17 +972,42 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
   }
   WT_TRY(check_act(x, "x", desc));
   WT_TRY(check_act(dy, "dy", desc));
+  alignas(64) CUtensorMap tmx, tmd;
+  memset(&tmx, 0, sizeof(tmx));
+  memset(&tmd, 0, sizeof(tmd));
+  if (pl.win) {
+    // box copies of the x windows and dy tiles (re-planned for plain loads if
+    // a map cannot be encoded), then the plain-load divisors
+    bool boxed = true;
+    if (pl.win_load == 1)
+      boxed = encode_plane_map(&tmx, x, desc, pl.xs[0].stride, pl.xbf / pl.xs[0].stride, pl.P) &&
+              encode_plane_map(&tmd, dy, desc, pl.ds[0].stride, pl.th, pl.P);
+    else if (pl.win_load == 2)
+      boxed = encode_map16(&tmx, x, desc, pl.Ws[0], pl.Hs[0], pl.P) &&
+              encode_map16(&tmd, dy, desc, pl.tw, pl.th, pl.P);
+    if (!boxed) WT_TRY(plan_bw_win(desc, pl, 0));
+    pl.vec_ok = vec_ok(desc, x, dy);
+    const int v = pl.vec_ok ? (int)(16 / elem_size(desc->dtype)) : 1;
+    pl.ld_pp = make_div(pl.Hs[0] * (pl.Ws[0] / v));
+    pl.ld_w = make_div(pl.Ws[0] / v);
+    pl.dld_pp = make_div(pl.th * (pl.tw / v));
+    pl.dld_w = make_div(pl.tw / v);
+  }
   const size_t need = bw_workspace_bytes(pl);
   if (!ws || ws_bytes < need)
     return fail(WTCONV_ERR_WORKSPACE, "workspace of %zu B given, %zu B needed", ws ? ws_bytes : 0, need);
   if (!aligned(ws, 256)) return fail(WTCONV_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+  if (pl.win) {
+    cudaError_t e = wt::launch_bwd_weight_win(pl, tmx, tmd, desc->dtype, x, dy, w_base, b_base, w_sub, base_scale,
+                                              wavelet_scale, dw_base, db_base, dw_sub, dbase_scale, dwavelet_scale,
+                                              static_cast<float*>(ws), st);
+    if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_weight: %s", cudaGetErrorString(e));
+    return ok();
+  }
   set_load_divs(pl, desc, vec_ok(desc, x, dy));
   set_bulk(pl, desc, x, pl.stage_off > 0 ? 4L * (pl.work_off - pl.stage_off) / 2 : 0);
   if (pl.use_bulk == 1 && !(aligned(dy, 16) && 2L * pl.P * pl.bulk_bytes < (1L << 20))) pl.use_bulk = 2;
   if (pl.use_bulk == 2 && !aligned(dy, 8)) pl.use_bulk = 0;
-  alignas(64) CUtensorMap tmx, tmd;
-  memset(&tmx, 0, sizeof(tmx));
-  memset(&tmd, 0, sizeof(tmd));
   pl.use_tma = encode_plane_map(&tmx, x, desc, pl.xs[0].stride, pl.xbf / pl.xs[0].stride, pl.P) &&
                encode_plane_map(&tmd, dy, desc, pl.ds[0].stride, pl.dbf / pl.ds[0].stride, pl.P);
   cudaError_t e = wt::launch_bwd_weight(pl, tmx, tmd, desc->dtype, x, dy, w_base, b_base, w_sub, base_scale,
@@ -813,7 +1033,7 @@ const char* wtconv_last_error(void) { return g_last_error; }
 
 unsigned int wtconv_device_faults(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return 0;
-  return wt::take_fwd_faults() + wt::take_win_faults() + wt::take_bw_faults();
+  return wt::take_fwd_faults() + wt::take_win_faults() + wt::take_bw_faults() + wt::take_bww_faults();
 }
 
 }  // extern "C"

@@ -404,6 +404,13 @@ cudaError_t launch_bwd_weight(const WtBwPlan& pl, const CUtensorMap& tmx, const 
   else if (dtype == 1) e = launch_bw_k<__half>(pl, tmx, tmd, x, dy, part, stream);
   else e = launch_bw_k<__nv_bfloat16>(pl, tmx, tmd, x, dy, part, stream);
   if (e != cudaSuccess) return e;
+  return launch_bw_finalize(pl, part, w_base, b_base, w_sub, s_base, s_w, dw_base, db_base, dw_sub, ds_base, ds_w,
+                            stream);
+}
+
+cudaError_t launch_bw_finalize(const WtBwPlan& pl, const float* part, const float* w_base, const float* b_base,
+                               const float* w_sub, const float* s_base, const float* s_w, float* dw_base,
+                               float* db_base, float* dw_sub, float* ds_base, float* ds_w, cudaStream_t stream) {
   const int warps = pl.C * pl.nbands;
   const int threads = 256;
   bw_finalize_kernel<<<(warps * 32 + threads - 1) / threads, threads, 0, stream>>>(

@@ -28,54 +28,6 @@ namespace wt {
 // Bounded waits that gave up; read by take_win_faults().
 static __device__ unsigned int g_win_faults;
 
-// Zero-filled load of np windows: buffer element (i, j), i < Hv, j < Wv, of
-// plane g is source element (oy + i, ox + j) of plane (n0 + g, c), or zero
-// outside the H x W plane.  vec: 16-byte items (W and ox multiples of the item
-// width, source 16-byte aligned), so an item lies wholly inside or wholly
-// outside the plane; B.pcol and B.stride are multiples of 4.
-template <typename T>
-__device__ __forceinline__ void load_window(float* dbase, int dps, const WtBuf B, const T* __restrict__ src,
-                                            int n0, int np, int c, int C, int H, int W, int oy, int ox, int Hv,
-                                            int Wv, bool vec, const WtDiv& dpp, const WtDiv& dw, int tid,
-                                            int nthreads) {
-  const size_t HW = (size_t)H * W;
-  if (vec) {
-    constexpr int V = Vec16<T>::N;
-    const int Wq = Wv / V;
-    const int per_plane = Hv * Wq;
-    for (int it = tid; it < np * per_plane; it += nthreads) {
-      const int g = fdiv(it, dpp);
-      const int rem = it - g * per_plane;
-      const int i = fdiv(rem, dw);
-      const int jq = rem - i * Wq;
-      const int gi = oy + i, gj = ox + jq * V;
-      float v[V];
-      if (gi >= 0 && gi < H && gj >= 0 && gj < W) {
-        ldg16<T>(src + ((size_t)(n0 + g) * C + c) * HW + (size_t)gi * W + gj, v);
-      } else {
-#pragma unroll
-        for (int e = 0; e < V; ++e) v[e] = 0.f;
-      }
-      float* d = dbase + g * dps + B.off + (i + B.prow) * B.stride + jq * V + B.pcol;
-#pragma unroll
-      for (int e = 0; e < V; e += 4) *reinterpret_cast<float4*>(d + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-    }
-  } else {
-    const int per_plane = Hv * Wv;
-    for (int it = tid; it < np * per_plane; it += nthreads) {
-      const int g = fdiv(it, dpp);
-      const int rem = it - g * per_plane;
-      const int i = fdiv(rem, dw);
-      const int j = rem - i * Wv;
-      const int gi = oy + i, gj = ox + j;
-      const float v = (gi >= 0 && gi < H && gj >= 0 && gj < W)
-                          ? to_f32(src[((size_t)(n0 + g) * C + c) * HW + (size_t)gi * W + gj])
-                          : 0.f;
-      dbase[g * dps + B.off + (i + B.prow) * B.stride + j + B.pcol] = v;
-    }
-  }
-}
-
 // Persistent: CTA b owns the units [b*U/G, (b+1)*U/G) of the unit list,
 // ordered by channel, then plane group, then tile (row-major), so
 // consecutive units usually share a channel and its folded weights.

@@ -24,6 +24,7 @@ cudaError_t launch_fwd_win(const WtFwdPlan& pl, const CUtensorMap& tmx, int dtyp
 // (reads and clears a device counter; synchronises the device).
 unsigned int take_fwd_faults();
 unsigned int take_win_faults();
+unsigned int take_bww_faults();
 unsigned int take_bw_faults();
 
 // Parameter gradients: correlation kernel into `part`, then the finalize kernel.
@@ -34,9 +35,24 @@ cudaError_t launch_bwd_weight(const WtBwPlan& pl, const CUtensorMap& tmx, const 
                               float* dw_sub, float* ds_base, float* ds_w, float* part,
                               cudaStream_t stream);
 
+// The finalize alone: adds each channel's records in CTA order and unfolds
+// the scales (shared by the whole-plane and the windowed gradient passes).
+cudaError_t launch_bw_finalize(const WtBwPlan& pl, const float* part, const float* w_base, const float* b_base,
+                               const float* w_sub, const float* s_base, const float* s_w, float* dw_base,
+                               float* db_base, float* dw_sub, float* ds_base, float* ds_w, cudaStream_t stream);
+
+// Parameter gradients for planes beyond one CTA, tile by tile with a halo on
+// x (pl.win = 1); tmx / tmd describe x and dy for the box copies.
+cudaError_t launch_bwd_weight_win(const WtBwPlan& pl, const CUtensorMap& tmx, const CUtensorMap& tmd, int dtype,
+                                  const void* x, const void* dy, const float* w_base, const float* b_base,
+                                  const float* w_sub, const float* s_base, const float* s_w, float* dw_base,
+                                  float* db_base, float* dw_sub, float* ds_base, float* ds_w, float* part,
+                                  cudaStream_t stream);
+
 // Resident parameter-gradient CTAs per SM for a plan, from the runtime's
 // occupancy calculator (0 when it cannot tell).
 int bw_ctas_per_sm(const WtBwPlan& pl, int dtype);
+int bw_win_ctas_per_sm(const WtBwPlan& pl, int dtype);
 
 // Sets the thread-local message returned by wtconv_last_error().
 void set_last_error(const char* msg);

@@ -139,6 +139,25 @@ struct WtBwPlan {
   WtDiv an_pp[WT_MAXL + 1], an_w[WT_MAXL + 1];
   WtDiv ipp;                                   // items per plane
   WtDiv tiles[WT_MAXL + 1], tcd[WT_MAXL + 1];  // tr*tc and tc per level
+  // Windowed mode, for planes beyond one CTA: a unit is one th x tw tile of
+  // P planes of one channel, and `batches` counts the units of a channel
+  // (plane groups x tiles).  x arrives as the tile's window (the tile plus
+  // `halo` pixels on every side, zero outside the plane) and dy as the tile
+  // alone: tiles start at multiples of 2^L, so the tile's dy coefficients
+  // depend on the tile only.  Hs/Ws and xs[] then describe the x window,
+  // dHs/dWs and ds[] the dy tile, tr/tc the correlation tiles over the tile.
+  int win;               // 1 = windowed mode
+  int halo;              // h: 2^L * r rounded up to 8
+  int th, tw;            // tile, multiples of max(2^L, 8)
+  int nty, ntx;          // tiles per plane
+  int groups;            // plane groups per channel: ceil(N / P)
+  int dHs[WT_MAXL + 1], dWs[WT_MAXL + 1];  // dy tile pyramid: th >> l, tw >> l
+  int zo[WT_MAXL + 1];   // h >> l: the tile's first level-l coefficient in the x window
+  int win_load;          // 0 = plain loads, 1 = float32 box copies, 2 = 16-bit box copies into the staging area
+  WtDiv dn_pp[WT_MAXL + 1], dn_w[WT_MAXL + 1];  // analysis of the dy tile (l = 2: the fused 1+2 pass)
+  WtDiv dld_pp, dld_w;   // plain loads of the dy tile: items per tile, per row
+  WtDiv dwd_pp, dwd_w;   // widening of the raw 16-bit dy tiles: items per tile, per row
+  int stage_dx;          // 16-bit staging: floats from the staging area's start to the raw dy tiles
 };
 
 #define WT_SMEM_SLACK 128  // bytes added to every dynamic shared-memory size for 128-byte realignment

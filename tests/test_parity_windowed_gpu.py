@@ -1,23 +1,24 @@
-"""GPU parity of the windowed forward / input-gradient pass (planes whose Haar
-pyramid does not fit one CTA) against the float64 oracle.
+"""GPU parity of the windowed passes (planes whose Haar pyramids do not fit
+one CTA) against the float64 oracle: forward, input gradient and every
+parameter gradient.
 
 Every shape below is larger than any whole plane the library keeps in one
-CTA (at most about 112 x 112 pixels), so the calls run tile by tile with a
-halo.  The cases span every window load (float32 box copies, 16-bit box
-copies widened on chip, plain loads for rows that are not whole 16-byte
-chunks or pointers that are not 16-byte aligned), ragged edge tiles, odd
-sizes padded at every level, each kernel size and levels 1 to 5.
-Tolerances are those of the whole-plane tests (relative L2 and elementwise
-against the largest oracle magnitude).
+CTA (at most about 112 x 112 pixels for the forward, 56 x 56 for the
+parameter gradient), so the calls run tile by tile with a halo.  The cases
+span every window load (float32 box copies, 16-bit box copies widened on
+chip, plain loads for rows that are not whole 16-byte chunks or pointers
+that are not 16-byte aligned), ragged edge tiles, odd sizes padded at every
+level, each kernel size and levels 1 to 5.  Tolerances are those of the
+whole-plane tests (relative L2 and elementwise against the largest oracle
+magnitude).
 """
 import numpy as np
 import pytest
 import torch
 
-import oracle
 from memory_bound_cnn_wtconv2d_gb300 import synth
 
-from test_parity_gpu import compare, to_dev, wt  # noqa: F401  (wt is a fixture)
+from test_parity_gpu import GRADS, check_all, to_dev, wt  # noqa: F401  (wt is a fixture)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,13 +30,6 @@ def fwd_and_dx(wt, inp, d):
     torch.cuda.synchronize()
     assert wt.wtconv_device_faults() == 0, "an in-kernel bounded wait gave up"
     return y.float().cpu().numpy(), dx.float().cpu().numpy()
-
-
-def check(wt, inp, d=None):
-    d = to_dev(inp) if d is None else d
-    y, dx = fwd_and_dx(wt, inp, d)
-    compare("y", y, oracle.fwd(inp), inp.dtype, False)
-    compare("dx", dx, oracle.bwd(inp)["dx"], inp.dtype, False)
 
 
 # (N, C, H, W, L, k, dtype): the window load each one takes is in the id
@@ -58,7 +52,16 @@ WINDOWED = [
 @pytest.mark.parametrize("case", WINDOWED, ids=lambda s: "x".join(map(str, s)))
 def test_windowed_matches_oracle(wt, case):
     N, C, H, W, L, k, dtype = case
-    check(wt, synth.make_inputs(N, C, H, W, L, k, dtype=dtype, seed=H * 7 + W + L + k))
+    check_all(wt, synth.make_inputs(N, C, H, W, L, k, dtype=dtype, seed=H * 7 + W + L + k))
+
+
+# Planes the forward still keeps whole but the parameter gradient does not
+# (57..112 pixels): whole-plane forward, windowed parameter gradient.
+@pytest.mark.parametrize("case", [(2, 3, 64, 64, 3, 5, "f32"), (1, 2, 57, 61, 2, 7, "f32"), (3, 2, 96, 80, 4, 3, "f16"),
+                                  (2, 2, 72, 72, 1, 9, "bf16")], ids=lambda s: "x".join(map(str, s)))
+def test_windowed_parameter_gradient_only(wt, case):
+    N, C, H, W, L, k, dtype = case
+    check_all(wt, synth.make_inputs(N, C, H, W, L, k, dtype=dtype, seed=H + W * 3 + L + k))
 
 
 def test_windowed_without_bias_and_unaligned_pointers(wt):
@@ -71,7 +74,7 @@ def test_windowed_without_bias_and_unaligned_pointers(wt):
         view.copy_(d[key])
         d[key] = view
     assert d["x"].data_ptr() % 16 != 0
-    check(wt, inp, d)
+    check_all(wt, inp, d)
 
 
 def test_windowed_matches_whole_plane_results_elementwise(wt):
@@ -94,16 +97,25 @@ def test_windowed_matches_whole_plane_results_elementwise(wt):
     assert np.abs(dx_big[:, :, :64, :64] - dx_small).max() <= 1e-5 * scale
 
 
-def test_windowed_full_size_sampled_planes(wt):
+def test_windowed_full_size(wt):
     # An ImageNet-stem-sized layer (N=8, C=64, 224 x 224, 3 levels, k=5,
-    # float32) in the launch configuration a user gets; samples 0 and 7 of
-    # every channel are checked against the oracle.
-    inp = synth.make_inputs(8, 64, 224, 224, 3, 5, seed=224)
+    # float32) in the launch configuration a user gets, every output and
+    # every parameter gradient against the oracle.
+    check_all(wt, synth.make_inputs(8, 64, 224, 224, 3, 5, seed=224))
+
+
+def test_windowed_parameter_gradient_is_deterministic_and_noalloc_agrees(wt):
+    inp = synth.make_inputs(2, 3, 200, 136, 3, 5, seed=21)
     d = to_dev(inp)
-    y, dx = fwd_and_dx(wt, inp, d)
-    sub = synth.LayerInputs(**{**inp.__dict__, "N": 2, "x": inp.x[[0, 7]], "dy": inp.dy[[0, 7]]})
-    compare("y", y[[0, 7]], oracle.fwd(sub), "f32", False)
-    compare("dx", dx[[0, 7]], oracle.bwd(sub)["dx"], "f32", False)
+    args = (d["x"], d["dy"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 3, 5)
+    g1 = wt.wtconv_bwd_weight(*args)
+    g2 = wt.wtconv_bwd_weight(*args)
+    g3 = wt.wtconv_bwd_weight_noalloc(*args)
+    torch.cuda.synchronize()
+    assert wt.wtconv_device_faults() == 0
+    for name in GRADS:
+        assert torch.equal(g1[name], g2[name]), name
+        assert torch.equal(g1[name], g3[name]), name
 
 
 def test_reach_beyond_one_cta_is_refused(wt):
@@ -112,8 +124,12 @@ def test_reach_beyond_one_cta_is_refused(wt):
     # nothing and leaves the context usable.
     inp = synth.make_inputs(1, 2, 224, 224, 5, 5, seed=3)
     d = to_dev(inp)
-    with pytest.raises(wt.WtconvError) as e:
-        wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 5, 5)
-    assert e.value.status == wt.WTCONV_ERR_UNSUPPORTED
-    inp = synth.make_inputs(1, 2, 224, 224, 4, 5, seed=3)
-    check(wt, inp)
+    for call in ("fwd", "bwd_weight"):
+        with pytest.raises(wt.WtconvError) as e:
+            if call == "fwd":
+                wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 5, 5)
+            else:
+                wt.wtconv_bwd_weight(d["x"], d["dy"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"],
+                                     d["wavelet_scale"], 5, 5)
+        assert e.value.status == wt.WTCONV_ERR_UNSUPPORTED
+    check_all(wt, synth.make_inputs(1, 2, 224, 224, 4, 5, seed=3))
