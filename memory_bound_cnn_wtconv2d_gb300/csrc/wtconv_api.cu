@@ -600,8 +600,13 @@ void bw_win_layout(WtBwPlan& pl, int P, int nsets, int load) {
 // input sets minimise the modelled time of the call, as in plan_win: phase
 // rounds of the 256 threads (both pyramids, then one or two correlation
 // items per thread) times the number of units, weighted by the CTAs that fit
-// an SM (shared memory; at most 2, which the registers of 256-thread CTAs
-// allow at k <= 5).
+// an SM by shared memory and by the kernel's registers.  The weights (4-row
+// correlation items at 0.6 of their FMA count, 1 / 2 / 3 CTAs per SM at
+// 1.6 / 1.0 / 0.8, one float32 input set at 0.9 of two) were fitted to a
+// sweep of forced tilings on a GB300 (224 x 224 planes at levels 1-4 and
+// k = 5, 7; 128, 384 and 512-pixel planes; float32 and float16), where the
+// model's choice came within 0.3 % of the fastest measured tiling on seven
+// of eight shapes and within 6.3 % on the eighth.
 wtconv_status_t plan_bw_win(const wtconv_desc_t* d, WtBwPlan& pl, int load) {
   memset(&pl, 0, sizeof(pl));
   pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
@@ -624,21 +629,24 @@ wtconv_status_t plan_bw_win(const wtconv_desc_t* d, WtBwPlan& pl, int load) {
       const int slots = (tbr == 8 ? 1 : WT_BW_MAX_ITEMS) * NT;
       const int n12x = L >= 2 ? pl.Hs[2] * pl.Ws[2] : pl.Hs[1] * pl.Ws[1];
       const int n12d = L >= 2 ? pl.dHs[2] * pl.dWs[2] : pl.dHs[1] * pl.dWs[1];
-      const long citem = 4L * tbr * KK + 200;
+      const long citem = (tbr == 8 ? 4L * tbr * KK : 12L * tbr * KK / 5) + 200;
+      const int regs = wt::bw_win_regs(d->k, tbr, d->dtype);
+      const long ctas_r = regs > 0 ? 65536L / (NT * (long)round_up(regs, 8)) : 3;
       for (int q = 1; q <= Pmax && q * pl.items_per_plane <= slots; ++q) {
         for (int ns = (load == 1 ? 2 : 1); ns >= 1; --ns) {
           bw_win_layout(pl, q, ns, load);
           if (pl.smem_bytes > kMaxSmemPerBlock) continue;
           long ctas = kSmemPerSm / (pl.smem_bytes + 1024);
-          if (ctas > 2) ctas = 2;
+          if (ctas > ctas_r) ctas = ctas_r;
+          if (ctas > 3) ctas = 3;
           long cost = ceil_div(q * n12x, NT) * c12 + ceil_div(q * n12d, NT) * c12 +
                       ceil_div(q * pl.items_per_plane, NT) * citem + cunit;
           for (int l = 3; l <= L; ++l)
             cost += (ceil_div(q * pl.Hs[l] * pl.Ws[l], NT) + ceil_div(q * pl.dHs[l] * pl.dWs[l], NT)) * c3;
           if (load == 0) cost += ceil_div(q * (pl.Hs[0] * pl.Ws[0] + th * tw) / 4, NT) * 60;
           const double units = (double)ceil_div(d->N > 0 ? d->N : 1, q) * ceil_div(d->H, th) * ceil_div(d->W, tw);
-          const double occ = ctas >= 2 ? 1.0 : 1.6;
-          const double one_set = (load == 1 && ns == 1) ? 1.05 : 1.0;
+          const double occ = ctas >= 3 ? 0.8 : ctas == 2 ? 1.0 : 1.6;
+          const double one_set = (load == 1 && ns == 1) ? 0.9 : 1.0;
           const double total = (double)cost * units * occ * one_set;
           if (best < 0 || total < best * (1 - 1e-9)) {
             best = total;

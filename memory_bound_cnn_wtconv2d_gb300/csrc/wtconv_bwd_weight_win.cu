@@ -20,6 +20,8 @@
 // Reformulation" (arXiv 2608.10805), technical summary, "Key contributions"
 // (every parameter gradient reproduced) and "Methodology" (scales folded into
 // the weights, unfolded in the finalize).  The tiling is this library's.
+#include <mutex>
+
 #include "wtconv_device.cuh"
 #include "wtconv_launch.h"
 
@@ -288,6 +290,27 @@ cudaError_t launch_bwd_weight_win(const WtBwPlan& pl, const CUtensorMap& tmx, co
   if (e != cudaSuccess) return e;
   return launch_bw_finalize(pl, part, w_base, b_base, w_sub, s_base, s_w, dw_base, db_base, dw_sub, ds_base, ds_w,
                             stream);
+}
+
+int bw_win_regs(int k, int tbr, int dtype) {
+  static std::mutex mu;
+  static int cache[4][2][3];  // k = 3, 5, 7, 9; tbr = 8, 4; dtype; 0 = not yet read
+  const int ki = (k - 3) / 2, ti = tbr == 8 ? 0 : 1;
+  if (ki < 0 || ki > 3 || dtype < 0 || dtype > 2) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[ki][ti][dtype] == 0) {
+    WtBwPlan q;
+    q.K = k;
+    q.tbr = tbr;
+    const void* f = bw_win_pick(q, dtype);
+    cudaFuncAttributes a;
+    if (!f || cudaFuncGetAttributes(&a, f) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[ki][ti][dtype] = a.numRegs;
+  }
+  return cache[ki][ti][dtype];
 }
 
 int bw_win_ctas_per_sm(const WtBwPlan& pl, int dtype) {

@@ -53,6 +53,9 @@ cudaError_t launch_bwd_weight_win(const WtBwPlan& pl, const CUtensorMap& tmx, co
 // occupancy calculator (0 when it cannot tell).
 int bw_ctas_per_sm(const WtBwPlan& pl, int dtype);
 int bw_win_ctas_per_sm(const WtBwPlan& pl, int dtype);
+// Registers per thread of the windowed gradient kernel for (k, tile rows,
+// dtype), read once from the runtime (0 when it cannot tell).
+int bw_win_regs(int k, int tbr, int dtype);
 
 // Sets the thread-local message returned by wtconv_last_error().
 void set_last_error(const char* msg);
