@@ -483,7 +483,8 @@ def run_suite(args):
         # layer, and the training step (all three calls) against the unfused
         # PyTorch composition with autograd and a cuDNN depthwise 7x7, forward
         # alone and forward + backward, on the same x.
-        for N, C, H, W, L, k, dtype in synth.LARGE_PLANES:
+        cases = synth.LARGE_PLANES if args.large_case is None else [synth.LARGE_PLANES[args.large_case]]
+        for N, C, H, W, L, k, dtype in cases:
             pin = synth.make_inputs(1, C, 1, 1, L, k, dtype=dtype, seed=5000 + C + L)
             ps = [torch.tensor(a, dtype=torch.float32, device=dev) for a in
                   (pin.w_base, pin.b_base, pin.w_sub, pin.base_scale, pin.wavelet_scale)]
@@ -807,6 +808,8 @@ def main(argv=None):
     ap.add_argument("--suite", choices=["sweep", "network", "configs", "large"], default=None,
                     help="time the shape/level sweep, the 18-layer network, every workload with the "
                          "oracle beside it, or the planes larger than one CTA, instead of the bench step")
+    ap.add_argument("--large-case", type=int, default=None,
+                    help="with --suite large: time only this entry of synth.LARGE_PLANES")
     ap.add_argument("--arm-only", default=None,
                     choices=["fused", "unfused", "dw7x7", "fused_infer", "unfused_infer", "dw7x7_infer"],
                     help="run only this arm's training step or forward (steps + warmup times, no JSON); "
