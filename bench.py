@@ -1,9 +1,12 @@
 """WTConv2d forward + backward benchmark on GB300.
 
-One step = one full training pass of one WTConv2d layer: wtconv_fwd,
-wtconv_bwd_data and wtconv_bwd_weight through the C ABI, on the WTConvNeXt-T
-stage-1 layer shape x[64,96,56,56] float32, L=3, k=5 (synthetic seeded
-inputs and random-init weights).  Prints one JSON line.
+One step = one full training pass of one WTConv2d layer through the C ABI:
+wtconv_fwd, then wtconv_bwd (the input gradient and every parameter gradient
+in one call, one fused kernel over x and dy), on the WTConvNeXt-T stage-1
+layer shape x[64,96,56,56] float32, L=3, k=5 (synthetic seeded inputs and
+random-init weights).  The same backward as the two separate calls
+(wtconv_bwd_data + wtconv_bwd_weight) is timed beside it for context.
+Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -627,10 +630,13 @@ def run_ours(args, world, rank, local):
     grads = dict(dw_base=torch.empty_like(wb), db_base=torch.empty_like(bb), dw_sub=torch.empty_like(wsub),
                  dbase_scale=torch.empty_like(sb), dwavelet_scale=torch.empty_like(sw))
     desc = wtconv.desc_for(x0, L, k)
-    ws = torch.empty(max(wtconv.wtconv_workspace_size(desc, wtconv.OP_BWD_WEIGHT), 256), dtype=torch.uint8,
+    ws = torch.empty(max(wtconv.wtconv_workspace_size(desc, wtconv.OP_BWD),
+                         wtconv.wtconv_workspace_size(desc, wtconv.OP_BWD_WEIGHT), 256), dtype=torch.uint8,
                      device=dev)
-    launches_per_step = 4  # fwd, bwd_data, bwd_weight correlation + its finalize
+    launches_per_step = 3  # fwd, the fused backward kernel + its dW finalize
 
+    # One step: the forward, then the whole backward in one call (the fused
+    # backward kernel: dx and every parameter gradient from one read of x, dy).
     def step(i, ev=None):
         x, dy_ = xs[i % ROTATE], dys[i % ROTATE]
         if ev is not None:
@@ -638,18 +644,25 @@ def run_ours(args, world, rank, local):
         wtconv.wtconv_fwd(x, wb, bb, wsub, sb, sw, L, k, y=y, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        wtconv.wtconv_bwd_data(dy_, wb, wsub, sb, sw, L, k, dx=dx, stream=stream)
+        wtconv.wtconv_bwd(x, dy_, wb, bb, wsub, sb, sw, L, k, dx=dx, grads=grads, workspace=ws, stream=stream)
         if ev is not None:
             ev[2].record(stream)
+
+    # The same backward as the two separate calls, timed after the step (not
+    # part of the value): context for the fused call.
+    def step_separate(i, ev):
+        x, dy_ = xs[i % ROTATE], dys[i % ROTATE]
+        ev[0].record(stream)
+        wtconv.wtconv_bwd_data(dy_, wb, wsub, sb, sw, L, k, dx=dx, stream=stream)
+        ev[1].record(stream)
         wtconv.wtconv_bwd_weight(x, dy_, wb, bb, wsub, sb, sw, L, k, grads=grads, workspace=ws, stream=stream)
-        if ev is not None:
-            ev[3].record(stream)
+        ev[2].record(stream)
 
     warmup = max(args.warmup, 3)
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
@@ -663,12 +676,17 @@ def run_ours(args, world, rank, local):
         barrier(world)
     elapsed_ms = start.elapsed_time(end)
     elapsed_ms = max_over_ranks(world, elapsed_ms, dev)
-    per = {"fwd": [], "bwd_data": [], "bwd_weight": []}
+    per = {"fwd": [], "bwd": []}
     for e in evs:
         per["fwd"].append(e[0].elapsed_time(e[1]))
-        per["bwd_data"].append(e[1].elapsed_time(e[2]))
-        per["bwd_weight"].append(e[2].elapsed_time(e[3]))
+        per["bwd"].append(e[1].elapsed_time(e[2]))
     avg = {kname: sum(v) / len(v) for kname, v in per.items()}
+    sep_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step_separate(i, sep_ev[i])
+    torch.cuda.synchronize()
+    separate = {"bwd_data": sum(e[0].elapsed_time(e[1]) for e in sep_ev) / args.steps,
+                "bwd_weight": sum(e[1].elapsed_time(e[2]) for e in sep_ev) / args.steps}
 
     # End to end through the public API with host buffers (pinned): every step
     # copies its inputs in, runs the three calls and copies y, dx and the
@@ -705,9 +723,8 @@ def run_ours(args, world, rank, local):
                 if i >= 2:
                     stream.wait_event(ev_out[i - 2])  # step i-2's results have left output set b
                 wtconv.wtconv_fwd(xs[b], wb, bb, wsub, sb, sw, L, k, y=yd[b], stream=stream)
-                wtconv.wtconv_bwd_data(dys[b], wb, wsub, sb, sw, L, k, dx=dxd[b], stream=stream)
-                wtconv.wtconv_bwd_weight(xs[b], dys[b], wb, bb, wsub, sb, sw, L, k, grads=gd[b], workspace=ws,
-                                         stream=stream)
+                wtconv.wtconv_bwd(xs[b], dys[b], wb, bb, wsub, sb, sw, L, k, dx=dxd[b], grads=gd[b], workspace=ws,
+                                  stream=stream)
                 ev_cp[i].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_cp[i])
@@ -739,20 +756,25 @@ def run_ours(args, world, rank, local):
     peaks, peak_kind = measured_peaks()
     e = ESIZE[inp.dtype]
     ne = inp.numel
-    alg_bytes = {"fwd": 2 * ne * e, "bwd_data": 2 * ne * e, "bwd_weight": 2 * ne * e}
-    fma = fma_per_plane(inp.H, inp.W, L, k) * inp.N * inp.C
+    # algorithmic bytes: fwd reads x, writes y; the fused backward reads x and
+    # dy once and writes dx (5 element transfers per element per step)
+    alg_bytes = {"fwd": 2 * ne * e, "bwd": 3 * ne * e}
+    fma = fma_per_plane(inp.H, inp.W, L, k) * inp.N * inp.C  # one pass: fwd, dx, or the dW correlations
+    fma_kernel = {"fwd": fma, "bwd": 2 * fma}
     ms_step = elapsed_ms / args.steps
     step_bytes = sum(alg_bytes.values())
     hbm_tbs = step_bytes / (ms_step * 1e-3) / 1e12
     dom = max(avg, key=avg.get)
     clocks = clk.summary()
     alu_peak = NUM_SMS * FP32_LANES * 2 * SM_MAX_MHZ * 1e6 / 1e12  # TFLOP/s at the maximum SM clock
-    achieved_alu = 2 * fma / (avg[dom] * 1e-3) / 1e12
+    achieved_alu = 2 * fma_kernel[dom] / (avg[dom] * 1e-3) / 1e12
     roofline = {"bound": "alu", "kernel": dom, "achieved": round(achieved_alu, 2), "peak": round(alu_peak, 2),
                 "unit": "TFLOP/s", "frac": round(achieved_alu / alu_peak, 4), "traffic": measured_traffic(dom),
                 "traffic_unit": "bytes per launch (ncu dram read+write)",
                 "peak_source": f"{NUM_SMS} SMs x {FP32_LANES} FP32 FMA/clk x 2 x {SM_MAX_MHZ:.0f} MHz",
-                "algorithmic_fma_per_launch": fma}
+                "algorithmic_fma_per_launch": fma_kernel[dom],
+                "timed_span": "bwd = the fused backward kernel and its dW finalize (one C call)" if dom == "bwd"
+                else "the forward kernel"}
     hbm = {"achieved_step_tbs": round(hbm_tbs, 3), "peak_gbs": peaks.get("hbm_gbs"), "peak_kind": peak_kind,
            "frac_of_measured": round(hbm_tbs * 1e3 / peaks["hbm_gbs"], 4), "frac_of_8tbs": round(hbm_tbs / 8.0, 4),
            "algorithmic_bytes_per_step": step_bytes,
@@ -765,6 +787,8 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded N(0,1) activations, random-init weights)",
         "config": workload_config(inp) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kernel_ms": {kn: round(v, 4) for kn, v in avg.items()},
+        "separate_bwd_ms": {kn: round(v, 4) for kn, v in separate.items()} | {
+            "note": "the backward as wtconv_bwd_data + wtconv_bwd_weight, timed after the step; not in the value"},
         "roofline": roofline, "hbm": hbm, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "e2e": e2e,
     }

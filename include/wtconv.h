@@ -79,7 +79,8 @@ typedef enum { WTCONV_F32 = 0, WTCONV_F16 = 1, WTCONV_BF16 = 2 } wtconv_dtype_t;
 typedef enum {
   WTCONV_OP_FWD = 0,
   WTCONV_OP_BWD_DATA = 1,
-  WTCONV_OP_BWD_WEIGHT = 2
+  WTCONV_OP_BWD_WEIGHT = 2,
+  WTCONV_OP_BWD = 3  /* wtconv_bwd: input and parameter gradients in one call */
 } wtconv_op_t;
 
 /* Layer geometry.  All fields are plain ints so the layout is fixed. */
@@ -128,6 +129,23 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
                                   const float* base_scale, const float* wavelet_scale,
                                   float* dw_base, float* db_base, float* dw_sub, float* dbase_scale,
                                   float* dwavelet_scale, void* ws, size_t ws_bytes, void* stream);
+
+/* The whole backward in one call: dx (as wtconv_bwd_data) and every parameter
+ * gradient (as wtconv_bwd_weight, same arguments and conventions), computed
+ * by one kernel that reads x and dy once and builds the Haar pyramid of dy
+ * once for both (3 element transfers per element instead of 4).  The
+ * summary's "Key contributions" report that the fused implementation
+ * reproduces all gradients; merging the two backward passes is this
+ * library's.  Results match the two separate calls up to floating-point
+ * evaluation order; the parameter gradients are deterministic.  The
+ * workspace must hold wtconv_workspace_size(desc, WTCONV_OP_BWD) bytes
+ * (256-byte aligned).  Planes whose fused working set does not fit one CTA
+ * (beyond 56 x 56, depending on k and levels) run the two separate passes
+ * inside this call.  Errors as for the two calls. */
+wtconv_status_t wtconv_bwd(const wtconv_desc_t* desc, const void* x, const void* dy, const float* w_base,
+                           const float* b_base, const float* w_sub, const float* base_scale,
+                           const float* wavelet_scale, void* dx, float* dw_base, float* db_base, float* dw_sub,
+                           float* dbase_scale, float* dwavelet_scale, void* ws, size_t ws_bytes, void* stream);
 
 /* Parameter gradients without a workspace argument, for callers that cannot
  * allocate device memory themselves (for example a plugin inside a host

@@ -516,6 +516,105 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
   return bw_grid(d, pl, per_sm);
 }
 
+// Plan of the fused backward (input gradient and parameter gradients in one
+// kernel, planes that fit one CTA): the parameter-gradient plan's tiles,
+// items and units, with the dy buffers widened for the input-gradient
+// phases (an r-row, 4-column zero margin around the dy plane and every dy
+// band, so the band convolutions and the base convolution read their halo
+// from it), plus the input gradient's Z buffers and rotated folded weights.
+// Shared memory: [input sets: P x planes, P dy planes][work area: P x (x
+// pyramid, dy pyramid, Z buffers), or the end-of-channel reduction][weights]
+// [mbarriers].  Two input sets and two CTAs per SM are preferred, then one
+// set, then fewer planes per unit.
+wtconv_status_t plan_bwf(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan& fp) {
+  const wtconv_status_t st = plan_bw(d, pl);  // fails for planes beyond one CTA
+  if (st != WTCONV_OK) return st;
+  if (pl.tbr != 8)
+    return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d takes 4-row gradient tiles: no fused backward kernel",
+                d->H, d->W);
+  const int R = d->k / 2, L = d->levels, KK = d->k * d->k;
+  memset(&fp, 0, sizeof(fp));
+  fp.N = d->N; fp.C = d->C; fp.H = d->H; fp.W = d->W; fp.L = L; fp.K = d->k;
+  for (int l = 0; l <= L; ++l) {
+    fp.Hs[l] = pl.Hs[l];
+    fp.Ws[l] = pl.Ws[l];
+  }
+  // Half-height final tiles: with 256 threads and planes of at most 64 x 64,
+  // they never take more rounds than full-height ones and each is cheaper.
+  const int tp = WT_TP / 2;
+  fp.ftp = tp;
+  fp.ftr = ceil_div(pl.Hs[1], tp);
+  fp.ftc = ceil_div(pl.Ws[1], WT_TQ);
+  const int rows0 = std::max(pl.tbr * pl.tr[0], 2 * tp * fp.ftr);
+  const int cols0 = std::max(4 * pl.tc[0], 2 * WT_TQ * fp.ftc);
+  pl.xbf = place(pl.xs[0], 0, pl.tbr * pl.tr[0], 4 * pl.tc[0], R, 4, 1);
+  pl.dbf = place(pl.ds[0], 0, rows0, cols0, R, 4, 1, cols0 + 8);
+  int off = 0;
+  fp.zbegin[1] = 0;
+  for (int l = 1; l <= L; ++l) {
+    fp.ztr[l] = ceil_div(pl.Hs[l], WT_ZT);
+    fp.ztc[l] = ceil_div(pl.Ws[l], WT_ZT);
+    off = place(pl.xs[l], off, pl.tbr * pl.tr[l], 4 * pl.tc[l], R, R, 4);
+    off = place(pl.ds[l], off, std::max(pl.tbr * pl.tr[l], WT_ZT * fp.ztr[l]),
+                std::max(4 * pl.tc[l], WT_ZT * fp.ztc[l]), R, 4, 4);
+    fp.zbegin[l + 1] = fp.zbegin[l] + 4 * fp.ztr[l] * fp.ztc[l];
+  }
+  fp.zipp = fp.zbegin[L + 1];
+  for (int l = 1; l <= L; ++l) {
+    // Z^l: written at p < H_l, q < W_l; read by the final tiles at
+    // (p >> (l-1), q >> (l-1)) for every level-1 position of the tile grid.
+    const int fr = ((tp * fp.ftr - 1) >> (l - 1)) + 1, fc = ((WT_TQ * fp.ftc - 1) >> (l - 1)) + 1;
+    off = place(fp.zb[l], off, std::max(pl.Hs[l], fr), std::max(pl.Ws[l], fc), 0, 0, 4);
+  }
+  pl.wf = fp.wf = round_up(off, 4);
+  for (int l = 0; l <= L; ++l) fp.lev[l] = pl.ds[l];
+  fp.xf = pl.dbf;
+  fp.w_band = round_up(KK, 4);
+  const int wfloats = (1 + 4 * L) * fp.w_band;
+  // 16-bit planes that are whole 8-byte chunks get a staging area for their
+  // raw planes, and one input set (used when the tensors are aligned enough).
+  const bool staging = d->dtype != WTCONV_F32 && (2L * d->H * d->W) % 8 == 0;
+  auto layout = [&](int P, int nsets) {
+    pl.P = P;
+    pl.nsets = nsets;
+    pl.xr = round_up(P * pl.xbf, 32);
+    pl.islot = pl.xr + round_up(P * pl.dbf, 32);
+    pl.stage_off = nsets * pl.islot;
+    pl.work_off = pl.stage_off + (staging ? round_up(P * d->H * d->W, 32) : 0);
+    long region = (long)P * pl.wf;
+    const long red = (long)P * pl.items_per_plane * (KK + 1);
+    if (red > region) region = red;
+    pl.red_floats = (int)((region + 3) / 4 * 4);
+    fp.w_off = pl.work_off + pl.red_floats;
+    pl.mb_off = round_up(fp.w_off + wfloats, 2);
+    const long smem = 4L * pl.mb_off + 16 + WT_SMEM_SLACK;
+    pl.smem_bytes = smem > INT32_MAX ? INT32_MAX : (int)smem;
+    pl.tma_bytes = (uint32_t)(4L * P * (pl.xbf + pl.dbf));
+  };
+  const long two_per_sm = kSmemPerSm / 2 - 1024 - kStaticSmem;
+  bool found = false;
+  for (int q = pl.P; q >= 1 && !found; --q)
+    for (int ns = staging ? 1 : 2; ns >= 1 && !found; --ns) {
+      layout(q, ns);
+      found = pl.smem_bytes <= two_per_sm;
+    }
+  if (!found) {
+    layout(1, 1);
+    if (pl.smem_bytes > kMaxSmemPerBlock)
+      return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %d B of shared memory for the fused "
+                  "backward (max %d)", d->H, d->W, L, pl.smem_bytes, kMaxSmemPerBlock);
+  }
+  fp.P = pl.P;
+  fwd_divs(fp);
+  pl.batches = d->N > 0 ? ceil_div(d->N, pl.P) : 0;
+  int per_sm = wt::bwf_ctas_per_sm(pl, fp, d->dtype);
+  if (per_sm <= 0) {
+    per_sm = (int)(kSmemPerSm / (pl.smem_bytes + 1024));
+    if (per_sm > 2) per_sm = 2;
+  }
+  return bw_grid(d, pl, per_sm < 1 ? 1 : per_sm);
+}
+
 // Windowed parameter-gradient geometry for th x tw tiles and tbr-row
 // correlation tiles; pl.halo set.  x window: (th + 2h) x (tw + 2h) pixels
 // with r zero rows above and below and a 4-float margin left and right (the
@@ -864,6 +963,14 @@ extern "C" {
 
 size_t wtconv_workspace_size(const wtconv_desc_t* desc, int op) {
   if (validate_desc(desc) != WTCONV_OK) return 0;
+  if (op == WTCONV_OP_BWD) {
+    WtBwPlan pl;
+    WtFwdPlan fp;
+    const wtconv_status_t st = plan_bwf(desc, pl, fp);
+    if (st == WTCONV_OK) return bw_workspace_bytes(pl);
+    if (st != WTCONV_ERR_UNSUPPORTED) return 0;
+    op = WTCONV_OP_BWD_WEIGHT;  // the call runs the two separate passes
+  }
   if (op != WTCONV_OP_BWD_WEIGHT) return 0;
   WtBwPlan pl;
   const wtconv_status_t st = plan_bw(desc, pl);
@@ -946,6 +1053,56 @@ wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const
                        (cudaStream_t)stream);
   }
   if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_data: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+wtconv_status_t wtconv_bwd(const wtconv_desc_t* desc, const void* x, const void* dy, const float* w_base,
+                           const float* b_base, const float* w_sub, const float* base_scale,
+                           const float* wavelet_scale, void* dx, float* dw_base, float* db_base, float* dw_sub,
+                           float* dbase_scale, float* dwavelet_scale, void* ws, size_t ws_bytes, void* stream) {
+  WT_TRY(validate_desc(desc));
+  WT_TRY(check_param(w_base, "w_base", false));
+  WT_TRY(check_param(b_base, "b_base", true));
+  WT_TRY(check_param(w_sub, "w_sub", false));
+  WT_TRY(check_param(base_scale, "base_scale", false));
+  WT_TRY(check_param(wavelet_scale, "wavelet_scale", false));
+  WT_TRY(check_param(dw_base, "dw_base", false));
+  WT_TRY(check_param(db_base, "db_base", true));
+  WT_TRY(check_param(dw_sub, "dw_sub", false));
+  WT_TRY(check_param(dbase_scale, "dbase_scale", false));
+  WT_TRY(check_param(dwavelet_scale, "dwavelet_scale", false));
+  WtBwPlan pl;
+  WtFwdPlan fp;
+  const wtconv_status_t st = plan_bwf(desc, pl, fp);
+  if (st == WTCONV_ERR_UNSUPPORTED || desc->N == 0) {
+    // Planes beyond the fused kernel's working set (or an empty batch): the
+    // two separate passes, with the same results.
+    WT_TRY(wtconv_bwd_data(desc, dy, w_base, w_sub, base_scale, wavelet_scale, dx, nullptr, 0, stream));
+    return wtconv_bwd_weight(desc, x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, dw_base, db_base,
+                             dw_sub, dbase_scale, dwavelet_scale, ws, ws_bytes, stream);
+  }
+  if (st != WTCONV_OK) return st;
+  WT_TRY(check_act(x, "x", desc));
+  WT_TRY(check_act(dy, "dy", desc));
+  WT_TRY(check_act(dx, "dx", desc));
+  const size_t need = bw_workspace_bytes(pl);
+  if (!ws || ws_bytes < need)
+    return fail(WTCONV_ERR_WORKSPACE, "workspace of %zu B given, %zu B needed", ws ? ws_bytes : 0, need);
+  if (!aligned(ws, 256)) return fail(WTCONV_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+  set_load_divs(pl, desc, vec_ok(desc, x, dy));
+  fp.vec_ok = vec_ok(desc, dx, nullptr);
+  set_bulk(pl, desc, x, pl.work_off > pl.stage_off ? 4L * (pl.work_off - pl.stage_off) / 2 : 0);
+  if (pl.use_bulk == 1 && !(aligned(dy, 16) && 2L * pl.P * pl.bulk_bytes < (1L << 20))) pl.use_bulk = 2;
+  if (pl.use_bulk == 2 && !aligned(dy, 8)) pl.use_bulk = 0;
+  alignas(64) CUtensorMap tmx, tmd;
+  memset(&tmx, 0, sizeof(tmx));
+  memset(&tmd, 0, sizeof(tmd));
+  pl.use_tma = encode_plane_map(&tmx, x, desc, pl.xs[0].stride, pl.xbf / pl.xs[0].stride, pl.P) &&
+               encode_plane_map(&tmd, dy, desc, pl.ds[0].stride, pl.dbf / pl.ds[0].stride, pl.P);
+  cudaError_t e = wt::launch_bwd_fused(pl, fp, tmx, tmd, desc->dtype, x, dy, w_base, b_base, w_sub, base_scale,
+                                       wavelet_scale, dx, dw_base, db_base, dw_sub, dbase_scale, dwavelet_scale,
+                                       static_cast<float*>(ws), (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd: %s", cudaGetErrorString(e));
   return ok();
 }
 
@@ -1041,7 +1198,8 @@ const char* wtconv_last_error(void) { return g_last_error; }
 
 unsigned int wtconv_device_faults(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return 0;
-  return wt::take_fwd_faults() + wt::take_win_faults() + wt::take_bw_faults() + wt::take_bww_faults();
+  return wt::take_fwd_faults() + wt::take_win_faults() + wt::take_bw_faults() + wt::take_bww_faults() +
+         wt::take_bwf_faults();
 }
 
 }  // extern "C"

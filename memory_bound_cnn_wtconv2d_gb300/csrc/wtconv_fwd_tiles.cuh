@@ -58,14 +58,13 @@ __device__ __forceinline__ void stage_weights(float* wsm, int wb, int L, int C, 
 // xo = gi0 = gj0 = 0 and (Hg, Wg) = (H, W).  Windows: the grid covers the
 // output tile, whose first pixel is input-buffer element (xo, xo) and output
 // element (gi0, gj0) of an Hg x Wg plane; Z buffers hold the tile's
-// coefficients only.
-template <int K, typename T, int TP>
+// coefficients only.  NT threads share the tiles.
+template <int K, typename T, int TP, int NT = WT_FWD_THREADS>
 __device__ __forceinline__ void final_tiles(const WtFwdPlan& pl, const float* work, const float* xs, const float* wsm,
                                             float bias, T* __restrict__ y, int n0, int c, int np, int tid,
                                             int xo, int gi0, int gj0, int Hg, int Wg) {
   constexpr int R = K / 2;
   constexpr int TQ = WT_TQ;
-  constexpr int NT = WT_FWD_THREADS;
   const int XF = pl.xf, WF = pl.wf;
   const WtBuf X = pl.lev[0];
   const int L = pl.L, C = pl.C;

@@ -25,6 +25,7 @@ cudaError_t launch_fwd_win(const WtFwdPlan& pl, const CUtensorMap& tmx, int dtyp
 unsigned int take_fwd_faults();
 unsigned int take_win_faults();
 unsigned int take_bww_faults();
+unsigned int take_bwf_faults();
 unsigned int take_bw_faults();
 
 // Parameter gradients: correlation kernel into `part`, then the finalize kernel.
@@ -48,6 +49,15 @@ cudaError_t launch_bwd_weight_win(const WtBwPlan& pl, const CUtensorMap& tmx, co
                                   const float* w_sub, const float* s_base, const float* s_w, float* dw_base,
                                   float* db_base, float* dw_sub, float* ds_base, float* ds_w, float* part,
                                   cudaStream_t stream);
+
+// Fused backward: input gradient (into dx) and parameter gradients (records
+// into `part`, then the finalize) from one kernel over x and dy.
+cudaError_t launch_bwd_fused(const WtBwPlan& pl, const WtFwdPlan& fp, const CUtensorMap& tmx, const CUtensorMap& tmd,
+                             int dtype, const void* x, const void* dy, const float* w_base, const float* b_base,
+                             const float* w_sub, const float* s_base, const float* s_w, void* dx, float* dw_base,
+                             float* db_base, float* dw_sub, float* ds_base, float* ds_w, float* part,
+                             cudaStream_t stream);
+int bwf_ctas_per_sm(const WtBwPlan& pl, const WtFwdPlan& fp, int dtype);
 
 // Resident parameter-gradient CTAs per SM for a plan, from the runtime's
 // occupancy calculator (0 when it cannot tell).

@@ -25,9 +25,18 @@ class WTConv2dFunction(torch.autograd.Function):
     def backward(ctx, dy):
         x, w_base, b_base, w_sub, base_scale, wavelet_scale = ctx.saved_tensors
         dy = dy.contiguous().to(x.dtype)
-        dx = _c.wtconv_bwd_data(dy, w_base, w_sub, base_scale, wavelet_scale, ctx.levels, ctx.k)
-        g = _c.wtconv_bwd_weight(x, dy, w_base, b_base if ctx.has_bias else None, w_sub, base_scale,
-                                 wavelet_scale, ctx.levels, ctx.k)
+        b = b_base if ctx.has_bias else None
+        need_dx = ctx.needs_input_grad[0]
+        need_params = any(ctx.needs_input_grad[1:6])
+        dx, g = None, None
+        if need_dx and need_params:  # one call: the fused backward
+            dx, g = _c.wtconv_bwd(x, dy, w_base, b, w_sub, base_scale, wavelet_scale, ctx.levels, ctx.k)
+        elif need_dx:
+            dx = _c.wtconv_bwd_data(dy, w_base, w_sub, base_scale, wavelet_scale, ctx.levels, ctx.k)
+        elif need_params:
+            g = _c.wtconv_bwd_weight(x, dy, w_base, b, w_sub, base_scale, wavelet_scale, ctx.levels, ctx.k)
+        if g is None:
+            return (dx, None, None, None, None, None, None, None)
         return (dx, g["dw_base"], g["db_base"], g["dw_sub"], g["dbase_scale"], g["dwavelet_scale"],
                 None, None)
 

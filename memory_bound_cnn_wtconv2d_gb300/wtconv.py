@@ -19,11 +19,11 @@ LIB_PATH = os.path.join(_HERE, "libwtconv.so")
 
 WTCONV_OK, WTCONV_ERR_INVALID_ARG, WTCONV_ERR_UNSUPPORTED = 0, 1, 2
 WTCONV_ERR_MISALIGNED, WTCONV_ERR_WORKSPACE, WTCONV_ERR_CUDA = 3, 4, 5
-OP_FWD, OP_BWD_DATA, OP_BWD_WEIGHT = 0, 1, 2
+OP_FWD, OP_BWD_DATA, OP_BWD_WEIGHT, OP_BWD = 0, 1, 2, 3
 DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 # entry points declared in include/wtconv.h
-EXPORTS = ("wtconv_workspace_size", "wtconv_fwd", "wtconv_bwd_data", "wtconv_bwd_weight",
+EXPORTS = ("wtconv_workspace_size", "wtconv_fwd", "wtconv_bwd_data", "wtconv_bwd_weight", "wtconv_bwd",
            "wtconv_bwd_weight_noalloc", "wtconv_status_string", "wtconv_last_error",
            "wtconv_device_faults")
 
@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.wtconv_bwd_data.restype = ctypes.c_int
         L.wtconv_bwd_weight.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.wtconv_bwd_weight.restype = ctypes.c_int
+        L.wtconv_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.wtconv_bwd.restype = ctypes.c_int
         L.wtconv_bwd_weight_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.wtconv_bwd_weight_noalloc.restype = ctypes.c_int
         L.wtconv_status_string.argtypes = [ctypes.c_int]
@@ -167,6 +169,32 @@ def wtconv_bwd_weight(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, l
         _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
         _ptr(grads["dwavelet_scale"]), _ptr(workspace), workspace.numel(), _stream(stream)))
     return grads
+
+
+def wtconv_bwd(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k,
+               dx=None, grads=None, workspace=None, stream=None):
+    """The whole backward in one call (one kernel over x and dy where the planes
+    fit): returns (dx, grads) with grads as from wtconv_bwd_weight."""
+    _act(x, "x")
+    _act(dy, "dy")
+    desc = desc_for(x, levels, k)
+    dev = x.device
+    dx = torch.empty_like(dy) if dx is None else _act(dx, "dx")
+    if grads is None:
+        grads = dict(dw_base=torch.empty_like(w_base),
+                     db_base=None if b_base is None else torch.empty_like(b_base),
+                     dw_sub=torch.empty_like(w_sub), dbase_scale=torch.empty_like(base_scale),
+                     dwavelet_scale=torch.empty_like(wavelet_scale))
+    need = wtconv_workspace_size(desc, OP_BWD)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check(lib().wtconv_bwd(
+        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(_param(w_base, "w_base")),
+        _ptr(_param(b_base, "b_base", True)), _ptr(_param(w_sub, "w_sub")),
+        _ptr(_param(base_scale, "base_scale")), _ptr(_param(wavelet_scale, "wavelet_scale")), _ptr(dx),
+        _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
+        _ptr(grads["dwavelet_scale"]), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dx, grads
 
 
 def wtconv_bwd_weight_noalloc(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k,
