@@ -421,8 +421,7 @@ def run_suite(args):
     def fused_step(x, dy, ps, L, k, out):
         def run():
             wtconv.wtconv_fwd(x, *ps, L, k, y=out["y"])
-            wtconv.wtconv_bwd_data(dy, ps[0], ps[2], ps[3], ps[4], L, k, dx=out["dx"])
-            wtconv.wtconv_bwd_weight(x, dy, *ps, L, k, grads=out["g"], workspace=out["ws"])
+            wtconv.wtconv_bwd(x, dy, *ps, L, k, dx=out["dx"], grads=out["g"], workspace=out["ws"])
         return run
 
     def buffers(x, ps, L, k):
@@ -431,7 +430,8 @@ def run_suite(args):
                 "g": dict(dw_base=torch.empty_like(ps[0]), db_base=torch.empty_like(ps[1]),
                           dw_sub=torch.empty_like(ps[2]), dbase_scale=torch.empty_like(ps[3]),
                           dwavelet_scale=torch.empty_like(ps[4])),
-                "ws": torch.empty(max(wtconv.wtconv_workspace_size(desc, wtconv.OP_BWD_WEIGHT), 256),
+                "ws": torch.empty(max(wtconv.wtconv_workspace_size(desc, wtconv.OP_BWD),
+                                      wtconv.wtconv_workspace_size(desc, wtconv.OP_BWD_WEIGHT), 256),
                                   dtype=torch.uint8, device=dev)}
 
     rows = []
@@ -482,7 +482,8 @@ def run_suite(args):
         line = {"suite": "configs", "metric": "fwd+bwd ms per layer; oracle seconds per layer", "rows": rows}
     elif args.suite == "large":
         # Planes beyond one CTA (tiled with a halo): each call of the fused
-        # layer, and the training step (all three calls) against the unfused
+        # layer, and the training step (wtconv_fwd + wtconv_bwd, which runs the
+        # two windowed backward passes for such planes) against the unfused
         # PyTorch composition with autograd and a cuDNN depthwise 7x7, forward
         # alone and forward + backward, on the same x.
         cases = synth.LARGE_PLANES if args.large_case is None else [synth.LARGE_PLANES[args.large_case]]
