@@ -525,10 +525,13 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
 // Shared memory: [input sets: P x planes, P dy planes][work area: P x (x
 // pyramid, dy pyramid, Z buffers), or the end-of-channel reduction][weights]
 // [mbarriers].  Two input sets and two CTAs per SM are preferred, then one
-// set, then fewer planes per unit.
+// set, then fewer planes per unit; layers that cannot keep two CTAs per SM
+// are refused (the caller then runs the two separate passes).
 wtconv_status_t plan_bwf(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan& fp) {
   const wtconv_status_t st = plan_bw(d, pl);  // fails for planes beyond one CTA
   if (st != WTCONV_OK) return st;
+  // 4-row correlation tiles (deep pyramids, small planes): the fused kernel
+  // measured no faster than the two passes there, and is not built for them.
   if (pl.tbr != 8)
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d takes 4-row gradient tiles: no fused backward kernel",
                 d->H, d->W);
@@ -598,16 +601,18 @@ wtconv_status_t plan_bwf(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan& fp) {
       layout(q, ns);
       found = pl.smem_bytes <= two_per_sm;
     }
-  if (!found) {
-    layout(1, 1);
-    if (pl.smem_bytes > kMaxSmemPerBlock)
-      return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %d B of shared memory for the fused "
-                  "backward (max %d)", d->H, d->W, L, pl.smem_bytes, kMaxSmemPerBlock);
-  }
+  // One 256-thread CTA per SM leaves too few warps to hide the phases'
+  // latency: such layers run the two separate passes (which keep 2-3 CTAs
+  // per SM) instead.
+  if (!found)
+    return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels: the fused backward's working set leaves "
+                "one CTA per SM", d->H, d->W, L);
   fp.P = pl.P;
   fwd_divs(fp);
   pl.batches = d->N > 0 ? ceil_div(d->N, pl.P) : 0;
   int per_sm = wt::bwf_ctas_per_sm(pl, fp, d->dtype);
+  if (per_sm == 1)
+    return fail(WTCONV_ERR_UNSUPPORTED, "k=%d: the fused backward's registers leave one CTA per SM", d->k);
   if (per_sm <= 0) {
     per_sm = (int)(kSmemPerSm / (pl.smem_bytes + 1024));
     if (per_sm > 2) per_sm = 2;

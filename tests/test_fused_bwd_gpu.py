@@ -2,10 +2,12 @@
 x and dy where the planes fit), against the float64 oracle and against the
 two separate calls it replaces.
 
-The FUSED shapes are ones whose planes the fused kernel takes (8-row
-gradient tiles, planes up to 64 x 64 pixels); the FALLBACK shapes are ones
-it hands to the two separate passes (4-row gradient tiles, planes beyond one
-CTA), which the call must do transparently.  Tolerances against the oracle
+The FUSED shapes are ones the fused kernel takes in float32 (8-row gradient
+tiles, planes up to 64 x 64 pixels); the FALLBACK shapes are ones it hands
+to the two separate passes, which the call must do transparently: 4-row
+gradient tiles (deep pyramids, small planes packed several per unit),
+planes beyond one CTA, and a 16-bit layer whose fused working set would
+leave one CTA per SM.  Tolerances against the oracle
 are those of the other parity tests; against the separate calls (same
 float32 arithmetic, other evaluation order) dx and every gradient agree to
 a relative 1e-6 of their largest magnitude in float32.
@@ -23,7 +25,8 @@ pytestmark = pytest.mark.gpu
 
 FUSED = [(2, 4, 56, 56, 3, 5), (3, 4, 28, 28, 2, 5), (2, 2, 40, 40, 1, 5), (2, 2, 64, 48, 6, 3),
          (2, 3, 16, 16, 2, 5), (3, 2, 32, 32, 1, 7), (2, 2, 48, 40, 3, 9), (2, 2, 56, 55, 2, 5)]
-FALLBACK = [(2, 3, 13, 17, 3, 5), (9, 6, 7, 7, 2, 5), (2, 2, 130, 124, 2, 5)]
+FALLBACK = [(2, 3, 13, 17, 3, 5, "f32"), (9, 6, 7, 7, 2, 5, "f32"), (2, 3, 28, 28, 4, 5, "f16"),
+            (2, 2, 130, 124, 2, 5, "f32"), (2, 4, 56, 56, 3, 5, "bf16")]
 
 
 def run_fused(wt, inp, d):
@@ -69,9 +72,10 @@ def test_fused_matches_oracle_and_separate_calls(wt, shape, dtype):
     check(wt, synth.make_inputs(*shape, dtype=dtype, seed=sum(shape) + 7))
 
 
-@pytest.mark.parametrize("shape", FALLBACK, ids=lambda s: "x".join(map(str, s)))
-def test_planes_the_fused_kernel_does_not_take(wt, shape):
-    check(wt, synth.make_inputs(*shape, seed=sum(shape) + 9))
+@pytest.mark.parametrize("case", FALLBACK, ids=lambda s: "x".join(map(str, s)))
+def test_layers_the_fused_kernel_does_not_take(wt, case):
+    *shape, dtype = case
+    check(wt, synth.make_inputs(*shape, dtype=dtype, seed=sum(shape) + 9))
 
 
 @pytest.mark.parametrize("name", ["stage1", "stage2_f16"])
