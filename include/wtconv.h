@@ -139,9 +139,12 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
  * library's.  Results match the two separate calls up to floating-point
  * evaluation order; the parameter gradients are deterministic.  The
  * workspace must hold wtconv_workspace_size(desc, WTCONV_OP_BWD) bytes
- * (256-byte aligned).  Planes whose fused working set does not fit one CTA
- * (beyond 56 x 56, depending on k and levels) run the two separate passes
- * inside this call.  Errors as for the two calls. */
+ * (256-byte aligned).  Layers the fused kernel does not take run the two
+ * separate passes inside this call, with the same results: planes beyond
+ * 56 x 56 (depending on k and levels), pyramids whose gradient pass uses
+ * 4-row tiles (deep pyramids, small planes packed several per unit; the
+ * fused kernel measured no faster there), and layers whose fused working
+ * set would leave one CTA per SM.  Errors as for the two calls. */
 wtconv_status_t wtconv_bwd(const wtconv_desc_t* desc, const void* x, const void* dy, const float* w_base,
                            const float* b_base, const float* w_sub, const float* base_scale,
                            const float* wavelet_scale, void* dx, float* dw_base, float* db_base, float* dw_sub,
