@@ -9,7 +9,9 @@
 #include <string.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "../../include/wtconv.h"
 #include "wtconv_launch.h"
@@ -962,6 +964,67 @@ wtconv_status_t prepare_win(const wtconv_desc_t* d, WtFwdPlan& pl, CUtensorMap* 
 
 namespace wt {
 void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
+namespace {
+std::mutex g_cache_mu;
+std::map<std::pair<int, const void*>, int> g_smem_set;                    // (device, kernel) -> limit set
+std::map<std::tuple<int, const void*, int, int>, int> g_occupancy;        // (device, kernel, threads, smem)
+std::map<int, int> g_sms;                                                 // device -> SM count
+}  // namespace
+
+cudaError_t ensure_smem(const void* f, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  auto it = g_smem_set.find({dev, f});
+  if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) g_smem_set[{dev, f}] = bytes;
+  return e;
+}
+
+int occupancy(const void* f, int threads, int smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    auto it = g_occupancy.find({dev, f, threads, smem});
+    if (it != g_occupancy.end()) return it->second;
+  }
+  int n = 0;
+  if (ensure_smem(f, smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  g_occupancy[{dev, f, threads, smem}] = n;
+  return n;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    auto it = g_sms.find(dev);
+    if (it != g_sms.end()) return it->second;
+  }
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  g_sms[dev] = n;
+  return n;
+}
 }  // namespace wt
 
 extern "C" {

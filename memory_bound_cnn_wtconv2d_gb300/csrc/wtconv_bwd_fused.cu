@@ -23,7 +23,7 @@ cudaError_t launch_bwd_fused(const WtBwPlan& pl, const WtFwdPlan& fp, const CUte
                              cudaStream_t stream) {
   const void* f = bwf_pick(pl, fp, dtype);
   if (!f) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+  cudaError_t e = ensure_smem(f, pl.smem_bytes);
   if (e != cudaSuccess) return e;
   WtBwPlan plc = pl;
   WtFwdPlan fpc = fp;
@@ -39,16 +39,7 @@ cudaError_t launch_bwd_fused(const WtBwPlan& pl, const WtFwdPlan& fp, const CUte
 int bwf_ctas_per_sm(const WtBwPlan& pl, const WtFwdPlan& fp, int dtype) {
   const void* f = bwf_pick(pl, fp, dtype);
   if (!f) return 0;
-  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, WT_BW_THREADS, pl.smem_bytes) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
+  return occupancy(f, WT_BW_THREADS, pl.smem_bytes);
 }
 
 unsigned int take_bwf_faults() { return take_bwf_faults_tr8(); }

@@ -373,7 +373,7 @@ template <int K, typename T>
 static cudaError_t launch_bw_t(const WtBwPlan& pl, const CUtensorMap& tmx, const CUtensorMap& tmd, const void* x,
                                const void* dy, float* part, cudaStream_t stream) {
   auto kern = pl.tbr == 8 ? bw_kernel<K, T, 8> : bw_kernel<K, T, 4>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+  cudaError_t e = ensure_smem((const void*)kern, pl.smem_bytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)pl.grid;
   kern<<<grid, WT_BW_THREADS, pl.smem_bytes, stream>>>(pl, tmx, tmd, static_cast<const T*>(x),
@@ -436,16 +436,7 @@ int bw_ctas_per_sm(const WtBwPlan& pl, int dtype) {
   else { WT_BW_PICK_K(__nv_bfloat16) }
 #undef WT_BW_PICK_K
 #undef WT_BW_PICK
-  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, WT_BW_THREADS, pl.smem_bytes) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
+  return occupancy(f, WT_BW_THREADS, pl.smem_bytes);
 }
 
 unsigned int take_bw_faults() {

@@ -281,7 +281,7 @@ cudaError_t launch_bwd_weight_win(const WtBwPlan& pl, const CUtensorMap& tmx, co
                                   cudaStream_t stream) {
   const void* f = bw_win_pick(pl, dtype);
   if (!f) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+  cudaError_t e = ensure_smem(f, pl.smem_bytes);
   if (e != cudaSuccess) return e;
   WtBwPlan plc = pl;
   CUtensorMap mx = tmx, md = tmd;
@@ -316,16 +316,7 @@ int bw_win_regs(int k, int tbr, int dtype) {
 int bw_win_ctas_per_sm(const WtBwPlan& pl, int dtype) {
   const void* f = bw_win_pick(pl, dtype);
   if (!f) return 0;
-  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, WT_BW_THREADS, pl.smem_bytes) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
+  return occupancy(f, WT_BW_THREADS, pl.smem_bytes);
 }
 
 unsigned int take_bww_faults() {

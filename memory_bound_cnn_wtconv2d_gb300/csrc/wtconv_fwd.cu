@@ -251,13 +251,11 @@ static cudaError_t launch_fwd_t(const WtFwdPlan& pl, const CUtensorMap& tmx, con
                                 const float* b_base, const float* w_sub, const float* s_base,
                                 const float* s_w, void* y, cudaStream_t stream) {
   auto kern = fwd_kernel<K, T, ROT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+  cudaError_t e = ensure_smem((const void*)kern, pl.smem_bytes);
   if (e != cudaSuccess) return e;
-  int per_sm = 0, dev = 0, sms = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, WT_FWD_THREADS, pl.smem_bytes);
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
+  const int per_sm = occupancy((const void*)kern, WT_FWD_THREADS, pl.smem_bytes);
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
   const long long units = (long long)pl.C * pl.groups;
   long long slots = (long long)(per_sm < 1 ? 1 : per_sm) * sms;
   const unsigned grid = (unsigned)(units < slots ? units : slots);

@@ -70,4 +70,15 @@ int bw_win_regs(int k, int tbr, int dtype);
 // Sets the thread-local message returned by wtconv_last_error().
 void set_last_error(const char* msg);
 
+// Host-side caches, per device, of what every call would otherwise ask the
+// runtime again (each a few microseconds):
+//   ensure_smem: raises kernel f's opt-in dynamic shared-memory limit to at
+//     least `bytes` (one cudaFuncSetAttribute per new maximum);
+//   occupancy: resident CTAs per SM of f at `threads` threads and `smem`
+//     dynamic bytes (after ensure_smem), 0 if the runtime cannot tell;
+//   sm_count: the current device's SM count.
+cudaError_t ensure_smem(const void* f, int bytes);
+int occupancy(const void* f, int threads, int smem);
+int sm_count();
+
 }  // namespace wt
