@@ -3,13 +3,38 @@
 A drop-in replacement for a depthwise k x k convolution ("Fast and
 Memory-Efficient Wavelet Convolutions via I/O-Aware Reformulation",
 arXiv 2608.10805, technical summary "Problem statement").  Forward runs
-``wtconv_fwd``; backward runs ``wtconv_bwd_data`` and ``wtconv_bwd_weight``.
+``wtconv_fwd``; backward runs ``wtconv_bwd`` (input and parameter gradients
+in one fused call), or ``wtconv_bwd_data`` / ``wtconv_bwd_weight`` alone when
+only one of them is needed.
 """
 from __future__ import annotations
+
+import threading
 
 import torch
 
 from . import wtconv as _c
+
+# Gradient workspaces, one per (device, stream, layer shape, dtype, call),
+# reused across steps: the library overwrites every byte it reads, so a
+# workspace needs no clearing, and reusing it spares each backward step a
+# size query (a full launch plan) and an allocation.  Calls on one stream
+# run in order, so sharing a workspace between them is safe.
+_WORKSPACES: dict = {}
+_WS_LOCK = threading.Lock()
+
+
+def _workspace(x, levels, k, op):
+    stream = torch.cuda.current_stream(x.device)
+    key = (x.device, stream.cuda_stream, tuple(x.shape), x.dtype, levels, k, op)
+    with _WS_LOCK:
+        ws = _WORKSPACES.get(key)
+    if ws is None:
+        need = _c.wtconv_workspace_size(_c.desc_for(x, levels, k), op)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+        with _WS_LOCK:
+            _WORKSPACES[key] = ws
+    return ws
 
 
 class WTConv2dFunction(torch.autograd.Function):
@@ -30,11 +55,13 @@ class WTConv2dFunction(torch.autograd.Function):
         need_params = any(ctx.needs_input_grad[1:6])
         dx, g = None, None
         if need_dx and need_params:  # one call: the fused backward
-            dx, g = _c.wtconv_bwd(x, dy, w_base, b, w_sub, base_scale, wavelet_scale, ctx.levels, ctx.k)
+            dx, g = _c.wtconv_bwd(x, dy, w_base, b, w_sub, base_scale, wavelet_scale, ctx.levels, ctx.k,
+                                  workspace=_workspace(x, ctx.levels, ctx.k, _c.OP_BWD))
         elif need_dx:
             dx = _c.wtconv_bwd_data(dy, w_base, w_sub, base_scale, wavelet_scale, ctx.levels, ctx.k)
         elif need_params:
-            g = _c.wtconv_bwd_weight(x, dy, w_base, b, w_sub, base_scale, wavelet_scale, ctx.levels, ctx.k)
+            g = _c.wtconv_bwd_weight(x, dy, w_base, b, w_sub, base_scale, wavelet_scale, ctx.levels, ctx.k,
+                                     workspace=_workspace(x, ctx.levels, ctx.k, _c.OP_BWD_WEIGHT))
         if g is None:
             return (dx, None, None, None, None, None, None, None)
         return (dx, g["dw_base"], g["db_base"], g["dw_sub"], g["dbase_scale"], g["dwavelet_scale"],

@@ -159,8 +159,8 @@ def wtconv_bwd_weight(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, l
                      db_base=None if b_base is None else torch.empty_like(b_base),
                      dw_sub=torch.empty_like(w_sub), dbase_scale=torch.empty_like(base_scale),
                      dwavelet_scale=torch.empty_like(wavelet_scale))
-    need = wtconv_workspace_size(desc, OP_BWD_WEIGHT)
-    if workspace is None:
+    if workspace is None:  # a caller-provided workspace is checked by the library itself
+        need = wtconv_workspace_size(desc, OP_BWD_WEIGHT)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _check(lib().wtconv_bwd_weight(
         ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(_param(w_base, "w_base")),
@@ -185,8 +185,8 @@ def wtconv_bwd(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, 
                      db_base=None if b_base is None else torch.empty_like(b_base),
                      dw_sub=torch.empty_like(w_sub), dbase_scale=torch.empty_like(base_scale),
                      dwavelet_scale=torch.empty_like(wavelet_scale))
-    need = wtconv_workspace_size(desc, OP_BWD)
-    if workspace is None:
+    if workspace is None:  # a caller-provided workspace is checked by the library itself
+        need = wtconv_workspace_size(desc, OP_BWD)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _check(lib().wtconv_bwd(
         ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(_param(w_base, "w_base")),
