@@ -122,6 +122,116 @@ void fwd_geometry(const wtconv_desc_t* d, WtFwdPlan& pl, int tp) {
   pl.wf = round_up(off, 4);
 }
 
+// Plans depend only on the layer geometry, the load mode (windowed passes)
+// and the device (occupancy), not on the tensors, so successful plans are
+// kept: a call with a known layer does not plan again (planning is a few
+// microseconds of host time; a layer's fused backward is one launch, so that
+// time would otherwise delay it).  Failures are not kept (their message is
+// set by planning).
+struct PlanKey {
+  int v[9];
+  bool operator<(const PlanKey& o) const {
+    for (int i = 0; i < 9; ++i)
+      if (v[i] != o.v[i]) return v[i] < o.v[i];
+    return false;
+  }
+};
+
+PlanKey plan_key(const wtconv_desc_t* d, int extra) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  return PlanKey{{dev, d->N, d->C, d->H, d->W, d->levels, d->k, d->dtype, extra}};
+}
+
+template <typename T>
+class PlanCache {
+ public:
+  bool get(const PlanKey& k, T* out) {
+    std::lock_guard<std::mutex> lock(mu_);
+    auto it = m_.find(k);
+    if (it == m_.end()) return false;
+    *out = it->second;
+    return true;
+  }
+  void put(const PlanKey& k, const T& v) {
+    std::lock_guard<std::mutex> lock(mu_);
+    if (m_.size() >= 1024) m_.clear();  // bound the memory of long-running processes with many shapes
+    m_[k] = v;
+  }
+
+ private:
+  std::mutex mu_;
+  std::map<PlanKey, T> m_;
+};
+
+struct BwfPlans {
+  WtBwPlan bw;
+  WtFwdPlan fwd;
+};
+
+wtconv_status_t plan_fwd_compute(const wtconv_desc_t* d, WtFwdPlan& pl);
+wtconv_status_t plan_win_compute(const wtconv_desc_t* d, WtFwdPlan& pl, int load);
+wtconv_status_t plan_bw_compute(const wtconv_desc_t* d, WtBwPlan& pl);
+wtconv_status_t plan_bwf_compute(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan& fp);
+wtconv_status_t plan_bw_win_compute(const wtconv_desc_t* d, WtBwPlan& pl, int load);
+
+wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
+  static PlanCache<WtFwdPlan> cache;
+  const PlanKey k = plan_key(d, -1);
+  if (cache.get(k, &pl)) return WTCONV_OK;
+  const wtconv_status_t st = plan_fwd_compute(d, pl);
+  if (st == WTCONV_OK) cache.put(k, pl);
+  return st;
+}
+
+wtconv_status_t plan_win(const wtconv_desc_t* d, WtFwdPlan& pl, int load) {
+  static PlanCache<WtFwdPlan> cache;
+  const PlanKey k = plan_key(d, load);
+  if (cache.get(k, &pl)) return WTCONV_OK;
+  const wtconv_status_t st = plan_win_compute(d, pl, load);
+  if (st == WTCONV_OK) cache.put(k, pl);
+  return st;
+}
+
+wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
+  static PlanCache<WtBwPlan> cache;
+  const PlanKey k = plan_key(d, -1);
+  if (cache.get(k, &pl)) return WTCONV_OK;
+  const wtconv_status_t st = plan_bw_compute(d, pl);
+  if (st == WTCONV_OK) cache.put(k, pl);
+  return st;
+}
+
+wtconv_status_t plan_bw_win(const wtconv_desc_t* d, WtBwPlan& pl, int load) {
+  static PlanCache<WtBwPlan> cache;
+  const PlanKey k = plan_key(d, load);
+  if (cache.get(k, &pl)) return WTCONV_OK;
+  const wtconv_status_t st = plan_bw_win_compute(d, pl, load);
+  if (st == WTCONV_OK) cache.put(k, pl);
+  return st;
+}
+
+wtconv_status_t plan_bwf(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan& fp) {
+  static PlanCache<BwfPlans> cache;
+  const PlanKey k = plan_key(d, -1);
+  BwfPlans b;
+  if (cache.get(k, &b)) {
+    pl = b.bw;
+    fp = b.fwd;
+    return WTCONV_OK;
+  }
+  const wtconv_status_t st = plan_bwf_compute(d, pl, fp);
+  if (st == WTCONV_OK) {
+    b.bw = pl;
+    b.fwd = fp;
+    cache.put(k, b);
+  }
+  return st;
+}
+
 // Loop divisors of the analysis, band-convolution and final-tile phases.
 void fwd_divs(WtFwdPlan& pl) {
   const int L = pl.L;
@@ -145,7 +255,7 @@ void fwd_divs(WtFwdPlan& pl) {
   pl.f_c = make_div(pl.ftc);
 }
 
-wtconv_status_t plan_fwd(const wtconv_desc_t* d, WtFwdPlan& pl) {
+wtconv_status_t plan_fwd_compute(const wtconv_desc_t* d, WtFwdPlan& pl) {
   memset(&pl, 0, sizeof(pl));
   pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
   const int L = d->levels, KK = d->k * d->k;
@@ -297,7 +407,7 @@ long win_smem_bytes(const WtFwdPlan& pl, int P, int nsets, int load, int wfloats
 // forced tilings on a GB300 (224 x 224 planes at levels 1-4 and k = 3, 5, 7;
 // 128 x 128 and 512 x 512 planes; float32 and float16), where the model's
 // choice came within 2% of the fastest tiling measured.
-wtconv_status_t plan_win(const wtconv_desc_t* d, WtFwdPlan& pl, int load) {
+wtconv_status_t plan_win_compute(const wtconv_desc_t* d, WtFwdPlan& pl, int load) {
   memset(&pl, 0, sizeof(pl));
   pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
   const int R = d->k / 2, L = d->levels, KK = d->k * d->k, S = 1 << L;
@@ -433,7 +543,7 @@ wtconv_status_t bw_grid(const wtconv_desc_t* d, WtBwPlan& pl, int per_sm) {
   return WTCONV_OK;
 }
 
-wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
+wtconv_status_t plan_bw_compute(const wtconv_desc_t* d, WtBwPlan& pl) {
   memset(&pl, 0, sizeof(pl));
   pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
   const int R = d->k / 2, L = d->levels, KK = d->k * d->k;
@@ -529,7 +639,7 @@ wtconv_status_t plan_bw(const wtconv_desc_t* d, WtBwPlan& pl) {
 // [mbarriers].  Two input sets and two CTAs per SM are preferred, then one
 // set, then fewer planes per unit; layers that cannot keep two CTAs per SM
 // are refused (the caller then runs the two separate passes).
-wtconv_status_t plan_bwf(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan& fp) {
+wtconv_status_t plan_bwf_compute(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan& fp) {
   const wtconv_status_t st = plan_bw(d, pl);  // fails for planes beyond one CTA
   if (st != WTCONV_OK) return st;
   // 4-row correlation tiles (deep pyramids, small planes): the fused kernel
@@ -713,7 +823,7 @@ void bw_win_layout(WtBwPlan& pl, int P, int nsets, int load) {
 // k = 5, 7; 128, 384 and 512-pixel planes; float32 and float16), where the
 // model's choice came within 0.3 % of the fastest measured tiling on seven
 // of eight shapes and within 6.3 % on the eighth.
-wtconv_status_t plan_bw_win(const wtconv_desc_t* d, WtBwPlan& pl, int load) {
+wtconv_status_t plan_bw_win_compute(const wtconv_desc_t* d, WtBwPlan& pl, int load) {
   memset(&pl, 0, sizeof(pl));
   pl.N = d->N; pl.C = d->C; pl.H = d->H; pl.W = d->W; pl.L = d->levels; pl.K = d->k;
   const int R = d->k / 2, L = d->levels, KK = d->k * d->k, S = 1 << L;
