@@ -94,3 +94,30 @@ def test_workspace_size_invalid_desc_is_zero(L):
     d = wtconv.make_desc(4, 8, 28, 28, 3, 4, 0)
     assert L.wtconv_workspace_size(ctypes.byref(d), wtconv.OP_BWD_WEIGHT) == 0
     assert L.wtconv_workspace_size(None, wtconv.OP_BWD_WEIGHT) == 0
+
+
+def test_plans_are_consistent_under_concurrent_calls(L):
+    # Launch plans are cached per layer geometry inside the library and shared
+    # by all threads; ctypes releases the interpreter lock during the call, so
+    # these queries run concurrently in the library.  Every thread must see
+    # the same workspace sizes as a single-threaded pass, for every call kind
+    # (whole planes, planes beyond one CTA, the fused backward).
+    import concurrent.futures
+    shapes = [(N, C, H, W, lv, k, dt) for (N, C, H, W) in ((2, 3, 13, 17), (64, 96, 56, 56), (3, 4, 28, 28),
+                                                          (2, 2, 150, 150), (1, 2, 57, 61), (9, 6, 7, 7))
+              for lv in (1, 3) for k in (3, 5) for dt in (0, 1)]
+    ops = (wtconv.OP_BWD_WEIGHT, wtconv.OP_BWD)
+
+    def sizes():
+        out = []
+        for s in shapes:
+            d = wtconv.make_desc(*s)
+            out.append(tuple(L.wtconv_workspace_size(ctypes.byref(d), op) for op in ops))
+        return out
+
+    reference = sizes()
+    assert all(a > 0 and b > 0 for a, b in reference)
+    with concurrent.futures.ThreadPoolExecutor(8) as ex:
+        results = list(ex.map(lambda _: sizes(), range(16)))
+    for r in results:
+        assert r == reference
