@@ -56,3 +56,15 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["unit"] == "ms/layer" and line["higher_is_better"] is False
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_bench_algorithmic_counts():
+    # The roofline's algorithmic figures: 181,300 FMAs per 56x56 plane at 3
+    # levels and k = 5 (25 per base output and per coefficient of the 4 bands
+    # at 28x28, 14x14, 7x7), i.e. 1.114 G per pass over the stage-1 layer's
+    # 6144 planes; odd sizes are padded to even at every level.
+    import bench
+    assert bench.fma_per_plane(56, 56, 3, 5) == 25 * (56 * 56 + 4 * (28 * 28 + 14 * 14 + 7 * 7)) == 181300
+    assert bench.fma_per_plane(56, 56, 3, 5) * 64 * 96 == 1113907200
+    assert bench.level_sizes(7, 5, 3) == ([7, 4, 2, 1], [5, 3, 2, 1])
+    assert bench.fma_per_plane(1, 1, 2, 3) == 9 * (1 + 4 * 2)

@@ -24,7 +24,9 @@ from test_parity_gpu import GRADS, compare, to_dev, wt  # noqa: F401  (wt is a f
 pytestmark = pytest.mark.gpu
 
 FUSED = [(2, 4, 56, 56, 3, 5), (3, 4, 28, 28, 2, 5), (2, 2, 40, 40, 1, 5), (2, 2, 64, 48, 6, 3),
-         (2, 3, 16, 16, 2, 5), (3, 2, 32, 32, 1, 7), (2, 2, 48, 40, 3, 9), (2, 2, 56, 55, 2, 5)]
+         (2, 3, 16, 16, 2, 5), (3, 2, 32, 32, 1, 7), (2, 2, 48, 40, 3, 9), (2, 2, 56, 55, 2, 5),
+         # ragged last plane group (3 + 1, 3 + 3 + 1, 2 + 2 + 1 planes per unit) and the largest plane
+         (4, 4, 28, 28, 2, 5), (7, 2, 32, 32, 1, 7), (5, 3, 40, 40, 1, 5), (2, 2, 64, 64, 1, 5)]
 FALLBACK = [(2, 3, 13, 17, 3, 5, "f32"), (9, 6, 7, 7, 2, 5, "f32"), (2, 3, 28, 28, 4, 5, "f16"),
             (2, 2, 130, 124, 2, 5, "f32"), (2, 4, 56, 56, 3, 5, "bf16")]
 
