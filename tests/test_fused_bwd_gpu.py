@@ -117,3 +117,42 @@ def test_empty_batch_and_small_workspace(wt):
                       2, 5, workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
     assert err.value.status == wt.WTCONV_ERR_WORKSPACE
     check(wt, inp, d)  # the refusal launched nothing and left the context usable
+
+
+def test_step_replays_from_a_cuda_graph(wt):
+    # No call synchronises the host or allocates, so a whole step (forward +
+    # fused backward) can be captured once and replayed, which is how small,
+    # launch-bound layers are best run.  The replay must reproduce the eager
+    # results bit for bit, on new inputs copied into the captured buffers.
+    inp = synth.make_inputs(2, 32, 32, 32, 2, 5, seed=41)
+    d = to_dev(inp)
+    ps = [d[n] for n in ("w_base", "b_base", "w_sub", "base_scale", "wavelet_scale")]
+    x, dy = d["x"].clone(), d["dy"].clone()
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    g = {n: torch.empty_like(p) for n, p in zip(GRADS, ps)}
+    ws = torch.empty(max(wt.wtconv_workspace_size(wt.desc_for(x, 2, 5), wt.OP_BWD), 256), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        wt.wtconv_fwd(x, *ps, 2, 5, y=y)
+        wt.wtconv_bwd(x, dy, *ps, 2, 5, dx=dx, grads=g, workspace=ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    x.copy_(torch.flip(d["x"], dims=[3]))
+    dy.copy_(torch.flip(d["dy"], dims=[2]))
+    graph.replay()
+    torch.cuda.synchronize()
+    got = (y.clone(), dx.clone(), {n: t.clone() for n, t in g.items()})
+    step()
+    torch.cuda.synchronize()
+    assert wt.wtconv_device_faults() == 0
+    assert torch.equal(got[0], y) and torch.equal(got[1], dx)
+    for n in GRADS:
+        assert torch.equal(got[2][n], g[n]), n
