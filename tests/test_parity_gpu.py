@@ -172,6 +172,42 @@ def test_autograd_module_matches_oracle(wt):
     compare("dwavelet_scale", m.wavelet_scale.grad.cpu().numpy(), g["dwavelet_scale"], "f32", True)
 
 
+@pytest.mark.parametrize("which", ["input_only", "params_only"])
+def test_autograd_module_single_gradient_paths(wt, which):
+    # The module's backward computes only what autograd asks for: dx alone
+    # (frozen parameters) runs the input-gradient call, parameter gradients
+    # alone (an input that needs no gradient) the parameter-gradient call.
+    from memory_bound_cnn_wtconv2d_gb300.layer import WTConv2d
+    torch.manual_seed(1)
+    m = WTConv2d(4, kernel_size=5, levels=2, device="cuda")
+    x = torch.randn(2, 4, 20, 24, device="cuda", requires_grad=(which == "input_only"))
+    if which == "input_only":
+        for p in m.parameters():
+            p.requires_grad_(False)
+    y = m(x)
+    dy = torch.randn_like(y)
+    y.backward(dy)
+    inp = synth.make_inputs(2, 4, 20, 24, 2, 5)
+    inp.x = x.detach().cpu().numpy()
+    inp.dy = dy.cpu().numpy()
+    inp.w_base = m.weight.detach().cpu().numpy()
+    inp.b_base = m.bias.detach().cpu().numpy()
+    inp.w_sub = m.wavelet_weight.detach().cpu().numpy()
+    inp.base_scale = m.base_scale.detach().cpu().numpy()
+    inp.wavelet_scale = m.wavelet_scale.detach().cpu().numpy()
+    g = oracle.bwd(inp)
+    if which == "input_only":
+        compare("dx", x.grad.cpu().numpy(), g["dx"], "f32", False)
+        assert all(p.grad is None for p in m.parameters())
+    else:
+        assert x.grad is None
+        compare("dw_base", m.weight.grad.cpu().numpy(), g["dw_base"], "f32", True)
+        compare("db_base", m.bias.grad.cpu().numpy(), g["db_base"], "f32", True)
+        compare("dw_sub", m.wavelet_weight.grad.cpu().numpy(), g["dw_sub"], "f32", True)
+        compare("dbase_scale", m.base_scale.grad.cpu().numpy(), g["dbase_scale"], "f32", True)
+        compare("dwavelet_scale", m.wavelet_scale.grad.cpu().numpy(), g["dwavelet_scale"], "f32", True)
+
+
 # ---- full-size workloads, in the launch configuration the benchmark times ----
 
 @pytest.mark.parametrize("name", ["stage1", "stage2_f16", "stage2_bf16"])
