@@ -121,3 +121,32 @@ def test_plans_are_consistent_under_concurrent_calls(L):
         results = list(ex.map(lambda _: sizes(), range(16)))
     for r in results:
         assert r == reference
+
+
+def test_fused_backward_argument_checks(L):
+    # wtconv_bwd validates everything before any launch: null and misaligned
+    # activations, null required gradients, and a missing, short or
+    # misaligned workspace each return their status code (no device needed).
+    d = wtconv.make_desc(2, 4, 56, 56, 3, 5, 0)  # a layer the fused kernel takes
+    need = L.wtconv_workspace_size(ctypes.byref(d), wtconv.OP_BWD)
+    assert need > 0 and need % 256 == 0
+    p = ctypes.c_void_p(FAKE)
+
+    def call(x=FAKE, dy=FAKE, dx=FAKE, dw=FAKE, ws=FAKE, ws_bytes=None):
+        v = lambda a: None if a == 0 else ctypes.c_void_p(a)
+        return L.wtconv_bwd(ctypes.byref(d), v(x), v(dy), p, None, p, p, p, v(dx), v(dw), None, p, p, p, v(ws),
+                            need if ws_bytes is None else ws_bytes, None)
+
+    assert call(x=0) == wtconv.WTCONV_ERR_INVALID_ARG
+    assert call(dx=0) == wtconv.WTCONV_ERR_INVALID_ARG
+    assert call(dw=0) == wtconv.WTCONV_ERR_INVALID_ARG
+    assert call(dy=FAKE + 2) == wtconv.WTCONV_ERR_MISALIGNED
+    assert call(dx=FAKE + 1) == wtconv.WTCONV_ERR_MISALIGNED
+    assert call(ws=0) == wtconv.WTCONV_ERR_WORKSPACE
+    assert call(ws_bytes=need - 256) == wtconv.WTCONV_ERR_WORKSPACE
+    assert call(ws=FAKE + 16) == wtconv.WTCONV_ERR_MISALIGNED
+    bad = wtconv.make_desc(2, 4, 56, 56, 3, 4, 0)  # even k
+    v = ctypes.c_void_p(FAKE)
+    assert L.wtconv_bwd(ctypes.byref(bad), v, v, v, None, v, v, v, v, v, None, v, v, v, v, need, None) == \
+        wtconv.WTCONV_ERR_INVALID_ARG
+    assert L.wtconv_last_error().decode() != ""
