@@ -100,20 +100,69 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _act(t, name):
-    if not (t.is_cuda and t.is_contiguous()):
+# The library sees plain pointers, so every size it relies on is checked
+# here: a tensor smaller than the layer implies would be read or written past
+# its end by the kernels.
+
+
+def _act(t, name, like=None):
+    """An activation: contiguous CUDA; `like` (x) fixes shape, dtype and device."""
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if like is not None and (t.shape != like.shape or t.dtype != like.dtype or t.device != like.device):
+        raise ValueError(f"{name} must be {tuple(like.shape)} {like.dtype} on {like.device}, "
+                         f"got {tuple(t.shape)} {t.dtype} on {t.device}")
     return t
 
 
-def _param(t, name, optional=False):
+def _param(t, name, numel, device, optional=False):
+    """A parameter or gradient: contiguous float32 on `device` with `numel`
+    elements (any shape: [C,k,k] and the depthwise [C,1,k,k] both work)."""
     if t is None:
         if optional:
             return None
         raise ValueError(f"{name} is required")
-    if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.float32):
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous() and t.dtype == torch.float32):
         raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    if t.device != device or t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} elements on {device}, got {t.numel()} on {t.device}")
     return t
+
+
+def _param_sizes(x, levels, k):
+    """Element counts of w_base, b_base, w_sub, base_scale, wavelet_scale."""
+    C, L, kk = x.shape[1], int(levels), int(k) * int(k)
+    return C * kk, C, L * 4 * C * kk, C, L * 4 * C
+
+
+def _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale):
+    n = _param_sizes(x, levels, k)
+    d = x.device
+    return (_param(w_base, "w_base", n[0], d), _param(b_base, "b_base", n[1], d, True),
+            _param(w_sub, "w_sub", n[2], d), _param(base_scale, "base_scale", n[3], d),
+            _param(wavelet_scale, "wavelet_scale", n[4], d))
+
+
+def _grads(grads, params):
+    """The caller's gradient buffers (checked), or new ones shaped like the
+    parameters.  Without a bias db_base may be absent or None; a db_base that
+    is given still receives the gradient a bias would have (s_base * sum dy)."""
+    names = ("dw_base", "db_base", "dw_sub", "dbase_scale", "dwavelet_scale")
+    if grads is None:
+        return {n: None if p is None else torch.empty_like(p) for n, p in zip(names, params)}
+    C = params[3].numel()
+    for n, p in zip(names, params):
+        if p is not None:
+            _param(grads.get(n), n, p.numel(), p.device)
+        elif grads.get(n) is not None:
+            _param(grads[n], n, C, params[0].device)
+    return grads if "db_base" in grads else dict(grads, db_base=None)
+
+
+def _workspace_bytes(ws, device):
+    if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.is_contiguous() and ws.device == device):
+        raise ValueError(f"workspace must be a contiguous CUDA tensor on {device}")
+    return ws.numel() * ws.element_size()
 
 
 def _stream(stream):
@@ -126,11 +175,9 @@ def wtconv_fwd(x, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k, y
     """y = WTConv2d(x)."""
     _act(x, "x")
     desc = desc_for(x, levels, k)
-    y = torch.empty_like(x) if y is None else _act(y, "y")
-    _check(lib().wtconv_fwd(ctypes.byref(desc), _ptr(x), _ptr(_param(w_base, "w_base")),
-                            _ptr(_param(b_base, "b_base", True)), _ptr(_param(w_sub, "w_sub")),
-                            _ptr(_param(base_scale, "base_scale")),
-                            _ptr(_param(wavelet_scale, "wavelet_scale")), _ptr(y), None, 0, _stream(stream)))
+    ps = _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale)
+    y = torch.empty_like(x) if y is None else _act(y, "y", like=x)
+    _check(lib().wtconv_fwd(ctypes.byref(desc), _ptr(x), *map(_ptr, ps), _ptr(y), None, 0, _stream(stream)))
     return y
 
 
@@ -138,11 +185,10 @@ def wtconv_bwd_data(dy, w_base, w_sub, base_scale, wavelet_scale, levels, k, dx=
     """dx = dL/dx for upstream gradient dy."""
     _act(dy, "dy")
     desc = desc_for(dy, levels, k)
-    dx = torch.empty_like(dy) if dx is None else _act(dx, "dx")
-    _check(lib().wtconv_bwd_data(ctypes.byref(desc), _ptr(dy), _ptr(_param(w_base, "w_base")),
-                                 _ptr(_param(w_sub, "w_sub")), _ptr(_param(base_scale, "base_scale")),
-                                 _ptr(_param(wavelet_scale, "wavelet_scale")), _ptr(dx), None, 0,
-                                 _stream(stream)))
+    wb, _, ws_, sb, sw = _params(dy, levels, k, w_base, None, w_sub, base_scale, wavelet_scale)
+    dx = torch.empty_like(dy) if dx is None else _act(dx, "dx", like=dy)
+    _check(lib().wtconv_bwd_data(ctypes.byref(desc), _ptr(dy), _ptr(wb), _ptr(ws_), _ptr(sb), _ptr(sw), _ptr(dx),
+                                 None, 0, _stream(stream)))
     return dx
 
 
@@ -151,23 +197,18 @@ def wtconv_bwd_weight(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, l
     """Parameter gradients as a dict: dw_base, db_base (None without bias), dw_sub,
     dbase_scale, dwavelet_scale (float32, overwritten)."""
     _act(x, "x")
-    _act(dy, "dy")
+    _act(dy, "dy", like=x)
     desc = desc_for(x, levels, k)
-    dev = x.device
-    if grads is None:
-        grads = dict(dw_base=torch.empty_like(w_base),
-                     db_base=None if b_base is None else torch.empty_like(b_base),
-                     dw_sub=torch.empty_like(w_sub), dbase_scale=torch.empty_like(base_scale),
-                     dwavelet_scale=torch.empty_like(wavelet_scale))
-    if workspace is None:  # a caller-provided workspace is checked by the library itself
+    ps = _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale)
+    grads = _grads(grads, ps)
+    if workspace is None:  # a caller-provided workspace's size is checked by the library itself
         need = wtconv_workspace_size(desc, OP_BWD_WEIGHT)
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    ws_bytes = _workspace_bytes(workspace, x.device)
     _check(lib().wtconv_bwd_weight(
-        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(_param(w_base, "w_base")),
-        _ptr(_param(b_base, "b_base", True)), _ptr(_param(w_sub, "w_sub")),
-        _ptr(_param(base_scale, "base_scale")), _ptr(_param(wavelet_scale, "wavelet_scale")),
+        ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps),
         _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
-        _ptr(grads["dwavelet_scale"]), _ptr(workspace), workspace.numel(), _stream(stream)))
+        _ptr(grads["dwavelet_scale"]), _ptr(workspace), ws_bytes, _stream(stream)))
     return grads
 
 
@@ -176,24 +217,19 @@ def wtconv_bwd(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, 
     """The whole backward in one call (one kernel over x and dy where the planes
     fit): returns (dx, grads) with grads as from wtconv_bwd_weight."""
     _act(x, "x")
-    _act(dy, "dy")
+    _act(dy, "dy", like=x)
     desc = desc_for(x, levels, k)
-    dev = x.device
-    dx = torch.empty_like(dy) if dx is None else _act(dx, "dx")
-    if grads is None:
-        grads = dict(dw_base=torch.empty_like(w_base),
-                     db_base=None if b_base is None else torch.empty_like(b_base),
-                     dw_sub=torch.empty_like(w_sub), dbase_scale=torch.empty_like(base_scale),
-                     dwavelet_scale=torch.empty_like(wavelet_scale))
-    if workspace is None:  # a caller-provided workspace is checked by the library itself
+    ps = _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale)
+    dx = torch.empty_like(dy) if dx is None else _act(dx, "dx", like=x)
+    grads = _grads(grads, ps)
+    if workspace is None:  # a caller-provided workspace's size is checked by the library itself
         need = wtconv_workspace_size(desc, OP_BWD)
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    ws_bytes = _workspace_bytes(workspace, x.device)
     _check(lib().wtconv_bwd(
-        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(_param(w_base, "w_base")),
-        _ptr(_param(b_base, "b_base", True)), _ptr(_param(w_sub, "w_sub")),
-        _ptr(_param(base_scale, "base_scale")), _ptr(_param(wavelet_scale, "wavelet_scale")), _ptr(dx),
+        ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps), _ptr(dx),
         _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
-        _ptr(grads["dwavelet_scale"]), _ptr(workspace), workspace.numel(), _stream(stream)))
+        _ptr(grads["dwavelet_scale"]), _ptr(workspace), ws_bytes, _stream(stream)))
     return dx, grads
 
 
@@ -203,17 +239,12 @@ def wtconv_bwd_weight_noalloc(x, dy, w_base, b_base, w_sub, base_scale, wavelet_
     library's built-in 4 MiB device scratch replaces the workspace.  For callers
     that cannot allocate device memory; concurrent calls race on the scratch."""
     _act(x, "x")
-    _act(dy, "dy")
+    _act(dy, "dy", like=x)
     desc = desc_for(x, levels, k)
-    if grads is None:
-        grads = dict(dw_base=torch.empty_like(w_base),
-                     db_base=None if b_base is None else torch.empty_like(b_base),
-                     dw_sub=torch.empty_like(w_sub), dbase_scale=torch.empty_like(base_scale),
-                     dwavelet_scale=torch.empty_like(wavelet_scale))
+    ps = _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale)
+    grads = _grads(grads, ps)
     _check(lib().wtconv_bwd_weight_noalloc(
-        ctypes.byref(desc), _ptr(x), _ptr(dy), _ptr(_param(w_base, "w_base")),
-        _ptr(_param(b_base, "b_base", True)), _ptr(_param(w_sub, "w_sub")),
-        _ptr(_param(base_scale, "base_scale")), _ptr(_param(wavelet_scale, "wavelet_scale")),
+        ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps),
         _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
         _ptr(grads["dwavelet_scale"]), _stream(stream)))
     return grads
