@@ -55,6 +55,13 @@
  *     anything is launched.  N = 0 is a valid empty batch.
  *   - Pointers must be aligned to their element size (WTCONV_ERR_MISALIGNED
  *     otherwise); 16-byte alignment enables vector loads and stores.
+ *   - Aliasing: no output (y, dx, a gradient, the workspace) may overlap an
+ *     input (x, dy, a parameter) or another output.  Nothing is computed in
+ *     place: tiles of large planes read halo pixels that neighbouring tiles
+ *     write, and the two passes inside wtconv_bwd's fallback read dy after
+ *     dx is written.  The library cannot see buffer lengths and does not
+ *     check this; overlapping buffers give undefined results (never an
+ *     access outside the buffers).
  */
 #ifndef WTCONV_H_
 #define WTCONV_H_

@@ -21,6 +21,8 @@ WTCONV_OK, WTCONV_ERR_INVALID_ARG, WTCONV_ERR_UNSUPPORTED = 0, 1, 2
 WTCONV_ERR_MISALIGNED, WTCONV_ERR_WORKSPACE, WTCONV_ERR_CUDA = 3, 4, 5
 OP_FWD, OP_BWD_DATA, OP_BWD_WEIGHT, OP_BWD = 0, 1, 2, 3
 DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+PARAM_NAMES = ("w_base", "b_base", "w_sub", "base_scale", "wavelet_scale")
+GRAD_NAMES = ("dw_base", "db_base", "dw_sub", "dbase_scale", "dwavelet_scale")
 
 # entry points declared in include/wtconv.h
 EXPORTS = ("wtconv_workspace_size", "wtconv_fwd", "wtconv_bwd_data", "wtconv_bwd_weight", "wtconv_bwd",
@@ -102,12 +104,17 @@ def _ptr(t):
 
 # The library sees plain pointers, so every size it relies on is checked
 # here: a tensor smaller than the layer implies would be read or written past
-# its end by the kernels.
+# its end by the kernels.  Outputs must not overlap inputs or each other
+# (include/wtconv.h, "Aliasing"), which is checked here too.
+
+
+def _on_cuda(t):
+    return t.is_cuda
 
 
 def _act(t, name, like=None):
     """An activation: contiguous CUDA; `like` (x) fixes shape, dtype and device."""
-    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+    if not (isinstance(t, torch.Tensor) and _on_cuda(t) and t.is_contiguous()):
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if like is not None and (t.shape != like.shape or t.dtype != like.dtype or t.device != like.device):
         raise ValueError(f"{name} must be {tuple(like.shape)} {like.dtype} on {like.device}, "
@@ -122,7 +129,7 @@ def _param(t, name, numel, device, optional=False):
         if optional:
             return None
         raise ValueError(f"{name} is required")
-    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous() and t.dtype == torch.float32):
+    if not (isinstance(t, torch.Tensor) and _on_cuda(t) and t.is_contiguous() and t.dtype == torch.float32):
         raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
     if t.device != device or t.numel() != numel:
         raise ValueError(f"{name} must hold {numel} elements on {device}, got {t.numel()} on {t.device}")
@@ -147,11 +154,10 @@ def _grads(grads, params):
     """The caller's gradient buffers (checked), or new ones shaped like the
     parameters.  Without a bias db_base may be absent or None; a db_base that
     is given still receives the gradient a bias would have (s_base * sum dy)."""
-    names = ("dw_base", "db_base", "dw_sub", "dbase_scale", "dwavelet_scale")
     if grads is None:
-        return {n: None if p is None else torch.empty_like(p) for n, p in zip(names, params)}
+        return {n: None if p is None else torch.empty_like(p) for n, p in zip(GRAD_NAMES, params)}
     C = params[3].numel()
-    for n, p in zip(names, params):
+    for n, p in zip(GRAD_NAMES, params):
         if p is not None:
             _param(grads.get(n), n, p.numel(), p.device)
         elif grads.get(n) is not None:
@@ -160,9 +166,23 @@ def _grads(grads, params):
 
 
 def _workspace_bytes(ws, device):
-    if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.is_contiguous() and ws.device == device):
+    if not (isinstance(ws, torch.Tensor) and _on_cuda(ws) and ws.is_contiguous() and ws.device == device):
         raise ValueError(f"workspace must be a contiguous CUDA tensor on {device}")
     return ws.numel() * ws.element_size()
+
+
+def _disjoint(outs, ins):
+    """Raise if an output's memory overlaps an input's or another output's.
+    outs, ins: (name, tensor or None) pairs."""
+    def span(t):
+        p = t.data_ptr()
+        return p, p + t.numel() * t.element_size()
+    o = [(n, span(t)) for n, t in outs if t is not None and t.numel()]
+    every = o + [(n, span(t)) for n, t in ins if t is not None and t.numel()]
+    for i, (n, (a0, a1)) in enumerate(o):
+        for m, (b0, b1) in every[i + 1:]:
+            if a0 < b1 and b0 < a1:
+                raise ValueError(f"{n} overlaps {m}: outputs may not share memory with inputs or other outputs")
 
 
 def _stream(stream):
@@ -177,6 +197,7 @@ def wtconv_fwd(x, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k, y
     desc = desc_for(x, levels, k)
     ps = _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale)
     y = torch.empty_like(x) if y is None else _act(y, "y", like=x)
+    _disjoint([("y", y)], [("x", x), *zip(PARAM_NAMES, ps)])
     _check(lib().wtconv_fwd(ctypes.byref(desc), _ptr(x), *map(_ptr, ps), _ptr(y), None, 0, _stream(stream)))
     return y
 
@@ -187,6 +208,7 @@ def wtconv_bwd_data(dy, w_base, w_sub, base_scale, wavelet_scale, levels, k, dx=
     desc = desc_for(dy, levels, k)
     wb, _, ws_, sb, sw = _params(dy, levels, k, w_base, None, w_sub, base_scale, wavelet_scale)
     dx = torch.empty_like(dy) if dx is None else _act(dx, "dx", like=dy)
+    _disjoint([("dx", dx)], [("dy", dy), ("w_base", wb), ("w_sub", ws_), ("base_scale", sb), ("wavelet_scale", sw)])
     _check(lib().wtconv_bwd_data(ctypes.byref(desc), _ptr(dy), _ptr(wb), _ptr(ws_), _ptr(sb), _ptr(sw), _ptr(dx),
                                  None, 0, _stream(stream)))
     return dx
@@ -205,6 +227,8 @@ def wtconv_bwd_weight(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, l
         need = wtconv_workspace_size(desc, OP_BWD_WEIGHT)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     ws_bytes = _workspace_bytes(workspace, x.device)
+    _disjoint([*((n, grads.get(n)) for n in GRAD_NAMES), ("workspace", workspace)],
+              [("x", x), ("dy", dy), *zip(PARAM_NAMES, ps)])
     _check(lib().wtconv_bwd_weight(
         ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps),
         _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
@@ -226,6 +250,8 @@ def wtconv_bwd(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, 
         need = wtconv_workspace_size(desc, OP_BWD)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     ws_bytes = _workspace_bytes(workspace, x.device)
+    _disjoint([("dx", dx), *((n, grads.get(n)) for n in GRAD_NAMES), ("workspace", workspace)],
+              [("x", x), ("dy", dy), *zip(PARAM_NAMES, ps)])
     _check(lib().wtconv_bwd(
         ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps), _ptr(dx),
         _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
@@ -243,6 +269,7 @@ def wtconv_bwd_weight_noalloc(x, dy, w_base, b_base, w_sub, base_scale, wavelet_
     desc = desc_for(x, levels, k)
     ps = _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale)
     grads = _grads(grads, ps)
+    _disjoint([(n, grads.get(n)) for n in GRAD_NAMES], [("x", x), ("dy", dy), *zip(PARAM_NAMES, ps)])
     _check(lib().wtconv_bwd_weight_noalloc(
         ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps),
         _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
