@@ -23,8 +23,9 @@
  *
  * The library computes each call on the GPU in one pass over the activations
  * (the pages' "Methodology": the Haar butterflies are recomputed on chip, the
- * synthesis is collapsed into one pass indexed by output-coordinate bits, the
- * scales are folded into the weights).
+ * multi-level synthesis becomes a single sum whose terms are picked by the
+ * bits of each output row and column, the scales are folded into the
+ * weights).
  *
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
