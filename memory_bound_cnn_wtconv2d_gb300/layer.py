@@ -10,6 +10,7 @@ only one of them is needed.
 from __future__ import annotations
 
 import threading
+from collections import OrderedDict
 
 import torch
 
@@ -19,8 +20,14 @@ from . import wtconv as _c
 # reused across steps: the library overwrites every byte it reads, so a
 # workspace needs no clearing, and reusing it spares each backward step a
 # size query (a full launch plan) and an allocation.  Calls on one stream
-# run in order, so sharing a workspace between them is safe.
-_WORKSPACES: dict = {}
+# run in order, so sharing a workspace between them is safe.  The cache keeps
+# the most recently used MAX_WORKSPACES entries, so a process that meets many
+# shapes (varying batch sizes) does not grow it without bound.  Dropping an
+# entry is safe while a kernel may still use it: the workspace was allocated
+# on the stream it serves, and PyTorch's caching allocator hands a freed
+# block only to later work on that stream.
+MAX_WORKSPACES = 64
+_WORKSPACES: "OrderedDict" = OrderedDict()
 _WS_LOCK = threading.Lock()
 
 
@@ -29,11 +36,15 @@ def _workspace(x, levels, k, op):
     key = (x.device, stream.cuda_stream, tuple(x.shape), x.dtype, levels, k, op)
     with _WS_LOCK:
         ws = _WORKSPACES.get(key)
+        if ws is not None:
+            _WORKSPACES.move_to_end(key)
     if ws is None:
         need = _c.wtconv_workspace_size(_c.desc_for(x, levels, k), op)
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
         with _WS_LOCK:
             _WORKSPACES[key] = ws
+            while len(_WORKSPACES) > MAX_WORKSPACES:
+                _WORKSPACES.popitem(last=False)
     return ws
 
 

@@ -171,3 +171,23 @@ def test_refusals_reach_nothing(fake):
     # adjacent, disjoint views of one buffer are accepted
     wtconv.wtconv_fwd(big[:n].view_as(x), *ps, 2, 5, y=big[n:].view_as(x), stream=0)
     assert len(fake.calls) == 1
+
+
+def test_layer_workspace_cache_is_reused_and_bounded(monkeypatch):
+    from memory_bound_cnn_wtconv2d_gb300 import layer as layer_mod
+
+    class Stream:
+        cuda_stream = 7
+
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda device=None: Stream())
+    monkeypatch.setattr(wtconv, "wtconv_workspace_size", lambda desc, op: 1000 + desc.N)
+    monkeypatch.setattr(layer_mod, "_WORKSPACES", type(layer_mod._WORKSPACES)())
+    first = torch.empty(1, 3, 8, 8)
+    ws = layer_mod._workspace(first, 2, 5, wtconv.OP_BWD)
+    assert ws.numel() == 1001 and ws.dtype == torch.uint8
+    assert layer_mod._workspace(first, 2, 5, wtconv.OP_BWD) is ws  # reused, not reallocated
+    assert layer_mod._workspace(first, 2, 5, wtconv.OP_BWD_WEIGHT) is not ws  # one per call kind
+    for n in range(2, 2 + 3 * layer_mod.MAX_WORKSPACES):  # many batch sizes
+        layer_mod._workspace(torch.empty(n, 3, 8, 8), 2, 5, wtconv.OP_BWD)
+        assert layer_mod._workspace(first, 2, 5, wtconv.OP_BWD) is ws  # kept while in use
+    assert len(layer_mod._WORKSPACES) == layer_mod.MAX_WORKSPACES
