@@ -798,6 +798,19 @@ int main(int argc, char** argv) {
             check_fwd(3, 2, H, W, L, K);
             check_bw(3, 2, H, W, L, K);
           }
+  // Very large batches (tens of GB of activations): unit counts, grid splits
+  // and record slots in 32-bit arithmetic.
+  for (g_dtype = 0; g_dtype < 2; ++g_dtype) {
+    check_fwd(4096, 96, 56, 56, 3, 5);
+    check_bw(4096, 96, 56, 56, 3, 5);
+    check_fwd(8192, 768, 7, 7, 2, 5);
+    check_bw(8192, 768, 7, 7, 2, 5);
+  }
+  check_win(1024, 96, 224, 224, 3, 5, 1, 0);
+  check_win(1024, 96, 224, 224, 3, 5, 2, 1);
+  check_bw_win(1024, 96, 224, 224, 3, 5, 1, 0);
+  check_bw_win(512, 64, 512, 512, 2, 5, 2, 1);
+  check_bwf(4096, 96, 56, 56, 3, 5, 0);
   // Windowed plans: every load mode, level count and k on planes of many shapes.
   {
     const int wsh[][2] = {{1, 1}, {7, 9}, {56, 56}, {64, 64}, {100, 100}, {113, 129}, {128, 128}, {150, 150},
