@@ -91,6 +91,14 @@ class WTConv2d(torch.nn.Module):
                  device=None):
         super().__init__()
         C, k, L = channels, kernel_size, levels
+        # the library's limits (include/wtconv.h), checked here so that a bad
+        # layer fails when it is built rather than at its first call
+        if not (isinstance(k, int) and 3 <= k <= 9 and k % 2 == 1):
+            raise ValueError(f"kernel_size must be odd and in [3, 9], got {k}")
+        if not (isinstance(L, int) and 1 <= L <= 8):
+            raise ValueError(f"levels must be in [1, 8], got {L}")
+        if not (isinstance(C, int) and C >= 1):
+            raise ValueError(f"channels must be a positive int, got {C}")
         f = dict(device=device, dtype=torch.float32)
         bound = 1.0 / k
         self.levels, self.k = L, k
@@ -99,6 +107,10 @@ class WTConv2d(torch.nn.Module):
         self.base_scale = torch.nn.Parameter(torch.ones(C, **f))
         self.wavelet_weight = torch.nn.Parameter(torch.empty(L, 4 * C, k, k, **f).uniform_(-bound, bound))
         self.wavelet_scale = torch.nn.Parameter(torch.full((L, 4 * C), 0.1, **f))
+
+    def extra_repr(self):
+        return (f"channels={self.weight.shape[0]}, kernel_size={self.k}, levels={self.levels}, "
+                f"bias={self.bias is not None}")
 
     def forward(self, x):
         return WTConv2dFunction.apply(x, self.weight, self.bias, self.wavelet_weight, self.base_scale,

@@ -191,3 +191,17 @@ def test_layer_workspace_cache_is_reused_and_bounded(monkeypatch):
         layer_mod._workspace(torch.empty(n, 3, 8, 8), 2, 5, wtconv.OP_BWD)
         assert layer_mod._workspace(first, 2, 5, wtconv.OP_BWD) is ws  # kept while in use
     assert len(layer_mod._WORKSPACES) == layer_mod.MAX_WORKSPACES
+
+
+def test_module_checks_its_hyperparameters_at_construction():
+    from memory_bound_cnn_wtconv2d_gb300.layer import WTConv2d
+    m = WTConv2d(4, kernel_size=5, levels=3)
+    assert m.weight.shape == (4, 5, 5) and m.wavelet_weight.shape == (3, 16, 5, 5)
+    assert m.wavelet_scale.shape == (3, 16) and m.bias.shape == (4,)
+    assert "kernel_size=5" in repr(m) and "levels=3" in repr(m)
+    assert WTConv2d(2, kernel_size=9, levels=8, bias=False).bias is None
+    for kw in (dict(kernel_size=4), dict(kernel_size=11), dict(kernel_size=1), dict(levels=0), dict(levels=9)):
+        with pytest.raises(ValueError):
+            WTConv2d(4, **kw)
+    with pytest.raises(ValueError):
+        WTConv2d(0)
