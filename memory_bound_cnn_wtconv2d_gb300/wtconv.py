@@ -84,6 +84,8 @@ def _check(status: int):
 
 
 def make_desc(N, C, H, W, levels, k, dtype) -> WtconvDesc:
+    if isinstance(dtype, torch.dtype) and dtype not in DTYPE_CODES:
+        raise ValueError(f"activations must be float32, float16 or bfloat16, got {dtype}")
     code = DTYPE_CODES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     return WtconvDesc(int(N), int(C), int(H), int(W), int(levels), int(k), code)
 

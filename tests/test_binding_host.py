@@ -163,6 +163,8 @@ def test_refusals_reach_nothing(fake):
         lambda: wtconv.wtconv_bwd(x, dy[:1], *ps, 2, 5, stream=0),
         lambda: wtconv.wtconv_bwd_weight(x, dy, *ps, 2, 5, grads=dict(g, dw_sub=g["dw_sub"][:1]), stream=0),
         lambda: wtconv.wtconv_bwd_weight(x, dy, wb.double(), *ps[1:], 2, 5, stream=0),
+        # an activation type the library does not take
+        lambda: wtconv.wtconv_fwd(x.double(), *ps, 2, 5, stream=0),
     ]
     for i, case in enumerate(cases):
         with pytest.raises(ValueError):
