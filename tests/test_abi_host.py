@@ -150,3 +150,21 @@ def test_fused_backward_argument_checks(L):
     assert L.wtconv_bwd(ctypes.byref(bad), v, v, v, None, v, v, v, v, v, None, v, v, v, v, need, None) == \
         wtconv.WTCONV_ERR_INVALID_ARG
     assert L.wtconv_last_error().decode() != ""
+
+
+def test_binding_argtypes_match_the_header(L):
+    # every prototype's parameter count and pointer-or-integer kind, as the
+    # binding declares them to ctypes
+    from test_binding_host import header_params
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "wtconv.h")).read(), flags=re.S)
+    for name, params in header_params().items():
+        argtypes = getattr(L, name).argtypes
+        assert argtypes is not None and len(argtypes) == len(params), name
+        proto = re.search(r"\b" + name + r"\s*\(([^;{]*?)\)\s*;", src).group(1)
+        for decl, t in zip([a.strip() for a in proto.split(",") if a.strip() not in ("", "void")], argtypes):
+            if "*" in decl:
+                assert t in (ctypes.c_void_p, ctypes.POINTER(wtconv.WtconvDesc)), (name, decl, t)
+            elif decl.startswith("size_t"):
+                assert t is ctypes.c_size_t, (name, decl, t)
+            else:
+                assert t is ctypes.c_int, (name, decl, t)
