@@ -56,6 +56,14 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["unit"] == "ms/layer" and line["higher_is_better"] is False
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    # every key of the bench line's contract, with the reference arm's own values
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["steps"] == 1 and line["warmup"] == 0 and line["ms_per_step"] == line["value"]
+    assert "workload" in line["config"] and line["dtype"] == "f64" and line["vs_baseline"] is None
+    assert {"value", "unit", "cores", "sample", "kind"} <= set(line["cpu_baseline"])
+    assert line["cpu_baseline"]["value"] == line["value"] and line["e2e"]["value"] == line["value"]
 
 
 def test_bench_algorithmic_counts():
