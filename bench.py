@@ -34,7 +34,6 @@ from memory_bound_cnn_wtconv2d_gb300 import synth  # noqa: E402
 METRIC = "WTConv2d fwd+bwd ms/layer and achieved HBM TB/s vs ~8 TB/s peak (1 GB300)"
 WORKLOAD = "stage1"
 ROTATE = 4          # input buffer sets cycled through (4 x 154 MB > 129 MB L2)
-NUM_SMS = 152
 FP32_LANES = 128    # FP32 FMA lanes per SM (measured: 128 FMA/clk/SM)
 SM_MAX_MHZ = 2070.0
 ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
@@ -56,9 +55,8 @@ def fma_per_plane(H, W, L, k):
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
-# kernel of the step, from one ncu capture of the stage-1 layer
-# (profiles/ncu_full_stage1_f32.md), valid only for the kernel sources they
-# were taken on (hash below).
+# kernel of the step, from one ncu capture of the stage-1 layer, valid only
+# for the kernel sources they were taken on (hash below).
 MEASURED_TRAFFIC = {
     "csrc_sha256": "6c39dc4bd66c8f12bfda3ce6f0c0a1ae03a70b52a0b144355e07f1185b524d4c",
     "workload": "stage1",
@@ -603,25 +601,30 @@ PAGES_CONTEXT = ("pages (RTX A6000, context only): training 3.71-4.35x fp32 / 2.
 
 
 def run_reference(args, world, rank):
-    """The oracle on the host cores, each step a bounded sample of the workload."""
+    """The oracle on the host cores: every step is one fwd+bwd of the float64
+    oracle over the whole workload (all images), split over all host cores."""
     if rank != 0:
         return None
+    import platform
+
     import oracle
     oracle.build()
     inp = synth.workload(WORKLOAD)
-    n_img = 1
+    workers = max(1, min(os.cpu_count() or 1, inp.N))
     for _ in range(args.warmup):
-        time_oracle(inp, n_img)
-    times = [time_oracle(inp, n_img) for _ in range(args.steps)]
-    ms_layer = 1e3 * sum(times) / len(times) * (inp.N / n_img)
-    sample = f"{n_img} of {inp.N} images per step ({n_img * inp.C} planes), scaled to the full batch"
+        time_oracle_parallel(inp, workers)
+    times = [time_oracle_parallel(inp, workers) for _ in range(args.steps)]
+    ms_layer = 1e3 * sum(times) / len(times)
+    cpu = platform.processor() or platform.machine()
+    sample = (f"the whole workload every step: fwd+bwd over all {inp.N} images ({inp.N * inp.C} planes), "
+              f"split over {workers} threads on {cpu}")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(ms_layer, 3), "unit": "ms/layer",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_layer, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) activations, random-init weights)",
-        "config": workload_config(inp),
-        "cpu_baseline": {"value": round(ms_layer, 3), "unit": "ms/layer", "cores": 1, "kind": "oracle",
+        "config": workload_config(inp) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "cpu_baseline": {"value": round(ms_layer, 3), "unit": "ms/layer", "cores": workers, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(ms_layer, 3), "unit": "ms/layer", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -789,12 +792,13 @@ def run_ours(args, world, rank, local):
     hbm_tbs = step_bytes / (ms_step * 1e-3) / 1e12
     dom = max(avg, key=avg.get)
     clocks = clk.summary()
-    alu_peak = NUM_SMS * FP32_LANES * 2 * SM_MAX_MHZ * 1e6 / 1e12  # TFLOP/s at the maximum SM clock
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = num_sms * FP32_LANES * 2 * SM_MAX_MHZ * 1e6 / 1e12  # TFLOP/s at the maximum SM clock
     achieved_alu = 2 * fma_kernel[dom] / (avg[dom] * 1e-3) / 1e12
     roofline = {"bound": "alu", "kernel": dom, "achieved": round(achieved_alu, 2), "peak": round(alu_peak, 2),
                 "unit": "TFLOP/s", "frac": round(achieved_alu / alu_peak, 4), "traffic": measured_traffic(dom),
                 "traffic_unit": "bytes per launch (ncu dram read+write)",
-                "peak_source": f"{NUM_SMS} SMs x {FP32_LANES} FP32 FMA/clk x 2 x {SM_MAX_MHZ:.0f} MHz",
+                "peak_source": f"{num_sms} SMs x {FP32_LANES} FP32 FMA/clk x 2 x {SM_MAX_MHZ:.0f} MHz",
                 "algorithmic_fma_per_launch": fma_kernel[dom],
                 "timed_span": "bwd = the fused backward kernel and its dW finalize (one C call)" if dom == "bwd"
                 else "the forward kernel"}

@@ -103,7 +103,8 @@ typedef struct {
  * none, or if desc is invalid; the parameter-gradient grid, and with it the
  * size, follows the device's occupancy).  The workspace must be 256-byte
  * aligned; its contents need not be initialised and are garbage after the
- * call. */
+ * call.  Packaging: the pages define no such call (their layer is an
+ * operator, not an API); it exists because the library never allocates. */
 size_t wtconv_workspace_size(const wtconv_desc_t* desc, int op);
 
 /* Forward: y = WTConv2d(x).  b_base may be NULL (no bias).
@@ -129,6 +130,12 @@ wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const
 /* Parameter gradients for upstream gradient dy at input x:
  *   dw_base[C,k,k], db_base[C] (may be NULL), dw_sub[L,4C,k,k],
  *   dbase_scale[C], dwavelet_scale[L,4C]   (float32, overwritten).
+ * The summary's "Key contributions" report that the fused implementation
+ * reproduces all parameter gradients; with the scales folded into the
+ * weights ("Methodology"), each follows from one correlation sum per weight
+ * tap: dW = s * G, ds = <W, G> (+ b * sum dy for the base scale),
+ * db = s_base * sum dy, where G correlates the level-l Haar bands of dy with
+ * those of x (level 0: the planes themselves).
  * b_base (may be NULL) enters dbase_scale.  Partial correlation sums are
  * reduced in a deterministic order through the workspace, which must hold
  * wtconv_workspace_size(desc, WTCONV_OP_BWD_WEIGHT) bytes. */
@@ -169,9 +176,12 @@ wtconv_status_t wtconv_bwd(const wtconv_desc_t* desc, const void* x, const void*
  * process exits.  Layers needing more than 4 MiB of scratch (see
  * wtconv_workspace_size) return WTCONV_ERR_UNSUPPORTED with a message; use
  * wtconv_bwd_weight for them.  Nothing is allocated by this call.
- * The first call on a device looks up the array's device address on the
- * current device (cudaGetSymbolAddress); make that first call before any
- * stream capture.  All calls share the one array and it keeps the last
+ * Every call outside stream capture looks up the array's device address on
+ * the current device (cudaGetSymbolAddress), so the address stays right after
+ * a cudaDeviceReset; a call inside a capture uses the address kept from the
+ * last call outside one, so make a first call on each device before any
+ * capture (and again after a reset), else the call returns
+ * WTCONV_ERR_INVALID_ARG.  All calls share the one array and it keeps the last
  * call's contents (every entry is rewritten before use, so nothing needs
  * clearing): calls that can overlap on the GPU -- on different streams, or
  * from different host threads -- race on it and must be serialised by the
@@ -182,14 +192,16 @@ wtconv_status_t wtconv_bwd_weight_noalloc(const wtconv_desc_t* desc, const void*
                                           float* dw_base, float* db_base, float* dw_sub,
                                           float* dbase_scale, float* dwavelet_scale, void* stream);
 
-/* Static name of a status code. */
+/* Static name of a status code.  Packaging (no counterpart in the pages). */
 const char* wtconv_status_string(wtconv_status_t status);
 
-/* Thread-local description of the last failure on this thread ("" if none). */
+/* Thread-local description of the last failure on this thread ("" if none).
+ * Packaging (no counterpart in the pages). */
 const char* wtconv_last_error(void);
 
-/* Number of in-kernel waits on the current device that gave up since the
- * previous call, then resets the count.  The kernels wait for their own
+/* Packaging (no counterpart in the pages): the number of in-kernel waits on
+ * the current device that gave up since the previous call, then resets the
+ * count.  The kernels wait for their own
  * asynchronous (TMA and bulk) plane copies with a time limit of about a second; a
  * wait that runs out records itself here and the kernel stops early (its
  * outputs are then invalid).  0 in normal operation.  Synchronises the

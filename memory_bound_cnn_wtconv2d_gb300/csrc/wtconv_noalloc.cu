@@ -31,10 +31,13 @@ static __device__ __align__(256) float g_scratch[kScratchBytes / sizeof(float)];
 std::mutex g_mu;
 float* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_scratch on the current device, looked up once per
-// device.  In host code `g_scratch` names a host-side shadow, not device
-// memory, so it must never be passed to a kernel directly.
-wtconv_status_t scratch_for_current_device(float** out) {
+// Device address of g_scratch on the current device.  In host code
+// `g_scratch` names a host-side shadow, not device memory, so it must never be
+// passed to a kernel directly.  Outside stream capture the address is looked
+// up on every call (a cudaDeviceReset reloads the device code, which may move
+// the array) and kept per device; inside a capture, where the lookup could
+// load code, the kept address from an earlier call is used.
+wtconv_status_t scratch_for_current_device(cudaStream_t stream, float** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
@@ -47,8 +50,17 @@ wtconv_status_t scratch_for_current_device(float** out) {
     wt::set_last_error("wtconv_bwd_weight_noalloc: device ordinal beyond the supported 64 devices");
     return WTCONV_ERR_UNSUPPORTED;
   }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "wtconv_bwd_weight_noalloc: cudaStreamIsCapturing failed: %s",
+             cudaGetErrorString(e));
+    wt::set_last_error(msg);
+    return WTCONV_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -59,6 +71,10 @@ wtconv_status_t scratch_for_current_device(float** out) {
       return WTCONV_ERR_CUDA;
     }
     g_scratch_ptr[dev] = static_cast<float*>(p);
+  } else if (g_scratch_ptr[dev] == nullptr) {
+    wt::set_last_error("wtconv_bwd_weight_noalloc: the first call on a device must come before any stream "
+                       "capture (it looks up the scratch array's device address)");
+    return WTCONV_ERR_INVALID_ARG;
   }
   *out = g_scratch_ptr[dev];
   return WTCONV_OK;
@@ -88,7 +104,7 @@ extern "C" wtconv_status_t wtconv_bwd_weight_noalloc(
                              dw_sub, dbase_scale, dwavelet_scale, nullptr, 0, stream);
   }
   float* scratch = nullptr;
-  const wtconv_status_t st = scratch_for_current_device(&scratch);
+  const wtconv_status_t st = scratch_for_current_device(static_cast<cudaStream_t>(stream), &scratch);
   if (st != WTCONV_OK) return st;
   // Every partial-sum record is written before it is read, so the stale
   // contents left by an earlier call need no clearing.

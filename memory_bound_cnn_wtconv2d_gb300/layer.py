@@ -39,7 +39,8 @@ def _workspace(x, levels, k, op):
         if ws is not None:
             _WORKSPACES.move_to_end(key)
     if ws is None:
-        need = _c.wtconv_workspace_size(_c.desc_for(x, levels, k), op)
+        with _c._device_ctx(x.device):  # the size follows that device's occupancy
+            need = _c.wtconv_workspace_size(_c.desc_for(x, levels, k), op)
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
         with _WS_LOCK:
             _WORKSPACES[key] = ws

@@ -187,10 +187,20 @@ def _disjoint(outs, ins):
                 raise ValueError(f"{n} overlaps {m}: outputs may not share memory with inputs or other outputs")
 
 
-def _stream(stream):
+def _stream(stream, device):
+    """The stream handle for a call on `device`: the given stream, else that
+    device's current torch stream."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _device_ctx(device):
+    """Makes `device` the current CUDA device for the duration of a call: the
+    library launches on the current device and picks per-device state (plan
+    caches, the no-alloc scratch) by it, so it must be the device that holds
+    the tensors."""
+    return torch.cuda.device(device)
 
 
 def wtconv_fwd(x, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k, y=None, stream=None):
@@ -200,7 +210,9 @@ def wtconv_fwd(x, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k, y
     ps = _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale)
     y = torch.empty_like(x) if y is None else _act(y, "y", like=x)
     _disjoint([("y", y)], [("x", x), *zip(PARAM_NAMES, ps)])
-    _check(lib().wtconv_fwd(ctypes.byref(desc), _ptr(x), *map(_ptr, ps), _ptr(y), None, 0, _stream(stream)))
+    with _device_ctx(x.device):
+        _check(lib().wtconv_fwd(ctypes.byref(desc), _ptr(x), *map(_ptr, ps), _ptr(y), None, 0,
+                                _stream(stream, x.device)))
     return y
 
 
@@ -211,8 +223,9 @@ def wtconv_bwd_data(dy, w_base, w_sub, base_scale, wavelet_scale, levels, k, dx=
     wb, _, ws_, sb, sw = _params(dy, levels, k, w_base, None, w_sub, base_scale, wavelet_scale)
     dx = torch.empty_like(dy) if dx is None else _act(dx, "dx", like=dy)
     _disjoint([("dx", dx)], [("dy", dy), ("w_base", wb), ("w_sub", ws_), ("base_scale", sb), ("wavelet_scale", sw)])
-    _check(lib().wtconv_bwd_data(ctypes.byref(desc), _ptr(dy), _ptr(wb), _ptr(ws_), _ptr(sb), _ptr(sw), _ptr(dx),
-                                 None, 0, _stream(stream)))
+    with _device_ctx(dy.device):
+        _check(lib().wtconv_bwd_data(ctypes.byref(desc), _ptr(dy), _ptr(wb), _ptr(ws_), _ptr(sb), _ptr(sw), _ptr(dx),
+                                     None, 0, _stream(stream, dy.device)))
     return dx
 
 
@@ -226,15 +239,17 @@ def wtconv_bwd_weight(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, l
     ps = _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale)
     grads = _grads(grads, ps)
     if workspace is None:  # a caller-provided workspace's size is checked by the library itself
-        need = wtconv_workspace_size(desc, OP_BWD_WEIGHT)
+        with _device_ctx(x.device):  # the size follows the device's occupancy
+            need = wtconv_workspace_size(desc, OP_BWD_WEIGHT)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     ws_bytes = _workspace_bytes(workspace, x.device)
     _disjoint([*((n, grads.get(n)) for n in GRAD_NAMES), ("workspace", workspace)],
               [("x", x), ("dy", dy), *zip(PARAM_NAMES, ps)])
-    _check(lib().wtconv_bwd_weight(
-        ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps),
-        _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
-        _ptr(grads["dwavelet_scale"]), _ptr(workspace), ws_bytes, _stream(stream)))
+    with _device_ctx(x.device):
+        _check(lib().wtconv_bwd_weight(
+            ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps),
+            _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
+            _ptr(grads["dwavelet_scale"]), _ptr(workspace), ws_bytes, _stream(stream, x.device)))
     return grads
 
 
@@ -249,15 +264,17 @@ def wtconv_bwd(x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, 
     dx = torch.empty_like(dy) if dx is None else _act(dx, "dx", like=x)
     grads = _grads(grads, ps)
     if workspace is None:  # a caller-provided workspace's size is checked by the library itself
-        need = wtconv_workspace_size(desc, OP_BWD)
+        with _device_ctx(x.device):  # the size follows the device's occupancy
+            need = wtconv_workspace_size(desc, OP_BWD)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     ws_bytes = _workspace_bytes(workspace, x.device)
     _disjoint([("dx", dx), *((n, grads.get(n)) for n in GRAD_NAMES), ("workspace", workspace)],
               [("x", x), ("dy", dy), *zip(PARAM_NAMES, ps)])
-    _check(lib().wtconv_bwd(
-        ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps), _ptr(dx),
-        _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
-        _ptr(grads["dwavelet_scale"]), _ptr(workspace), ws_bytes, _stream(stream)))
+    with _device_ctx(x.device):
+        _check(lib().wtconv_bwd(
+            ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps), _ptr(dx),
+            _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
+            _ptr(grads["dwavelet_scale"]), _ptr(workspace), ws_bytes, _stream(stream, x.device)))
     return dx, grads
 
 
@@ -272,10 +289,11 @@ def wtconv_bwd_weight_noalloc(x, dy, w_base, b_base, w_sub, base_scale, wavelet_
     ps = _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale)
     grads = _grads(grads, ps)
     _disjoint([(n, grads.get(n)) for n in GRAD_NAMES], [("x", x), ("dy", dy), *zip(PARAM_NAMES, ps)])
-    _check(lib().wtconv_bwd_weight_noalloc(
-        ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps),
-        _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
-        _ptr(grads["dwavelet_scale"]), _stream(stream)))
+    with _device_ctx(x.device):
+        _check(lib().wtconv_bwd_weight_noalloc(
+            ctypes.byref(desc), _ptr(x), _ptr(dy), *map(_ptr, ps),
+            _ptr(grads["dw_base"]), _ptr(grads["db_base"]), _ptr(grads["dw_sub"]), _ptr(grads["dbase_scale"]),
+            _ptr(grads["dwavelet_scale"]), _stream(stream, x.device)))
     return grads
 
 

@@ -136,3 +136,59 @@ def haar_synthesis(bands: np.ndarray, H: int, W: int) -> np.ndarray:
     out = np.empty((H, W))
     _lib().oracle_haar_synthesis(_p(b), Hh, Wh, _p(out), H, W)
     return out
+
+
+def _slice(inp, a, b):
+    """The layer problem restricted to images a..b-1 (parameters shared)."""
+    import copy
+    part = copy.copy(inp)
+    part.N = b - a
+    part.x = inp.x[a:b]
+    part.dy = inp.dy[a:b]
+    return part
+
+
+def _bounds(N, workers):
+    workers = max(1, min(int(workers), N))
+    return [N * i // workers for i in range(workers + 1)]
+
+
+def fwd_parallel(inp, workers: int | None = None) -> np.ndarray:
+    """``fwd`` over the batch split into ``workers`` image slices, each run by
+    its own thread (the C calls release the interpreter lock).  Every image is
+    computed by the same code as ``fwd``; only the batch is cut."""
+    import concurrent.futures
+    workers = workers or os.cpu_count() or 1
+    if inp.N == 0:
+        return fwd(inp)
+    _lib()
+    b = _bounds(inp.N, workers)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(b) - 1) as ex:
+        parts = list(ex.map(lambda i: fwd(_slice(inp, b[i], b[i + 1])), range(len(b) - 1)))
+    return np.concatenate(parts, axis=0)
+
+
+def bwd_parallel(inp, workers: int | None = None) -> dict:
+    """``bwd`` over image slices run in threads: dx is the concatenation of the
+    slices' dx; each parameter gradient is a sum over the images of the batch
+    (the layer's parameters are shared by every image, and the unfolded
+    gradients are linear in the correlation sums), so the slices' gradients
+    are added in slice order, in float64."""
+    import concurrent.futures
+    workers = workers or os.cpu_count() or 1
+    if inp.N == 0:
+        return bwd(inp)
+    _lib()
+    b = _bounds(inp.N, workers)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(b) - 1) as ex:
+        parts = list(ex.map(lambda i: bwd(_slice(inp, b[i], b[i + 1])), range(len(b) - 1)))
+    out = {"dx": np.concatenate([p["dx"] for p in parts], axis=0)}
+    for name in ("dw_base", "db_base", "dw_sub", "dbase_scale", "dwavelet_scale"):
+        if parts[0][name] is None:
+            out[name] = None
+            continue
+        acc = parts[0][name].copy()
+        for p in parts[1:]:
+            acc += p[name]
+        out[name] = acc
+    return out

@@ -34,12 +34,16 @@ def header_params():
 class FakeLib:
     def __init__(self):
         self.calls = []
+        self.current = None  # the device the binding made current, as the library would see it
 
     def _record(name):
         def call(self, *args):
             self.calls.append((name, args))
+            self.devices.append(self.current)
             return 0
         return call
+
+    devices = None
 
     wtconv_fwd = _record("wtconv_fwd")
     wtconv_bwd_data = _record("wtconv_bwd_data")
@@ -53,9 +57,21 @@ class FakeLib:
 
 @pytest.fixture
 def fake(monkeypatch):
+    import contextlib
     lib = FakeLib()
+    lib.devices = []
+
+    @contextlib.contextmanager
+    def device_ctx(device):  # records the device made current around each call
+        prev, lib.current = lib.current, device
+        try:
+            yield
+        finally:
+            lib.current = prev
+
     monkeypatch.setattr(wtconv, "_LIB", lib)
     monkeypatch.setattr(wtconv, "_on_cuda", lambda t: True)
+    monkeypatch.setattr(wtconv, "_device_ctx", device_ctx)
     return lib
 
 
@@ -127,6 +143,19 @@ def test_arguments_reach_the_library_in_header_order(fake):
     assert fake.calls[-1][1][-2] == 4096
 
 
+def test_every_call_runs_with_the_tensors_device_current(fake):
+    # the library launches on the current device, so the binding makes the
+    # activations' device current around every call (and the workspace query)
+    inp, x, dy, ps = layer()
+    wtconv.wtconv_fwd(x, *ps, 2, 5, stream=0)
+    wtconv.wtconv_bwd_data(dy, ps[0], ps[2], ps[3], ps[4], 2, 5, stream=0)
+    wtconv.wtconv_bwd_weight(x, dy, *ps, 2, 5, stream=0)
+    wtconv.wtconv_bwd(x, dy, *ps, 2, 5, stream=0)
+    wtconv.wtconv_bwd_weight_noalloc(x, dy, *ps, 2, 5, stream=0)
+    assert len(fake.devices) == 5 and all(d == x.device for d in fake.devices)
+    assert fake.current is None  # restored after each call
+
+
 def test_no_bias_and_depthwise_weight_layout(fake):
     inp, x, dy, ps = layer(bias=False)
     wb, bb, wsub, sb, sw = ps
@@ -182,6 +211,8 @@ def test_layer_workspace_cache_is_reused_and_bounded(monkeypatch):
         cuda_stream = 7
 
     monkeypatch.setattr(torch.cuda, "current_stream", lambda device=None: Stream())
+    import contextlib
+    monkeypatch.setattr(wtconv, "_device_ctx", lambda device: contextlib.nullcontext())
     monkeypatch.setattr(wtconv, "wtconv_workspace_size", lambda desc, op: 1000 + desc.N)
     monkeypatch.setattr(layer_mod, "_WORKSPACES", type(layer_mod._WORKSPACES)())
     first = torch.empty(1, 3, 8, 8)
