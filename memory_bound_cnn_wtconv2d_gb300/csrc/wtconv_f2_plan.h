@@ -63,8 +63,14 @@ inline std::vector<int> strip_offsets(int P, int nb, int A, int T, int stride, i
 // enumeration's window loads have the fewest bank conflicts (ties: least
 // memory).  rows: allocated rows per band.
 inline void pick_strides(int P, int nb, int A, int T, int rows, int min_stride, int& stride, int& band,
-                         int& plane) {
+                         int& plane, bool tight = false) {
   const int s0 = rup(min_stride, 4);
+  if (tight) {  // the smallest layout, whatever its conflicts
+    stride = s0;
+    band = rows * s0;
+    plane = nb * band;
+    return;
+  }
   long best = -1;
   int bs = s0;
   for (int s = s0; s < s0 + 32; s += 4) {
@@ -95,7 +101,9 @@ inline void pick_strides(int P, int nb, int A, int T, int rows, int min_stride, 
 }
 
 // Shared-memory layout of a plan for P planes per unit; returns the bytes.
-inline int layout(WtF2Plan& pl, int P) {
+// tight: 0 = conflict-free strides everywhere; 1 = the smallest Z1 layout;
+// 2 = also the smallest B1 layout; 3 = also the smallest X layout.
+inline int layout(WtF2Plan& pl, int P, int tight = 0) {
   const int R = pl.K / 2, L = pl.L, NV = f2_nv(pl.K);
   const int es = pl.dtype == 0 ? 4 : 2;
   pl.P = P;
@@ -111,7 +119,7 @@ inline int layout(WtF2Plan& pl, int P) {
     WtF2Buf& X = pl.X;
     X.rows = F2_SA * pl.A[0] + 2 * R;
     const int ms = std::max(4 * (pl.T[0] - 1) + 4 * NV, pl.W + 2 * R);
-    pick_strides(P, 1, pl.A[0], pl.T[0], X.rows, ms, X.stride, X.band, X.plane);
+    pick_strides(P, 1, pl.A[0], pl.T[0], X.rows, ms, X.stride, X.band, X.plane, tight >= 3);
     X.off = off;
     pl.xslot = rup(P * X.plane, 32);
     off += 2 * pl.xslot;
@@ -122,7 +130,7 @@ inline int layout(WtF2Plan& pl, int P) {
     B.rows = F2_SA * pl.A[l] + 2 * R;
     const int ms = std::max(4 * (pl.T[l] - 1) + 4 * NV, pl.Ws[l] + 2 * R);
     if (l == 1) {
-      pick_strides(P, 4, pl.A[1], pl.T[1], B.rows, ms, B.stride, B.band, B.plane);
+      pick_strides(P, 4, pl.A[1], pl.T[1], B.rows, ms, B.stride, B.band, B.plane, tight >= 2);
     } else {
       B.stride = rup(ms, 4);
       B.band = B.rows * B.stride;
@@ -138,7 +146,7 @@ inline int layout(WtF2Plan& pl, int P) {
     if (l == 1) {
       Z.rows = std::max(F2_SA * pl.A[1], ((F2_SA * pl.A[0] - 1) >> 1) + 1);
       const int ms = std::max(4 * pl.T[1], 2 * pl.T[0]);
-      pick_strides(P, 4, pl.A[1], pl.T[1], Z.rows, ms, Z.stride, Z.band, Z.plane);
+      pick_strides(P, 4, pl.A[1], pl.T[1], Z.rows, ms, Z.stride, Z.band, Z.plane, tight >= 1);
     } else {
       Z.rows = F2_SA * pl.A[l];
       Z.stride = rup(4 * pl.T[l], 4);
@@ -219,16 +227,19 @@ bool plan(WtF2Plan& pl, int N, int C, int H, int W, int L, int K, int dtype, int
   pl.na = pl.nbh * pl.nbw;
   // per-SM budget for two CTAs (1 KB of each CTA's shared memory is reserved)
   const int budget = std::min(smem_per_sm / 2 - 1024 - 64, max_smem_cta);
-  if (layout(pl, 1) > budget) return false;
+  // the least tight layout that fits one plane per unit
+  int tight = 0;
+  while (tight <= 3 && layout(pl, 1, tight) > budget) ++tight;
+  if (tight > 3) return false;
   const int pmax = std::max(1, std::min(N, 64));
   int bestP = 1;
   double best = -1;
   for (int P = 1; P <= pmax; ++P) {
-    if (layout(pl, P) > budget) break;
+    if (layout(pl, P, tight) > budget) break;
     const double c = unit_cost(pl, P) / P;
     if (best < 0 || c < best * 0.98) best = c, bestP = P;
   }
-  layout(pl, bestP);
+  layout(pl, bestP, tight);
   pl.G = cdiv(N, bestP);
   pl.units = C * pl.G;
   pl.d_n1 = mkdiv(pl.n1);
