@@ -114,11 +114,12 @@ inline int layout(WtF2Plan& pl, int P, int tight = 0) {
   pl.raw_off = 0;
   pl.raw_slot = rup(P * pl.raw_pb, 128) / 4;
   off = 2 * pl.raw_slot;
-  // X: float32 planes, margin R, rows covering the final strips' windows
+  // X: float32 planes, R zero rows above and below, 4 zero columns left and
+  // at least R right; rows cover the final strips' windows
   {
     WtF2Buf& X = pl.X;
     X.rows = F2_SA * pl.A[0] + 2 * R;
-    const int ms = std::max(4 * (pl.T[0] - 1) + 4 * NV, pl.W + 2 * R);
+    const int ms = std::max(4 * (pl.T[0] - 1) + 4 * NV, 4 + pl.W + R);
     pick_strides(P, 1, pl.A[0], pl.T[0], X.rows, ms, X.stride, X.band, X.plane, tight >= 3);
     X.off = off;
     pl.xslot = rup(P * X.plane, 32);
@@ -127,7 +128,7 @@ inline int layout(WtF2Plan& pl, int P, int tight = 0) {
   // bands of every level, margin R
   for (int l = 1; l <= L; ++l) {
     WtF2Buf& B = pl.B[l];
-    B.rows = F2_SA * pl.A[l] + 2 * R;
+    B.rows = (l == 1 ? F2_SA : F2_SAC) * pl.A[l] + 2 * R;
     const int ms = std::max(4 * (pl.T[l] - 1) + 4 * NV, pl.Ws[l] + 2 * R);
     if (l == 1) {
       pick_strides(P, 4, pl.A[1], pl.T[1], B.rows, ms, B.stride, B.band, B.plane, tight >= 2);
@@ -145,10 +146,12 @@ inline int layout(WtF2Plan& pl, int P, int tight = 0) {
     WtF2Buf& Z = pl.Z[l];
     if (l == 1) {
       Z.rows = std::max(F2_SA * pl.A[1], ((F2_SA * pl.A[0] - 1) >> 1) + 1);
-      const int ms = std::max(4 * pl.T[1], 2 * pl.T[0]);
+      // written at buffer columns zo .. 4*T1 - 1 + zo; read up to level-1
+      // column (4*T0 - sh - 1) >> 1, plus zo
+      const int ms = std::max(4 * pl.T[1] + pl.zo, ((4 * pl.T[0] - f2_sh(pl.K) - 1) >> 1) + 1 + pl.zo + 1);
       pick_strides(P, 4, pl.A[1], pl.T[1], Z.rows, ms, Z.stride, Z.band, Z.plane, tight >= 1);
     } else {
-      Z.rows = F2_SA * pl.A[l];
+      Z.rows = F2_SAC * pl.A[l];
       Z.stride = rup(4 * pl.T[l], 4);
       Z.band = Z.rows * Z.stride;
       Z.plane = 4 * Z.band;
@@ -169,7 +172,7 @@ inline int layout(WtF2Plan& pl, int P, int tight = 0) {
   {
     WtF2Buf& R1 = pl.RC[1];
     R1.rows = std::max(pl.Hs[1], ((F2_SA * pl.A[0] - 1) >> 1) + 1);
-    R1.stride = rup(std::max(pl.Ws[1], 2 * pl.T[0]), 4);
+    R1.stride = rup(std::max(pl.Ws[1] + pl.zo, ((4 * pl.T[0] - f2_sh(pl.K) - 1) >> 1) + 1 + pl.zo + 1), 4);
     R1.band = R1.rows * R1.stride;
     R1.plane = R1.band;
     R1.off = off;
@@ -190,7 +193,7 @@ inline int layout(WtF2Plan& pl, int P, int tight = 0) {
 inline double unit_cost(const WtF2Plan& pl, int P) {
   const double strip = 25.0 * 4 * F2_SA * 1.15;  // a strip's FMAs and overhead, issue slots
   const double back = (cdiv(P * pl.n1, F2_NB) + cdiv(P * pl.nf, F2_NB)) * strip;
-  double front = cdiv(P * pl.na, F2_NF) * 90.0 + cdiv(P * pl.nco, F2_NF) * strip;
+  double front = cdiv(P * pl.na, F2_NF) * 90.0 + cdiv(P * pl.nco, F2_NF) * strip * F2_SAC / F2_SA;
   for (int l = 3; l <= pl.L; ++l) front += cdiv(P * pl.Hs[l] * pl.Ws[l], F2_NF) * 40.0 + 60.0;
   for (int l = 2; l <= pl.L; ++l) front += cdiv(P * pl.Hs[l] * pl.Ws[l], F2_NF) * 40.0 + 60.0;
   return std::max(back, front) + 300.0;
@@ -212,9 +215,10 @@ bool plan(WtF2Plan& pl, int N, int C, int H, int W, int L, int K, int dtype, int
     pl.Ws[l] = (pl.Ws[l - 1] + 1) / 2;
   }
   pl.A[0] = cdiv(H, F2_SA);
-  pl.T[0] = cdiv(W, 4);
+  pl.T[0] = cdiv(W + f2_sh(K), 4);
+  pl.zo = f2_zo(K);
   for (int l = 1; l <= L; ++l) {
-    pl.A[l] = cdiv(pl.Hs[l], F2_SA);
+    pl.A[l] = cdiv(pl.Hs[l], l == 1 ? F2_SA : F2_SAC);
     pl.T[l] = cdiv(pl.Ws[l], 4);
   }
   pl.n1 = 4 * pl.A[1] * pl.T[1];

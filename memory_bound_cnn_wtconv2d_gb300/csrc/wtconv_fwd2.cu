@@ -40,11 +40,24 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(mbar)) : "memory");
 }
 
+// One try_wait that may suspend the thread until the phase completes or
+// about `hint_ns` nanoseconds pass; a suspended warp issues nothing, so the
+// warps that are still working keep the issue slots.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* mbar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(mbar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of parity `parity` of mbar to complete, for at most
 // 2^shift clock cycles.  Returns false if it gave up.
 __device__ __forceinline__ bool f2_wait(uint64_t* mbar, uint32_t parity, int shift) {
   const long long t0 = clock64();
-  while (!mbar_try_wait(mbar, parity)) {
+  while (!mbar_try_wait_hint(mbar, parity, 100000u)) {
     if (clock64() - t0 > (1ll << shift)) return false;
   }
   return true;
@@ -53,17 +66,17 @@ __device__ __forceinline__ bool f2_wait(uint64_t* mbar, uint32_t parity, int shi
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 
 // acc[o][j] += sum_{du,dv} w[du][dv] * win[(o + du) * S + j + dv] for a strip
-// of F2_SA x 4 outputs; `win` is 16-byte aligned, rows are read as NV float4s.
-template <int K>
+// of SA x 4 outputs; `win` is 16-byte aligned, rows are read as NV float4s.
+template <int K, int SA = F2_SA>
 __device__ __forceinline__ void f2_strip(const float* __restrict__ win, int S, const float (&w)[K * K],
-                                         float (&acc)[F2_SA][4]) {
+                                         float (&acc)[SA][4]) {
   constexpr int NV = (K + 6) / 4;
 #pragma unroll
-  for (int a = 0; a < F2_SA + K - 1; ++a) {
+  for (int a = 0; a < SA + K - 1; ++a) {
     float seg[4 * NV];
     lds_row<NV>(win + a * S, seg);
 #pragma unroll
-    for (int o = 0; o < F2_SA; ++o) {
+    for (int o = 0; o < SA; ++o) {
       const int du = a - o;
       if (du >= 0 && du < K) {
 #pragma unroll
@@ -109,6 +122,8 @@ __global__ void __launch_bounds__(F2_NT, 2)
   float* const sm = align_smem128(sm_raw);
   constexpr int R = K / 2;
   constexpr int KK = K * K;
+  constexpr int SH = (4 - R) & 3;       // final strips' left shift (f2_sh)
+  constexpr int ZO = SH == 2 ? 1 : 0;   // Z1 / R1 column offset (f2_zo)
   const int tid = threadIdx.x;
   const int C = pl.C, L = pl.L, P = pl.P, H = pl.H, W = pl.W;
   const int u0 = (int)((long long)pl.units * blockIdx.x / gridDim.x);
@@ -174,7 +189,7 @@ __global__ void __launch_bounds__(F2_NT, 2)
     };
     issue(0);
     if (nu > 1) issue(1);
-    int wch[2] = {-1, -1};  // channel whose folded weights sit in each slot
+    int wch0 = -1, wch1 = -1;  // channel whose folded weights sit in slot 0 / 1
     for (int v = 0; v < nu; ++v) {
       const int u = u0 + v;
       const int c = wt_fdiv(u, pl.d_G);
@@ -204,9 +219,10 @@ __global__ void __launch_bounds__(F2_NT, 2)
         return;
       }
       float* const wsl = sm + pl.w_off + slot * pl.wslot;
-      if (wch[slot] != c) {
+      if ((slot ? wch1 : wch0) != c) {
         stage_weights<K, ROT>(wsl, pl.wb, L, C, c, w_base, w_sub, s_base, s_w, ft, F2_NF);
-        wch[slot] = c;
+        if (slot) wch1 = c;
+        else wch0 = c;
       }
       // (1) analysis of 4x4 input blocks: the float32 plane X, the level-1
       // bands B1 and (L >= 2) the level-2 bands B2.
@@ -232,15 +248,14 @@ __global__ void __launch_bounds__(F2_NT, 2)
 #pragma unroll
               for (int e = 0; e < 4; ++e) v4[a][e] = raw_at<T>(rp, i0 + a, j0 + e, H, W);
           }
-          // float32 input plane (interior only)
-          float* xd = sm + xo + g * XB.plane + (i0 + R) * XB.stride + j0 + R;
+          // float32 input plane (interior only; 16-byte aligned rows)
+          float* xd = sm + xo + g * XB.plane + (i0 + R) * XB.stride + j0 + 4;
 #pragma unroll
           for (int a = 0; a < 4; ++a) {
             if (i0 + a < H) {
               float* row = xd + a * XB.stride;
-              if ((R & 1) == 0 && j0 + 3 < W) {
-                *reinterpret_cast<float2*>(row) = make_float2(v4[a][0], v4[a][1]);
-                *reinterpret_cast<float2*>(row + 2) = make_float2(v4[a][2], v4[a][3]);
+              if (j0 + 3 < W) {
+                *reinterpret_cast<float4*>(row) = make_float4(v4[a][0], v4[a][1], v4[a][2], v4[a][3]);
               } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
@@ -312,17 +327,17 @@ __global__ void __launch_bounds__(F2_NT, 2)
           f2_coarse_strip(pl, it - g * pl.nco, l, b, r, s);
           float w[KK];
           f2_load_w<K>(wsl + (1 + 4 * (l - 1) + b) * pl.wb, w);
-          float acc[F2_SA][4];
+          float acc[F2_SAC][4];
 #pragma unroll
-          for (int o = 0; o < F2_SA; ++o)
+          for (int o = 0; o < F2_SAC; ++o)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[o][j] = 0.f;
           const WtF2Buf& Bl = pl.B[l];
-          f2_strip<K>(sm + f2_win(Bl, g, b, r, s), Bl.stride, w, acc);
+          f2_strip<K, F2_SAC>(sm + f2_win(Bl, g, b, r, s, F2_SAC), Bl.stride, w, acc);
           const WtF2Buf& Zl = pl.Z[l];
-          float* zd = sm + Zl.off + g * Zl.plane + b * Zl.band + F2_SA * r * Zl.stride + 4 * s;
+          float* zd = sm + Zl.off + g * Zl.plane + b * Zl.band + F2_SAC * r * Zl.stride + 4 * s;
 #pragma unroll
-          for (int o = 0; o < F2_SA; ++o)
+          for (int o = 0; o < F2_SAC; ++o)
             *reinterpret_cast<float4*>(zd + o * Zl.stride) = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
         }
         named_bar(1, F2_NF);
@@ -333,7 +348,7 @@ __global__ void __launch_bounds__(F2_NT, 2)
           const WtF2Buf Zl = pl.Z[l];
           const WtF2Buf Rin = pl.RC[l];  // rec_l (l < L)
           WtF2Buf Rout = pl.RC[l - 1];
-          if (l == 2) Rout.off += slot * pl.r1slot;
+          if (l == 2) Rout.off += slot * pl.r1slot + pl.zo;  // R1 columns shifted like Z1
           const int Hd = pl.Hs[l - 1], Wd = pl.Ws[l - 1];
           for (int it = ft; it < np * per; it += F2_NF) {
             const int g = it / per;
@@ -384,10 +399,18 @@ __global__ void __launch_bounds__(F2_NT, 2)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[o][j] = 0.f;
           f2_strip<K>(sm + f2_win(B1, t.g, t.b, t.r, t.s), B1.stride, w, acc);
-          float* zd = sm + Z1.off + t.g * Z1.plane + t.b * Z1.band + F2_SA * t.r * Z1.stride + 4 * t.s;
+          float* zd = sm + Z1.off + t.g * Z1.plane + t.b * Z1.band + F2_SA * t.r * Z1.stride + 4 * t.s + ZO;
 #pragma unroll
-          for (int o = 0; o < F2_SA; ++o)
-            *reinterpret_cast<float4*>(zd + o * Z1.stride) = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
+          for (int o = 0; o < F2_SA; ++o) {
+            float* zr = zd + o * Z1.stride;
+            if constexpr (ZO == 0) {
+              *reinterpret_cast<float4*>(zr) = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
+            } else {  // zo = 1: columns 4s+1 .. 4s+4
+              zr[0] = acc[o][0];
+              *reinterpret_cast<float2*>(zr + 1) = make_float2(acc[o][1], acc[o][2]);
+              zr[3] = acc[o][3];
+            }
+          }
         }
       }
       // R1 of unit v.  Every consumer thread has seen this phase complete
@@ -411,42 +434,72 @@ __global__ void __launch_bounds__(F2_NT, 2)
         const int r1o = R1.off + slot * pl.r1slot;
         for (int k = bt; k < np * pl.nf; k += F2_NB) {
           const F2Strip t = f2_final_strip(pl, k);
+          const int c0 = 4 * t.s - SH;  // first output column of the strip
+          const int qb = c0 >> 1;       // its level-1 column (floor)
+          const float* zrow = sm + Z1.off + t.g * Z1.plane;
+          const float* rrow = sm + r1o + t.g * R1.plane;
           float acc[F2_SA][4];
 #pragma unroll
           for (int o = 0; o < F2_SA; ++o) {
             const int i = F2_SA * t.r + o;
             const int p = i >> 1;
             const float su = (i & 1) ? -1.f : 1.f;
-            const float* z = sm + Z1.off + t.g * Z1.plane + p * Z1.stride + 2 * t.s;
-            const float2 z0 = *reinterpret_cast<const float2*>(z);
-            const float2 z1 = *reinterpret_cast<const float2*>(z + Z1.band);
-            const float2 z2 = *reinterpret_cast<const float2*>(z + 2 * Z1.band);
-            const float2 z3 = *reinterpret_cast<const float2*>(z + 3 * Z1.band);
-            float2 rr = make_float2(0.f, 0.f);
-            if (L >= 2) rr = *reinterpret_cast<const float2*>(sm + r1o + t.g * R1.plane + p * R1.stride + 2 * t.s);
-            const float a0 = fmaf(su, z1.x, z0.x + rr.x), b0 = fmaf(su, z3.x, z2.x);
-            const float a1 = fmaf(su, z1.y, z0.y + rr.y), b1 = fmaf(su, z3.y, z2.y);
-            acc[o][0] = bias + (a0 + b0);
-            acc[o][1] = bias + (a0 - b0);
-            acc[o][2] = bias + (a1 + b1);
-            acc[o][3] = bias + (a1 - b1);
+            // level-1 synthesis: output column c0 + j takes level-1 column
+            // qb + ((j + SH % 2) >> 1) with column parity (j + SH) & 1
+            float zv[4][3], rv[3];
+            if constexpr ((SH & 1) == 0) {
+              const float* z = zrow + p * Z1.stride + qb + ZO;  // even: one 8-byte load per band
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                const float2 t2 = *reinterpret_cast<const float2*>(z + b * Z1.band);
+                zv[b][0] = t2.x;
+                zv[b][1] = t2.y;
+                zv[b][2] = 0.f;
+              }
+              float2 r2 = make_float2(0.f, 0.f);
+              if (L >= 2) r2 = *reinterpret_cast<const float2*>(rrow + p * R1.stride + qb + ZO);
+              rv[0] = r2.x;
+              rv[1] = r2.y;
+              rv[2] = 0.f;
+            } else {
+#pragma unroll
+              for (int d = 0; d < 3; ++d) {
+                const int q = max(qb + d, 0) + ZO;  // columns left of the plane feed only discarded outputs
+#pragma unroll
+                for (int b = 0; b < 4; ++b) zv[b][d] = zrow[b * Z1.band + p * Z1.stride + q];
+                rv[d] = L >= 2 ? rrow[p * R1.stride + q] : 0.f;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int d = (j + (SH & 1)) >> 1;
+              const float a = fmaf(su, zv[1][d], zv[0][d] + rv[d]);
+              const float bb = fmaf(su, zv[3][d], zv[2][d]);
+              acc[o][j] = bias + ((((j + SH) & 1) == 0) ? a + bb : a - bb);
+            }
           }
           f2_strip<K>(sm + xo + t.g * XB.plane + F2_SA * t.r * XB.stride + 4 * t.s, XB.stride, w, acc);
           T* plane = y + ((size_t)(n0 + t.g) * C + c) * HW;
-          const int j0 = 4 * t.s;
-          const bool full = pl.out_vec && j0 + 4 <= W;
 #pragma unroll
           for (int o = 0; o < F2_SA; ++o) {
             const int i = F2_SA * t.r + o;
             if (i < H) {
-              T* dst = plane + (size_t)i * W + j0;
-              if (full) {
-                stg_row<T, 4>(dst, acc[o]);
-              } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  if (j0 + j < W) dst[j] = from_f32<T>(acc[o][j]);
+              T* dst = plane + (size_t)i * W;
+              if constexpr (SH == 0) {
+                if (pl.out_vec && c0 + 4 <= W) {
+                  stg_row<T, 4>(dst + c0, acc[o]);
+                  continue;
+                }
+              } else if constexpr (SH == 2) {
+                if (pl.out_vec && c0 >= 0 && c0 + 4 <= W) {  // two 2-element stores (c0 is even)
+                  stg_row<T, 2>(dst + c0, acc[o]);
+                  stg_row<T, 2>(dst + c0 + 2, acc[o] + 2);
+                  continue;
+                }
               }
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (c0 + j >= 0 && c0 + j < W) dst[c0 + j] = from_f32<T>(acc[o][j]);
             }
           }
         }

@@ -219,10 +219,9 @@ static void replay(int N, int C, int H, int W, int L, int K, int dtype) {
       }
       for (int a = 0; a < 4; ++a) {
         if (i0 + a >= H) continue;
-        const long xb = pl.X.off + (long)slot * pl.xslot + (long)g * pl.X.plane + (long)(i0 + a + R) * pl.X.stride + j0 + R;
-        if ((R & 1) == 0 && j0 + 3 < W) {
-          sh.w(xb, 2, ph_an, rX, "X write");
-          sh.w(xb + 2, 2, ph_an, rX, "X write");
+        const long xb = pl.X.off + (long)slot * pl.xslot + (long)g * pl.X.plane + (long)(i0 + a + R) * pl.X.stride + j0 + 4;
+        if (j0 + 3 < W) {
+          sh.w(xb, 4, ph_an, rX, "X write");
         } else {
           for (int e = 0; e < 4; ++e)
             if (j0 + e < W) sh.w(xb + e, 1, ph_an, rX, "X write");
@@ -271,13 +270,13 @@ static void replay(int N, int C, int H, int W, int L, int K, int dtype) {
         CHECK(l >= 2 && l <= L && b >= 0 && b < 4 && r >= 0 && r < pl.A[l] && s >= 0 && s < pl.T[l], "coarse strip");
         const long wsrc = pl.w_off + (long)slot * pl.wslot + (1 + 4 * (l - 1) + b) * pl.wb;
         for (int t = 0; t < KK; t += 4) sh.r(wsrc + t, 4, ph, rW, "coarse weights");
-        const long win = f2_win(pl.B[l], g, b, r, s);
+        const long win = f2_win(pl.B[l], g, b, r, s, F2_SAC);
         CHECK(win % 4 == 0 && pl.B[l].stride % 4 == 0, "coarse window alignment");
-        for (int a = 0; a < F2_SA + K - 1; ++a)
+        for (int a = 0; a < F2_SAC + K - 1; ++a)
           for (int v4 = 0; v4 < NV; ++v4)
             sh.r(win + (long)a * pl.B[l].stride + 4 * v4, 4, ph, reg("B" + std::to_string(l)), "coarse window");
-        const long zd = pl.Z[l].off + (long)g * pl.Z[l].plane + (long)b * pl.Z[l].band + (long)F2_SA * r * pl.Z[l].stride + 4 * s;
-        for (int o = 0; o < F2_SA; ++o) sh.w(zd + (long)o * pl.Z[l].stride, 4, ph, reg("Z" + std::to_string(l)), "Zc write");
+        const long zd = pl.Z[l].off + (long)g * pl.Z[l].plane + (long)b * pl.Z[l].band + (long)F2_SAC * r * pl.Z[l].stride + 4 * s;
+        for (int o = 0; o < F2_SAC; ++o) sh.w(zd + (long)o * pl.Z[l].stride, 4, ph, reg("Z" + std::to_string(l)), "Zc write");
       }
       ++ph;
       // (4) cascade
@@ -285,7 +284,7 @@ static void replay(int N, int C, int H, int W, int L, int K, int dtype) {
         const int per = pl.Hs[l] * pl.Ws[l];
         WtF2Buf Rout = pl.RC[l - 1];
         std::string rout = l == 2 ? (slot ? "R1_1" : "R1_0") : "RC" + std::to_string(l - 1);
-        if (l == 2) Rout.off += slot * pl.r1slot;
+        if (l == 2) Rout.off += slot * pl.r1slot + pl.zo;
         for (int it = 0; it < np * per; ++it) {
           const int g = it / per, rem = it - g * per, p = rem / pl.Ws[l], q = rem - p * pl.Ws[l];
           const long z = f2_at(pl.Z[l], g, 0, p, q, 0);
@@ -315,27 +314,63 @@ static void replay(int N, int C, int H, int W, int L, int K, int dtype) {
       for (int a = 0; a < F2_SA + K - 1; ++a)
         for (int v4 = 0; v4 < NV; ++v4) sh.r(win + (long)a * pl.B[1].stride + 4 * v4, 4, ph_l1, reg("B1"), "l1 window");
       const long zd = pl.Z[1].off + (long)t.g * pl.Z[1].plane + (long)t.b * pl.Z[1].band +
-                      (long)F2_SA * t.r * pl.Z[1].stride + 4 * t.s;
-      for (int o = 0; o < F2_SA; ++o) sh.w(zd + (long)o * pl.Z[1].stride, 4, ph_l1, reg("Z1"), "Z1 write");
+                      (long)F2_SA * t.r * pl.Z[1].stride + 4 * t.s + pl.zo;
+      CHECK(4 * t.s + pl.zo + 4 <= pl.Z[1].stride, "Z1 write beyond stride");
+      for (int o = 0; o < F2_SA; ++o) {
+        const long zr = zd + (long)o * pl.Z[1].stride;
+        if (pl.zo == 0) {
+          sh.w(zr, 4, ph_l1, reg("Z1"), "Z1 write");
+        } else {
+          sh.w(zr, 1, ph_l1, reg("Z1"), "Z1 write");
+          sh.w(zr + 1, 2, ph_l1, reg("Z1"), "Z1 write");
+          sh.w(zr + 3, 1, ph_l1, reg("Z1"), "Z1 write");
+        }
+      }
     }
     // (b) final strips
     const int ph_f = ph++;
+    const int SH = f2_sh(K);
     for (int k = 0; k < np * pl.nf; ++k) {
       const F2Strip t = f2_final_strip(pl, k);
       CHECK(t.g == k / pl.nf && t.r >= 0 && t.r < pl.A[0] && t.s >= 0 && t.s < pl.T[0], "final strip decode");
+      const int c0 = 4 * t.s - SH, qb = c0 >> 1;
       for (int o = 0; o < F2_SA; ++o) {
         const int i = F2_SA * t.r + o, p = i >> 1;
-        const long z = pl.Z[1].off + (long)t.g * pl.Z[1].plane + (long)p * pl.Z[1].stride + 2 * t.s;
-        CHECK(p < pl.Z[1].rows && 2 * t.s + 1 < pl.Z[1].stride, "Z1 read beyond rows/stride");
-        for (int b = 0; b < 4; ++b) {
-          sh.r(z + (long)b * pl.Z[1].band, 2, ph_f, reg("Z1"), "Z1 read");
-          if (i < H && 2 * t.s < pl.Ws[1]) CHECK(sh.wr[z + (long)b * pl.Z[1].band] == ph_l1, "valid output reads unwritten Z1");
+        CHECK(p < pl.Z[1].rows && (L < 2 || p < pl.RC[1].rows), "Z1/R1 row beyond rows");
+        // the columns this row reads, and which output columns each feeds
+        std::vector<std::pair<long, int>> zcols;  // (buffer column, width), level-1 column
+        if ((SH & 1) == 0) {
+          zcols.push_back({qb + pl.zo, 2});
+          CHECK((qb + pl.zo) >= 0 && (qb + pl.zo) % 2 == 0, "synthesis pair column");
+        } else {
+          for (int d = 0; d < 3; ++d) zcols.push_back({std::max(qb + d, 0) + pl.zo, 1});
         }
-        if (L >= 2) {
-          const long rr = pl.RC[1].off + (long)slot * pl.r1slot + (long)t.g * pl.RC[1].plane + (long)p * pl.RC[1].stride + 2 * t.s;
-          CHECK(p < pl.RC[1].rows && 2 * t.s + 1 < pl.RC[1].stride, "R1 read beyond rows/stride");
-          sh.r(rr, 2, ph_f, reg(slot ? "R1_1" : "R1_0"), "R1 read");
-          if (i < H && 2 * t.s < pl.Ws[1]) CHECK(sh.wr[rr] != 0, "valid output reads unwritten R1");
+        for (auto& zc : zcols) {
+          CHECK(zc.first + zc.second <= pl.Z[1].stride && (L < 2 || zc.first + zc.second <= pl.RC[1].stride),
+                "synthesis column beyond stride");
+          for (int b = 0; b < 4; ++b)
+            sh.r(pl.Z[1].off + (long)t.g * pl.Z[1].plane + (long)b * pl.Z[1].band + (long)p * pl.Z[1].stride + zc.first,
+                 zc.second, ph_f, reg("Z1"), "Z1 read");
+          if (L >= 2)
+            sh.r(pl.RC[1].off + (long)slot * pl.r1slot + (long)t.g * pl.RC[1].plane + (long)p * pl.RC[1].stride + zc.first,
+                 zc.second, ph_f, reg(slot ? "R1_1" : "R1_0"), "R1 read");
+        }
+        // every output column inside the plane reads its own level-1 column,
+        // which an earlier phase wrote
+        for (int j = 0; j < 4; ++j) {
+          const int cc = c0 + j;
+          if (i >= H || cc < 0 || cc >= W) continue;
+          const int q = cc >> 1;
+          const int d = (j + (SH & 1)) >> 1;
+          CHECK(q == qb + d, "synthesis column mapping");
+          for (int b = 0; b < 4; ++b) {
+            const long a = pl.Z[1].off + (long)t.g * pl.Z[1].plane + (long)b * pl.Z[1].band + (long)p * pl.Z[1].stride + q + pl.zo;
+            CHECK(sh.wr[a] == ph_l1, "valid output reads unwritten Z1");
+          }
+          if (L >= 2) {
+            const long a = pl.RC[1].off + (long)slot * pl.r1slot + (long)t.g * pl.RC[1].plane + (long)p * pl.RC[1].stride + q + pl.zo;
+            CHECK(sh.wr[a] != 0, "valid output reads unwritten R1");
+          }
         }
       }
       for (int q4 = 0; q4 < KK; q4 += 4) sh.r(pl.w_off + (long)slot * pl.wslot + q4, 4, ph_f, rW, "base weights");
@@ -346,12 +381,14 @@ static void replay(int N, int C, int H, int W, int L, int K, int dtype) {
         const int i = F2_SA * t.r + o;
         if (i >= H) continue;
         for (int j = 0; j < 4; ++j) {
-          const int jj = 4 * t.s + j;
-          if (jj >= W) continue;
+          const int jj = c0 + j;
+          if (jj < 0 || jj >= W) continue;
           const long e = ((long)(n0 + t.g) * C + c) * H * W + (long)i * W + jj;
           CHECK(e >= 0 && e < x_elems, "y store beyond y");
         }
-        if ((W & 3) == 0) CHECK(((((long)(n0 + t.g) * C + c) * H * W + (long)i * W + 4 * t.s) & 3) == 0, "y vector store");
+        const long e0 = ((long)(n0 + t.g) * C + c) * H * W + (long)i * W + c0;
+        if ((W & 3) == 0 && SH == 0) CHECK((e0 & 3) == 0, "y 4-element store alignment");
+        if ((W & 3) == 0 && SH == 2 && c0 >= 0) CHECK((e0 & 1) == 0, "y 2-element store alignment");
       }
     }
   }
