@@ -36,9 +36,20 @@ __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(mbar)) : "memory");
+// Arrives at named barrier `id` (of n threads) without waiting: the
+// signalling side of a producer/consumer handoff; the waiting side calls
+// named_bar (bar.sync), which sleeps in hardware until all n have arrived.
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(n) : "memory");
 }
+
+// Named barriers: 1 producer group, 2 consumer group; the handoffs between
+// the groups (all F2_NT threads): producer -> consumer "X, B1 and the weights
+// of unit v are ready" and "R1 of unit v is ready"; consumer -> producer "B1
+// of unit v has been read".
+#define F2_BAR_B1READY 3
+#define F2_BAR_FREADY 4
+#define F2_BAR_MID 5
 
 // One try_wait that may suspend the thread until the phase completes or
 // about `hint_ns` nanoseconds pass; a suspended warp issues nothing, so the
@@ -131,10 +142,7 @@ __global__ void __launch_bounds__(F2_NT, 2)
   const int nu = u1 - u0;
   uint64_t* const mb = reinterpret_cast<uint64_t*>(sm + pl.mb_off);
   uint64_t* const rawfull = mb;      // [2]: raw slot landed (bulk copies)
-  uint64_t* const b1ready = mb + 2;  // producer -> consumer: X, B1, weights of unit v
-  uint64_t* const mid = mb + 3;      // consumer -> producer: B1 of unit v read
-  uint64_t* const fready = mb + 4;   // producer -> consumer: R1 of unit v
-  __shared__ int s_abort_f, s_abort_b;
+  __shared__ int s_abort;            // a copy did not land in time: the rest of the work is skipped
 
   // Every margin of every buffer is zero and stays zero: later writes touch
   // interiors only.  (The raw slots, written by the copies, need no zeros.)
@@ -142,12 +150,8 @@ __global__ void __launch_bounds__(F2_NT, 2)
   if (tid == 0) {
     mbar_init(&rawfull[0], 1);
     mbar_init(&rawfull[1], 1);
-    mbar_init(b1ready, 1);
-    mbar_init(mid, 1);
-    mbar_init(fready, 1);
     fence_mbar_init();
-    s_abort_f = 0;
-    s_abort_b = 0;
+    s_abort = 0;
   }
   __syncthreads();
   if (nu <= 0) return;
@@ -187,9 +191,19 @@ __global__ void __launch_bounds__(F2_NT, 2)
         cp_async_commit();
       }
     };
-    issue(0);
-    if (nu > 1) issue(1);
+    // Copies issued and waited for, per raw slot (a slot has at most one copy
+    // in flight): after a failed wait the remaining copies are still waited
+    // for before the CTA exits.
+    int issued0 = 0, issued1 = 0, waited0 = 0, waited1 = 0;
+    auto issue_count = [&](int v) {
+      issue(v);
+      if (v & 1) ++issued1;
+      else ++issued0;
+    };
+    issue_count(0);
+    if (nu > 1) issue_count(1);
     int wch0 = -1, wch1 = -1;  // channel whose folded weights sit in slot 0 / 1
+    bool dead = false;         // uniform over the group: the work of the remaining units is skipped
     for (int v = 0; v < nu; ++v) {
       const int u = u0 + v;
       const int c = wt_fdiv(u, pl.d_G);
@@ -197,29 +211,25 @@ __global__ void __launch_bounds__(F2_NT, 2)
       const int np = min(P, pl.N - n0);
       const int slot = v & 1;
       bool ok = true;
-      if (bulk) {
-        ok = f2_wait(&rawfull[slot], (uint32_t)(v >> 1) & 1u, pl.wait_shift);
-      } else {
-        if (v + 1 < nu) cp_async_wait_1();  // unit v+1's group may still be in flight
-        else cp_async_wait_all();
-      }
-      if (ok && v >= 1) ok = f2_wait(mid, (uint32_t)(v - 1) & 1u, pl.wait_shift);  // B1 free again
-      if (!ok) s_abort_f = 1;
-      named_bar(1, F2_NF);
-      if (s_abort_f) {
-        if (ft == 0) {
-          atomicAdd(&g_fwd2_faults, 1u);
-          // let the copies in flight land before the CTA's shared memory goes away
-          if (bulk) {
-            f2_wait(&rawfull[slot], (uint32_t)(v >> 1) & 1u, pl.wait_shift);
-            if (v + 1 < nu) f2_wait(&rawfull[slot ^ 1], (uint32_t)((v + 1) >> 1) & 1u, pl.wait_shift);
-          }
+      if (!dead) {
+        if (bulk) {
+          ok = f2_wait(&rawfull[slot], (uint32_t)(v >> 1) & 1u, pl.wait_shift);
+          if (slot) ++waited1;
+          else ++waited0;
+        } else {
+          if (v + 1 < nu) cp_async_wait_1();  // unit v+1's group may still be in flight
+          else cp_async_wait_all();
         }
-        if (!bulk) cp_async_wait_all();
-        return;
+      }
+      if (v >= 1) named_bar(F2_BAR_MID, F2_NT);  // the consumers have read B1 of unit v-1
+      if (!ok) s_abort = 1;
+      named_bar(1, F2_NF);
+      if (!dead && s_abort) {
+        dead = true;
+        if (ft == 0) atomicAdd(&g_fwd2_faults, 1u);
       }
       float* const wsl = sm + pl.w_off + slot * pl.wslot;
-      if ((slot ? wch1 : wch0) != c) {
+      if (!dead && (slot ? wch1 : wch0) != c) {
         stage_weights<K, ROT>(wsl, pl.wb, L, C, c, w_base, w_sub, s_base, s_w, ft, F2_NF);
         if (slot) wch1 = c;
         else wch0 = c;
@@ -231,7 +241,7 @@ __global__ void __launch_bounds__(F2_NT, 2)
         const bool vec = (W & 3) == 0;
         const WtF2Buf XB = pl.X, B1 = pl.B[1], B2 = pl.B[2];
         const int xo = pl.X.off + slot * pl.xslot;
-        for (int it = ft; it < np * pl.na; it += F2_NF) {
+        for (int it = ft; it < (dead ? 0 : np * pl.na); it += F2_NF) {
           const int g = wt_fdiv(it, pl.d_na);
           const int rem = it - g * pl.na;
           const int bi = wt_fdiv(rem, pl.d_nbw);
@@ -300,10 +310,10 @@ __global__ void __launch_bounds__(F2_NT, 2)
         }
       }
       named_bar(1, F2_NF);
-      if (ft == 0) mbar_arrive(b1ready);  // X, B1 and the weights of unit v are ready
-      if (v + 2 < nu) issue(v + 2);       // the raw slot is consumed
+      named_arrive(F2_BAR_B1READY, F2_NT);       // X, B1 and the weights of unit v are ready
+      if (!dead && v + 2 < nu) issue_count(v + 2);  // the raw slot is consumed
       // (2) levels 3..L of the analysis.
-      for (int l = 3; l <= L; ++l) {
+      for (int l = 3; l <= (dead ? 0 : L); ++l) {
         const WtF2Buf S = pl.B[l - 1], D = pl.B[l];
         const int Hl = pl.Hs[l], Wl = pl.Ws[l], per = Hl * Wl;
         for (int it = ft; it < np * per; it += F2_NF) {
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(F2_NT, 2)
         named_bar(1, F2_NF);
       }
       // (3) band convolutions of levels 2..L (Zc).
-      if (L >= 2) {
+      if (!dead && L >= 2) {
         for (int it = ft; it < np * pl.nco; it += F2_NF) {
           const int g = it / pl.nco;
           int l, b, r, s;
@@ -370,9 +380,16 @@ __global__ void __launch_bounds__(F2_NT, 2)
           named_bar(1, F2_NF);
         }
       }
-      if (ft == 0) mbar_arrive(fready);  // R1 of unit v is ready
+      named_arrive(F2_BAR_FREADY, F2_NT);  // R1 of unit v is ready
     }
-    if (!bulk) cp_async_wait_all();
+    named_bar(F2_BAR_MID, F2_NT);  // the consumers' last arrival
+    // Copies still in flight (only after a failed wait) land before exit.
+    if (bulk) {
+      if (issued0 > waited0) f2_wait(&rawfull[0], (uint32_t)waited0 & 1u, pl.wait_shift);
+      if (issued1 > waited1) f2_wait(&rawfull[1], (uint32_t)waited1 & 1u, pl.wait_shift);
+    } else {
+      cp_async_wait_all();
+    }
   } else {
     // ======================= consumer group =======================
     const int bt = tid - F2_NF;
@@ -385,47 +402,39 @@ __global__ void __launch_bounds__(F2_NT, 2)
       const int np = min(P, pl.N - n0);
       const int slot = v & 1;
       const float* wsl = sm + pl.w_off + slot * pl.wslot;
-      bool ok = f2_wait(b1ready, (uint32_t)v & 1u, pl.wait_shift);
-      if (!ok) s_abort_b = 1;
+      named_bar(F2_BAR_B1READY, F2_NT);  // X, B1 and the weights of unit v
+      const bool dead = s_abort != 0;     // set before the producer's arrival: work is skipped
       // (a) level-1 band convolutions -> Z1.
-      if (ok) {
-        for (int k = bt; k < np * pl.n1; k += F2_NB) {
-          const F2Strip t = f2_l1_strip(pl, k);
-          float w[KK];
-          f2_load_w<K>(wsl + (1 + t.b) * pl.wb, w);
-          float acc[F2_SA][4];
+      for (int k = bt; k < (dead ? 0 : np * pl.n1); k += F2_NB) {
+        const F2Strip t = f2_l1_strip(pl, k);
+        float w[KK];
+        f2_load_w<K>(wsl + (1 + t.b) * pl.wb, w);
+        float acc[F2_SA][4];
 #pragma unroll
-          for (int o = 0; o < F2_SA; ++o)
+        for (int o = 0; o < F2_SA; ++o)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[o][j] = 0.f;
-          f2_strip<K>(sm + f2_win(B1, t.g, t.b, t.r, t.s), B1.stride, w, acc);
-          float* zd = sm + Z1.off + t.g * Z1.plane + t.b * Z1.band + F2_SA * t.r * Z1.stride + 4 * t.s + ZO;
+          for (int j = 0; j < 4; ++j) acc[o][j] = 0.f;
+        f2_strip<K>(sm + f2_win(B1, t.g, t.b, t.r, t.s), B1.stride, w, acc);
+        float* zd = sm + Z1.off + t.g * Z1.plane + t.b * Z1.band + F2_SA * t.r * Z1.stride + 4 * t.s + ZO;
 #pragma unroll
-          for (int o = 0; o < F2_SA; ++o) {
-            float* zr = zd + o * Z1.stride;
-            if constexpr (ZO == 0) {
-              *reinterpret_cast<float4*>(zr) = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
-            } else {  // zo = 1: columns 4s+1 .. 4s+4
-              zr[0] = acc[o][0];
-              *reinterpret_cast<float2*>(zr + 1) = make_float2(acc[o][1], acc[o][2]);
-              zr[3] = acc[o][3];
-            }
+        for (int o = 0; o < F2_SA; ++o) {
+          float* zr = zd + o * Z1.stride;
+          if constexpr (ZO == 0) {
+            *reinterpret_cast<float4*>(zr) = make_float4(acc[o][0], acc[o][1], acc[o][2], acc[o][3]);
+          } else {  // zo = 1: columns 4s+1 .. 4s+4
+            zr[0] = acc[o][0];
+            *reinterpret_cast<float2*>(zr + 1) = make_float2(acc[o][1], acc[o][2]);
+            zr[3] = acc[o][3];
           }
         }
       }
-      // R1 of unit v.  Every consumer thread has seen this phase complete
-      // before `mid` lets the producer start unit v+1 (and later complete the
-      // next phase), so no waiter can miss a phase.
-      if (!f2_wait(fready, (uint32_t)v & 1u, pl.wait_shift)) s_abort_b = 1;
-      named_bar(2, F2_NB);
-      if (s_abort_b) {
-        if (bt == 0) atomicAdd(&g_fwd2_faults, 1u);
-        return;
-      }
-      if (bt == 0) mbar_arrive(mid);  // B1 of unit v may be overwritten
+      // R1 of unit v; this barrier also orders every consumer's Z1 writes
+      // before the final strips read them.
+      named_bar(F2_BAR_FREADY, F2_NT);
+      named_arrive(F2_BAR_MID, F2_NT);  // B1 of unit v may be overwritten
       // (b) final strips: bias + level-1 synthesis of Z1 + R1, then the base
       // convolution accumulated on top, stored to HBM.
-      {
+      if (!dead) {
         const float bias = (!ROT && b_base != nullptr) ? s_base[c] * b_base[c] : 0.f;
         float w[KK];
         f2_load_w<K>(wsl, w);
@@ -505,10 +514,6 @@ __global__ void __launch_bounds__(F2_NT, 2)
         }
       }
       named_bar(2, F2_NB);  // Z1 is rewritten by the next unit
-      if (s_abort_b) {
-        if (bt == 0) atomicAdd(&g_fwd2_faults, 1u);
-        return;
-      }
     }
   }
 }
