@@ -14,7 +14,6 @@
 #include <tuple>
 
 #include "../../include/wtconv.h"
-#include "wtconv_f2_plan.h"
 #include "wtconv_launch.h"
 #include "wtconv_plan.h"
 
@@ -213,55 +212,6 @@ wtconv_status_t plan_bw_win(const wtconv_desc_t* d, WtBwPlan& pl, int load) {
   const wtconv_status_t st = plan_bw_win_compute(d, pl, load);
   if (st == WTCONV_OK) cache.put(k, pl);
   return st;
-}
-
-// Plan of the pipelined whole-plane forward / input-gradient kernel, or
-// false when the layer does not fit it (two CTAs per SM at one plane per
-// unit): the phase-per-unit kernels take such layers.
-bool plan_f2(const wtconv_desc_t* d, WtF2Plan& pl) {
-  struct Entry {
-    bool ok;
-    WtF2Plan pl;
-  };
-  static PlanCache<Entry> cache;
-  const PlanKey k = plan_key(d, -2);
-  Entry e;
-  if (cache.get(k, &e)) {
-    pl = e.pl;
-    return e.ok;
-  }
-  e.ok = wt2::plan(e.pl, d->N, d->C, d->H, d->W, d->levels, d->k, d->dtype, kSmemPerSm, kMaxSmemPerBlock,
-                   wt::sm_count() > 0 ? wt::sm_count() : kNumSms,
-                   [](const WtF2Plan& p) { return wt::fwd2_ctas_per_sm(p); });
-  cache.put(k, e);
-  pl = e.pl;
-  return e.ok;
-}
-
-// Test hook state (wtconv_test_set_wait_limit): the bounded waits of the
-// pipelined kernel give up after 2^shift cycles, and its copy barriers expect
-// extra_tx more bytes than the copies deliver (0 in normal operation).
-std::mutex g_hook_mu;
-int g_hook_wait_shift = 31;
-uint32_t g_hook_extra_tx = 0;
-
-// Launches the pipelined kernel when the layer and the pointers suit it.
-// Returns false (nothing launched) otherwise.
-bool try_fwd2(const wtconv_desc_t* d, bool rotate, const void* src, const float* w_base, const float* b_base,
-              const float* w_sub, const float* base_scale, const float* wavelet_scale, void* dst,
-              cudaStream_t stream, cudaError_t* err) {
-  WtF2Plan pl;
-  if (!plan_f2(d, pl)) return false;
-  if (!wt2::set_load(pl, src)) return false;
-  const size_t es = elem_size(d->dtype);
-  pl.out_vec = (d->W % 4 == 0) && ((uintptr_t)dst % (4 * es) == 0);
-  {
-    std::lock_guard<std::mutex> lock(g_hook_mu);
-    pl.wait_shift = g_hook_wait_shift;
-    pl.dbg_extra_tx = g_hook_extra_tx;
-  }
-  *err = wt::launch_fwd2(pl, rotate, src, w_base, b_base, w_sub, base_scale, wavelet_scale, dst, stream);
-  return true;
 }
 
 wtconv_status_t plan_bwf(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan& fp) {
@@ -1235,11 +1185,6 @@ wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float
   alignas(64) CUtensorMap tmx;
   memset(&tmx, 0, sizeof(tmx));
   cudaError_t e;
-  if (!pl.win && try_fwd2(desc, false, x, w_base, b_base, w_sub, base_scale, wavelet_scale, y,
-                          (cudaStream_t)stream, &e)) {
-    if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_fwd: %s", cudaGetErrorString(e));
-    return ok();
-  }
   if (pl.win) {
     WT_TRY(prepare_win(desc, pl, &tmx, x, y));
     e = wt::launch_fwd_win(pl, tmx, desc->dtype, false, x, w_base, b_base, w_sub, base_scale, wavelet_scale, y,
@@ -1274,11 +1219,6 @@ wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const
   alignas(64) CUtensorMap tmx;
   memset(&tmx, 0, sizeof(tmx));
   cudaError_t e;
-  if (!pl.win && try_fwd2(desc, true, dy, w_base, nullptr, w_sub, base_scale, wavelet_scale, dx,
-                          (cudaStream_t)stream, &e)) {
-    if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_data: %s", cudaGetErrorString(e));
-    return ok();
-  }
   if (pl.win) {
     WT_TRY(prepare_win(desc, pl, &tmx, dy, dx));
     e = wt::launch_fwd_win(pl, tmx, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale, wavelet_scale,
@@ -1437,7 +1377,7 @@ const char* wtconv_last_error(void) { return g_last_error; }
 unsigned int wtconv_device_faults(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return 0;
   return wt::take_fwd_faults() + wt::take_win_faults() + wt::take_bw_faults() + wt::take_bww_faults() +
-         wt::take_bwf_faults() + wt::take_fwd2_faults();
+         wt::take_bwf_faults();
 }
 
 }  // extern "C"

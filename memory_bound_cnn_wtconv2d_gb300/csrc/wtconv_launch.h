@@ -4,7 +4,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "wtconv_f2.h"
 #include "wtconv_plan.h"
 
 namespace wt {
@@ -20,14 +19,6 @@ cudaError_t launch_fwd(const WtFwdPlan& pl, const CUtensorMap& tmx, int dtype, b
 cudaError_t launch_fwd_win(const WtFwdPlan& pl, const CUtensorMap& tmx, int dtype, bool rotate, const void* x,
                            const float* w_base, const float* b_base, const float* w_sub, const float* s_base,
                            const float* s_w, void* y, cudaStream_t stream);
-
-// Pipelined whole-plane forward (rotate = false) or input-gradient pass
-// (rotate = true, no bias): fwd2_kernel, plan in wtconv_f2.h.
-cudaError_t launch_fwd2(const WtF2Plan& pl, bool rotate, const void* x, const float* w_base, const float* b_base,
-                        const float* w_sub, const float* s_base, const float* s_w, void* y, cudaStream_t stream);
-// Resident CTAs per SM of the kernel a plan launches (0 when it cannot tell).
-int fwd2_ctas_per_sm(const WtF2Plan& pl);
-unsigned int take_fwd2_faults();
 
 // Number of bounded in-kernel waits that gave up since the last call
 // (reads and clears a device counter; synchronises the device).

@@ -50,10 +50,6 @@ int bwf_ctas_per_sm(const WtBwPlan& pl, const WtFwdPlan&, int) { int n = (int)(2
 unsigned int take_bwf_faults() { return 0; }
 int bw_ctas_per_sm(const WtBwPlan& pl, int) { return (int)(233472 / (pl.smem_bytes + 1024)) > 3 ? 3 : (int)(233472 / (pl.smem_bytes + 1024)); }
 unsigned int take_bw_faults() { return 0; }
-cudaError_t launch_fwd2(const WtF2Plan&, bool, const void*, const float*, const float*, const float*, const float*,
-                        const float*, void*, cudaStream_t) { return cudaSuccess; }
-int fwd2_ctas_per_sm(const WtF2Plan& pl) { int n = (int)(233472 / (pl.smem_bytes + 1024)); return n > 2 ? 2 : n; }
-unsigned int take_fwd2_faults() { return 0; }
 }
 
 static long errors = 0;  // failed checks (the first 20 are printed)

@@ -50,26 +50,3 @@ def test_plans_of_the_random_gpu_sweep(replay, tmp_path):
     out = run([replay, "file", str(cases)])
     assert f"layers: {len(CASES)}, refused: 0" in out
 
-
-SRC_F2 = os.path.join(ROOT, "tests", "index_replay", "replay_f2.cpp")
-
-
-def test_pipelined_forward_plans():
-    # the pipelined whole-plane forward / input-gradient kernel: its planner's
-    # layouts and every index its phases form (host code, g++)
-    gxx = shutil.which("g++")
-    if gxx is None:
-        pytest.skip("g++ not available")
-    import tempfile
-    with tempfile.TemporaryDirectory() as d:
-        exe = os.path.join(d, "replay_f2")
-        subprocess.run([gxx, "-std=c++17", "-O2", "-I", os.path.join(ROOT, "include"),
-                        "-I", os.path.join(ROOT, "memory_bound_cnn_wtconv2d_gb300", "csrc"), SRC_F2, "-o", exe],
-                       check=True, capture_output=True)
-        out = run([exe])
-        assert "layers:" in out
-        from test_random_shapes_gpu import CASES, DTYPES
-        cases = os.path.join(d, "cases.txt")
-        with open(cases, "w") as f:
-            f.write("".join(" ".join(map(str, c[:6])) + f" {DTYPES.index(c[6])}\n" for c in CASES))
-        run([exe, "file", cases])
