@@ -208,6 +208,16 @@ const char* wtconv_last_error(void);
  * current device. */
 unsigned int wtconv_device_faults(void);
 
+/* Test support, off by default (no counterpart in the pages): with enable
+ * nonzero, every later call on any thread gives the in-kernel waits for its
+ * plane copies a limit of about 2^20 clock cycles and arms each copy's
+ * barrier with 16 bytes more than the copy delivers, so each such wait runs
+ * out: the kernel records the fault (see wtconv_device_faults), lets its copy
+ * land and leaves early, with its outputs invalid and the device usable.
+ * This exercises the give-up path of the bounded waits without a GPU fault.
+ * enable = 0 restores normal operation. */
+void wtconv_test_copy_timeout(int enable);
+
 #ifdef __cplusplus
 }
 #endif

@@ -214,6 +214,21 @@ wtconv_status_t plan_bw_win(const wtconv_desc_t* d, WtBwPlan& pl, int load) {
   return st;
 }
 
+// Test hook (wtconv_test_copy_timeout): while it is on, every launch gives
+// its bounded copy waits a limit of 2^20 clock cycles and arms each copy
+// barrier with 16 bytes more than its copies deliver, so that each wait runs
+// out.  Off: 2^31 cycles and no extra bytes.  Applied to the caller's copy of
+// a plan just before its launch (cached plans are not touched).
+std::mutex g_hook_mu;
+bool g_hook_on = false;
+
+template <typename Plan>
+void apply_wait_hook(Plan& pl) {
+  std::lock_guard<std::mutex> lock(g_hook_mu);
+  pl.wait_shift = g_hook_on ? 20 : 31;
+  pl.dbg_extra_tx = g_hook_on ? 16u : 0u;
+}
+
 wtconv_status_t plan_bwf(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan& fp) {
   static PlanCache<BwfPlans> cache;
   const PlanKey k = plan_key(d, -1);
@@ -1187,12 +1202,14 @@ wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float
   cudaError_t e;
   if (pl.win) {
     WT_TRY(prepare_win(desc, pl, &tmx, x, y));
+    apply_wait_hook(pl);
     e = wt::launch_fwd_win(pl, tmx, desc->dtype, false, x, w_base, b_base, w_sub, base_scale, wavelet_scale, y,
                            (cudaStream_t)stream);
   } else {
     set_load_divs(pl, desc, vec_ok(desc, x, y));
     pl.use_tma = encode_plane_map(&tmx, x, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
     set_bulk(pl, desc, x, 4L * (pl.work_off - pl.stage_off));
+    apply_wait_hook(pl);
     e = wt::launch_fwd(pl, tmx, desc->dtype, false, x, w_base, b_base, w_sub, base_scale, wavelet_scale, y,
                        (cudaStream_t)stream);
   }
@@ -1221,12 +1238,14 @@ wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const
   cudaError_t e;
   if (pl.win) {
     WT_TRY(prepare_win(desc, pl, &tmx, dy, dx));
+    apply_wait_hook(pl);
     e = wt::launch_fwd_win(pl, tmx, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale, wavelet_scale,
                            dx, (cudaStream_t)stream);
   } else {
     set_load_divs(pl, desc, vec_ok(desc, dy, dx));
     pl.use_tma = encode_plane_map(&tmx, dy, desc, pl.lev[0].stride, pl.lev[0].band / pl.lev[0].stride, pl.P);
     set_bulk(pl, desc, dy, 4L * (pl.work_off - pl.stage_off));
+    apply_wait_hook(pl);
     e = wt::launch_fwd(pl, tmx, desc->dtype, true, dy, w_base, nullptr, w_sub, base_scale, wavelet_scale, dx,
                        (cudaStream_t)stream);
   }
@@ -1277,6 +1296,7 @@ wtconv_status_t wtconv_bwd(const wtconv_desc_t* desc, const void* x, const void*
   memset(&tmd, 0, sizeof(tmd));
   pl.use_tma = encode_plane_map(&tmx, x, desc, pl.xs[0].stride, pl.xbf / pl.xs[0].stride, pl.P) &&
                encode_plane_map(&tmd, dy, desc, pl.ds[0].stride, pl.dbf / pl.ds[0].stride, pl.P);
+  apply_wait_hook(pl);
   cudaError_t e = wt::launch_bwd_fused(pl, fp, tmx, tmd, desc->dtype, x, dy, w_base, b_base, w_sub, base_scale,
                                        wavelet_scale, dx, dw_base, db_base, dw_sub, dbase_scale, dwavelet_scale,
                                        static_cast<float*>(ws), (cudaStream_t)stream);
@@ -1341,6 +1361,7 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
     return fail(WTCONV_ERR_WORKSPACE, "workspace of %zu B given, %zu B needed", ws ? ws_bytes : 0, need);
   if (!aligned(ws, 256)) return fail(WTCONV_ERR_MISALIGNED, "workspace is not 256-byte aligned");
   if (pl.win) {
+    apply_wait_hook(pl);
     cudaError_t e = wt::launch_bwd_weight_win(pl, tmx, tmd, desc->dtype, x, dy, w_base, b_base, w_sub, base_scale,
                                               wavelet_scale, dw_base, db_base, dw_sub, dbase_scale, dwavelet_scale,
                                               static_cast<float*>(ws), st);
@@ -1353,6 +1374,7 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
   if (pl.use_bulk == 2 && !aligned(dy, 8)) pl.use_bulk = 0;
   pl.use_tma = encode_plane_map(&tmx, x, desc, pl.xs[0].stride, pl.xbf / pl.xs[0].stride, pl.P) &&
                encode_plane_map(&tmd, dy, desc, pl.ds[0].stride, pl.dbf / pl.ds[0].stride, pl.P);
+  apply_wait_hook(pl);
   cudaError_t e = wt::launch_bwd_weight(pl, tmx, tmd, desc->dtype, x, dy, w_base, b_base, w_sub, base_scale,
                                         wavelet_scale, dw_base, db_base, dw_sub, dbase_scale,
                                         dwavelet_scale, static_cast<float*>(ws), st);
@@ -1373,6 +1395,11 @@ const char* wtconv_status_string(wtconv_status_t s) {
 }
 
 const char* wtconv_last_error(void) { return g_last_error; }
+
+void wtconv_test_copy_timeout(int enable) {
+  std::lock_guard<std::mutex> lock(g_hook_mu);
+  g_hook_on = enable != 0;
+}
 
 unsigned int wtconv_device_faults(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return 0;

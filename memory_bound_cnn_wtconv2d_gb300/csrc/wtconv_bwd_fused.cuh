@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
     const int n0 = (u - cc * NB) * P;
     float* const dst = sm + s * pl.islot;
     fence_proxy_async();  // earlier generic accesses of the set precede the copies
-    mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes);
+    mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes + pl.dbg_extra_tx);
     tma_load_4d(dst, &tmx, -4, -R, cc, n0, &mbar[s]);
     tma_load_4d(dst + pl.xr, &tmd, -4, -R, cc, n0, &mbar[s]);
   };
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
     const int n0 = (u - cc * NB) * P;
     const int npp = min(P, pl.N - n0);
     fence_proxy_async();  // the widening reads of the staging area precede the copies
-    mbar_arrive_expect_tx(&mbar[0], 2u * (uint32_t)npp * pl.bulk_bytes);
+    mbar_arrive_expect_tx(&mbar[0], 2u * (uint32_t)npp * pl.bulk_bytes + pl.dbg_extra_tx);
     for (int g = 0; g < npp; ++g) {
       const size_t src = ((size_t)(n0 + g) * C + cc) * HWp;
       bulk_load(stage_x + g * HWp, x + src, pl.bulk_bytes, &mbar[0]);
@@ -152,14 +152,14 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
       float* const in_d = in_x + pl.xr;          // ... and dy planes
       if (tma) {
         if (tid == 0) {
-          const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u);
+          const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u, pl.wait_shift);
           parity ^= 1u << slot;
           if (ok && dbl && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
           s_ok = ok;
         }
       } else if (bulk) {
         if (tid == 0) {
-          s_ok = mbar_wait_bounded(&mbar[0], parity & 1u);
+          s_ok = mbar_wait_bounded(&mbar[0], parity & 1u, pl.wait_shift);
           parity ^= 1u;
         }
       } else if (cpa) {
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
         const int mb = bulk ? 0 : slot;
         if (tid == 0) {
           atomicAdd(&g_bwf_faults, 1u);
-          mbar_wait_bounded(&mbar[mb], ((parity >> mb) & 1u) ^ 1u);  // let the copies in flight land
+          mbar_wait_bounded(&mbar[mb], ((parity >> mb) & 1u) ^ 1u, pl.wait_shift);  // let the copies in flight land
         }
         __syncthreads();
         return;  // records are not written: the caller sees the fault count

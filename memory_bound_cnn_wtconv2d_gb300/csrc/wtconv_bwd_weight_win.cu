@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
     int cc, n0, ty0, tx0;
     decode(u, cc, n0, ty0, tx0);
     fence_proxy_async();  // earlier generic accesses of the destinations precede the copies
-    mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes);
+    mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes + pl.dbg_extra_tx);
     if (box32) {
       float* const dst = sm + s * pl.islot;
       tma_load_4d(dst, &tmx, tx0 - h - 4, ty0 - h - R, cc, n0, &mbar[s]);
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
       float* const in_d = in_x + pl.xr;          // ... and dy tiles
       if (boxed) {
         if (tid == 0) {
-          const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u);
+          const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u, pl.wait_shift);
           parity ^= 1u << slot;
           if (ok && dbl && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
           s_ok = ok;
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
       if (boxed && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
         if (tid == 0) {
           atomicAdd(&g_bww_faults, 1u);
-          mbar_wait_bounded(&mbar[slot], ((parity >> slot) & 1u) ^ 1u);  // let the copies in flight land
+          mbar_wait_bounded(&mbar[slot], ((parity >> slot) & 1u) ^ 1u, pl.wait_shift);  // let the copies in flight land
         }
         __syncthreads();
         return;  // records are not written: the caller sees the fault count

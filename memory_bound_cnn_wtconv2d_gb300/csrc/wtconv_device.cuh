@@ -630,12 +630,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* mbar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for phase `parity` of mbar to complete, giving up after about 2^31
-// clock cycles (about a second).  Returns false if it gave up.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* mbar, uint32_t parity) {
+// Waits for phase `parity` of mbar to complete, giving up after about
+// 2^shift clock cycles (shift = 31 in normal operation: about a second).
+// Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* mbar, uint32_t parity, int shift) {
   const long long t0 = clock64();
   while (!mbar_try_wait(mbar, parity)) {
-    if (clock64() - t0 > (1ll << 31)) return false;
+    if (clock64() - t0 > (1ll << shift)) return false;
   }
   return true;
 }

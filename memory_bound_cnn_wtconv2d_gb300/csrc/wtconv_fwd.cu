@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     const int cc = uu / pl.groups;
     const int nn = (uu - cc * pl.groups) * pl.P;
     fence_proxy_async();  // earlier generic accesses of the buffer set precede the copy
-    mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes);
+    mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes + pl.dbg_extra_tx);
     tma_load_4d(sm + s * pl.xslot, &tmx, -4, -R, cc, nn, &mbar[s]);
   };
   // 16-bit staged path: the raw planes of a unit land in the staging area
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     const int nn = (uu - cc * pl.groups) * pl.P;
     const int npp = min(pl.P, pl.N - nn);
     fence_proxy_async();  // the widening reads of the staging area precede the copies
-    mbar_arrive_expect_tx(&mbar[0], (uint32_t)npp * pl.bulk_bytes);
+    mbar_arrive_expect_tx(&mbar[0], (uint32_t)npp * pl.bulk_bytes + pl.dbg_extra_tx);
     for (int g = 0; g < npp; ++g)
       bulk_load(stage + g * HWp, x + ((size_t)(nn + g) * C + cc) * HWp, pl.bulk_bytes, &mbar[0]);
   };
@@ -140,14 +140,14 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     if (tma) {
       if (tid == 0) {
         if (!dbl && u != u_begin) issue(u, 0);  // single set: the previous unit is done with it
-        const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u);
+        const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u, pl.wait_shift);
         parity ^= 1u << slot;
         if (ok && dbl && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
         s_ok = ok;
       }
     } else if (bulk) {
       if (tid == 0) {
-        s_ok = mbar_wait_bounded(&mbar[0], parity & 1u);
+        s_ok = mbar_wait_bounded(&mbar[0], parity & 1u, pl.wait_shift);
         parity ^= 1u;
       }
     } else if (cpa) {
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
       const int mb = bulk ? 0 : slot;
       if (tid == 0) {
         atomicAdd(&g_fwd_faults, 1u);
-        mbar_wait_bounded(&mbar[mb], ((parity >> mb) & 1u) ^ 1u);  // let the copy in flight land
+        mbar_wait_bounded(&mbar[mb], ((parity >> mb) & 1u) ^ 1u, pl.wait_shift);  // let the copy in flight land
       }
       __syncthreads();
       break;

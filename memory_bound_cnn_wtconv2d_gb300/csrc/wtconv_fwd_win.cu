@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     int cc, nn, oy, ox;
     decode(uu, cc, nn, oy, ox);
     fence_proxy_async();  // earlier generic accesses of the destination precede the copy
-    mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes);
+    mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes + pl.dbg_extra_tx);
     if (box32) tma_load_4d(sm + s * pl.xslot, &tmx, ox - 4, oy - R, cc, nn, &mbar[s]);
     else tma_load_4d(sm + pl.stage_off, &tmx, ox, oy, cc, nn, &mbar[s]);
   };
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     if (boxed) {
       if (tid == 0) {
         if (box32 && !dbl && u != u_begin) issue(u, 0);  // single set: the previous unit is done with it
-        const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u);
+        const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u, pl.wait_shift);
         parity ^= 1u << slot;
         if (ok && dbl && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
         s_ok = ok;
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     if (boxed && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
       if (tid == 0) {
         atomicAdd(&g_win_faults, 1u);
-        mbar_wait_bounded(&mbar[slot], ((parity >> slot) & 1u) ^ 1u);  // let the copy in flight land
+        mbar_wait_bounded(&mbar[slot], ((parity >> slot) & 1u) ^ 1u, pl.wait_shift);  // let the copy in flight land
       }
       __syncthreads();
       break;

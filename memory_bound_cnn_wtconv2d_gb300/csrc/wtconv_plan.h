@@ -88,6 +88,13 @@ struct WtFwdPlan {
   int zo[WT_MAXL + 1];   // h >> l: the tile's first level-l coefficient row / column in the window
   int win_load;          // 0 = plain loads, 1 = float32 box copy (margins included), 2 = 16-bit box copy into
                          // the staging area, widened per unit
+  // Bounded waits on the plane copies give up after 2^wait_shift clock
+  // cycles; each copy barrier expects dbg_extra_tx bytes more than its copies
+  // deliver.  31 and 0 in normal operation (set at launch; the test hook
+  // wtconv_test_copy_timeout shortens the limit and arms the extra bytes so
+  // that every wait runs out).
+  int wait_shift;
+  uint32_t dbg_extra_tx;
 };
 
 // Parameter-gradient pass.  The work is C * batches units (channel c, batch
@@ -158,6 +165,8 @@ struct WtBwPlan {
   WtDiv dld_pp, dld_w;   // plain loads of the dy tile: items per tile, per row
   WtDiv dwd_pp, dwd_w;   // widening of the raw 16-bit dy tiles: items per tile, per row
   int stage_dx;          // 16-bit staging: floats from the staging area's start to the raw dy tiles
+  int wait_shift;        // as in WtFwdPlan
+  uint32_t dbg_extra_tx;
 };
 
 #define WT_SMEM_SLACK 128  // bytes added to every dynamic shared-memory size for 128-byte realignment

@@ -27,7 +27,7 @@ GRAD_NAMES = ("dw_base", "db_base", "dw_sub", "dbase_scale", "dwavelet_scale")
 # entry points declared in include/wtconv.h
 EXPORTS = ("wtconv_workspace_size", "wtconv_fwd", "wtconv_bwd_data", "wtconv_bwd_weight", "wtconv_bwd",
            "wtconv_bwd_weight_noalloc", "wtconv_status_string", "wtconv_last_error",
-           "wtconv_device_faults")
+           "wtconv_device_faults", "wtconv_test_copy_timeout")
 
 
 class WtconvDesc(ctypes.Structure):
@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.wtconv_last_error.restype = ctypes.c_char_p
         L.wtconv_device_faults.argtypes = []
         L.wtconv_device_faults.restype = ctypes.c_uint
+        L.wtconv_test_copy_timeout.argtypes = [ctypes.c_int]
+        L.wtconv_test_copy_timeout.restype = None
         _LIB = L
     return _LIB
 
@@ -301,3 +303,9 @@ def wtconv_device_faults() -> int:
     """In-kernel bounded waits that gave up since the previous call (0 in
     normal operation); synchronises the device and resets the count."""
     return int(lib().wtconv_device_faults())
+
+
+def wtconv_test_copy_timeout(enable: bool) -> None:
+    """Test support: while on, the kernels' bounded waits for their plane copies
+    run out on purpose (see include/wtconv.h); off restores normal operation."""
+    lib().wtconv_test_copy_timeout(1 if enable else 0)
