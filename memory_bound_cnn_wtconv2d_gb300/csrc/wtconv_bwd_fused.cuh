@@ -79,6 +79,12 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
     tma_load_4d(dst, &tmx, -4, -R, cc, n0, &mbar[s]);
     tma_load_4d(dst + pl.xr, &tmd, -4, -R, cc, n0, &mbar[s]);
   };
+  auto prefetch = [&](int u) {  // the boxes issue(u, .) will copy, into L2
+    const int cc = fdiv(u, pl.nb_div);
+    const int n0 = (u - cc * NB) * P;
+    tma_prefetch_4d(&tmx, -4, -R, cc, n0);
+    tma_prefetch_4d(&tmd, -4, -R, cc, n0);
+  };
   // 16-bit staged path (as in the parameter-gradient kernel): a unit's raw x
   // and dy planes land in the staging area (one bulk copy per plane on
   // mbar[0], or 8-byte cp.async chunks from every thread) and are widened
@@ -155,6 +161,7 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
           const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u, pl.wait_shift);
           parity ^= 1u << slot;
           if (ok && dbl && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
+          if (ok && !dbl && u + 1 < u_end) prefetch(u + 1);       // single set: the copy comes later, from L2
           s_ok = ok;
         }
       } else if (bulk) {

@@ -76,6 +76,12 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
     tma_load_4d(dst, &tmx, -4, -R, cc, n0, &mbar[s]);
     tma_load_4d(dst + pl.xr, &tmd, 0, 0, cc, n0, &mbar[s]);
   };
+  auto prefetch = [&](int u) {  // the boxes issue(u, .) will copy, into L2
+    const int cc = unit_c(u);
+    const int n0 = (u - cc * NB) * P;
+    tma_prefetch_4d(&tmx, -4, -R, cc, n0);
+    tma_prefetch_4d(&tmd, 0, 0, cc, n0);
+  };
   // 16-bit staged path: a unit's raw x and dy planes land in the staging area
   // (one bulk copy per plane on mbar[0], or 8-byte cp.async chunks from every
   // thread); the unit widens them into its input set, after which the next
@@ -169,6 +175,7 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
           const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u, pl.wait_shift);
           parity ^= 1u << slot;
           if (ok && dbl && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
+          if (ok && !dbl && u + 1 < u_end) prefetch(u + 1);       // single set: the copy comes later, from L2
           s_ok = ok;
         }
       } else if (bulk) {

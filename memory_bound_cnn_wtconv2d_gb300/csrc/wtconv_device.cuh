@@ -612,6 +612,18 @@ __device__ __forceinline__ void tma_load_4d(float* dst, const CUtensorMap* map, 
       : "memory");
 }
 
+// Hint: bring the 4-D box at (c0, c1, c2, c3) of `map` into L2 (no shared
+// memory, no completion to wait for; out-of-range parts are ignored).  A CTA
+// with one input set issues it for the next unit as soon as the current
+// unit's copy has landed, so the next copy, issued when the set is free
+// again, is served from L2.
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 // Contiguous global -> shared bulk copy (both addresses 16-byte aligned, size
 // a multiple of 16); completes `bytes` of transaction on mbar.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* mbar) {

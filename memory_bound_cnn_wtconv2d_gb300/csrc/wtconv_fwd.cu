@@ -81,6 +81,11 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     mbar_arrive_expect_tx(&mbar[s], pl.tma_bytes + pl.dbg_extra_tx);
     tma_load_4d(sm + s * pl.xslot, &tmx, -4, -R, cc, nn, &mbar[s]);
   };
+  auto prefetch = [&](int uu) {  // the box issue(uu, .) will copy, into L2
+    const int cc = uu / pl.groups;
+    const int nn = (uu - cc * pl.groups) * pl.P;
+    tma_prefetch_4d(&tmx, -4, -R, cc, nn);
+  };
   // 16-bit staged path: the raw planes of a unit land in the staging area
   // after the first input set (one bulk copy per plane on mbar[0], or 8-byte
   // cp.async chunks from every thread); they are widened into the first set at
@@ -143,6 +148,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
         const bool ok = mbar_wait_bounded(&mbar[slot], (parity >> slot) & 1u, pl.wait_shift);
         parity ^= 1u << slot;
         if (ok && dbl && u + 1 < u_end) issue(u + 1, slot ^ 1);  // the other set was last read by unit u-1
+        if (ok && !dbl && u + 1 < u_end) prefetch(u + 1);       // single set: the copy comes later, from L2
         s_ok = ok;
       }
     } else if (bulk) {
