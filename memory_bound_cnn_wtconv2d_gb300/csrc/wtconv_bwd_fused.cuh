@@ -79,6 +79,23 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
     tma_load_4d(dst, &tmx, -4, -R, cc, n0, &mbar[s]);
     tma_load_4d(dst + pl.xr, &tmd, -4, -R, cc, n0, &mbar[s]);
   };
+  // Single input set: the x planes are last read by the correlations, the dy
+  // planes by the final tiles, so the next unit's x box is requested as soon
+  // as the correlations are done (issue_x, which also arms the barrier for
+  // both boxes) and its dy box when the unit ends (issue_dy).
+  auto issue_x = [&](int u) {
+    const int cc = fdiv(u, pl.nb_div);
+    const int n0 = (u - cc * NB) * P;
+    fence_proxy_async();  // earlier generic accesses of the x planes precede the copy
+    mbar_arrive_expect_tx(&mbar[0], pl.tma_bytes + pl.dbg_extra_tx);
+    tma_load_4d(sm, &tmx, -4, -R, cc, n0, &mbar[0]);
+  };
+  auto issue_dy = [&](int u) {
+    const int cc = fdiv(u, pl.nb_div);
+    const int n0 = (u - cc * NB) * P;
+    fence_proxy_async();  // earlier generic accesses of the dy planes precede the copy
+    tma_load_4d(sm + pl.xr, &tmd, -4, -R, cc, n0, &mbar[0]);
+  };
   auto prefetch = [&](int u) {  // the boxes issue(u, .) will copy, into L2
     const int cc = fdiv(u, pl.nb_div);
     const int n0 = (u - cc * NB) * P;
@@ -276,11 +293,12 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
         }
       }
       __syncthreads();
+      if (tma && !dbl && tid == 0 && u + 1 < u_end) issue_x(u + 1);  // single set: its x planes are free
       // (c) Input gradient, final tiles: rotated base convolution of the dy
       // plane + synthesis, stored to dx.
       final_tiles<K, T, TP, NT>(fp, work, in_d, wsm, 0.f, dx, n0, c, np, tid, 0, 0, 0, fp.H, fp.W);
       __syncthreads();  // every read of this unit is done
-      if (tma && !dbl && tid == 0 && u + 1 < u_end) issue(u + 1, 0);  // single set: refill it now
+      if (tma && !dbl && tid == 0 && u + 1 < u_end) issue_dy(u + 1);  // single set: its dy planes are free
     }
     // Leaving channel c: tile sums -> shared memory (the work area) -> one
     // record per band -> this CTA's record slot for c.
