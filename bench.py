@@ -550,7 +550,8 @@ def run_suite(args):
                          "speedup_fwd_vs_dw7x7": round(t7 / tf, 3),
                          "speedup_fwd_bwd_vs_dw7x7": round(t7t / tt, 3)})
             del x, dy, out
-        line = {"suite": "large", "metric": "ms per call and per fwd+bwd step on planes beyond one CTA (tiled with a halo)",
+        line = {"suite": "large", "metric": "ms per call and per fwd+bwd step on planes beyond one CTA (tiled with a "
+                "halo; the deepest reaches as a fine pass plus a coarse layer)",
                 "rows": rows}
     else:
         N, dtype = 128, "f16"

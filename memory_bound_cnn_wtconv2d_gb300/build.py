@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libwtconv.so")
 SOURCES = ("wtconv_api.cu", "wtconv_fwd.cu", "wtconv_fwd_win.cu", "wtconv_bwd_weight.cu", "wtconv_bwd_weight_win.cu",
-           "wtconv_bwd_fused.cu", "wtconv_noalloc.cu")
+           "wtconv_bwd_fused.cu", "wtconv_noalloc.cu", "wtconv_split.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

@@ -3,6 +3,7 @@
 // include/wtconv.h.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -1084,6 +1085,199 @@ wtconv_status_t prepare_win(const wtconv_desc_t* d, WtFwdPlan& pl, CUtensorMap* 
   return WTCONV_OK;
 }
 
+// ---- Coarse-level split ------------------------------------------------------
+// A layer whose tile window does not fit one CTA runs as two layers (the
+// reasoning and the element-wise kernels are in wtconv_split.cu): the fine
+// pass, levels 1..s and the base convolution on the full planes; and the
+// coarse layer, levels s+1..L and no base convolution, on the float32 level-s
+// low-pass planes, whose output is added back block-replicated.  The coarse
+// layer's level l' is the original level s + l': same kernels w_sub, and
+// wavelet scales times 4^-s, so that its folded weights 4^-l' * s' * W equal
+// the original 4^-(s+l') * s * W; its wavelet-scale gradient is therefore 4^s
+// times the original's.
+
+int box_mode(const wtconv_desc_t* d) {
+  if (d->dtype == WTCONV_F32) return d->W % 4 == 0 ? 1 : 0;
+  return d->W % 8 == 0 ? 2 : 0;
+}
+
+// Whether a forward / input-gradient pass has a plan whatever the pointers'
+// alignment (whole planes, or tiles under every load mode).
+bool fwd_plannable(const wtconv_desc_t* d) {
+  WtFwdPlan pl;
+  if (plan_fwd(d, pl) == WTCONV_OK) return true;
+  const int m = box_mode(d);
+  return plan_win(d, pl, 0) == WTCONV_OK && (m == 0 || plan_win(d, pl, m) == WTCONV_OK);
+}
+
+bool bw_plannable(const wtconv_desc_t* d) {
+  WtBwPlan pl;
+  if (plan_bw(d, pl) == WTCONV_OK) return true;
+  const int m = box_mode(d);
+  return plan_bw_win(d, pl, 0) == WTCONV_OK && (m == 0 || plan_bw_win(d, pl, m) == WTCONV_OK);
+}
+
+wtconv_desc_t fine_desc(const wtconv_desc_t* d, int s) {
+  wtconv_desc_t f = *d;
+  f.levels = s;
+  return f;
+}
+
+// The coarse layer: float32 planes of ceil(H / 2^s) x ceil(W / 2^s).
+wtconv_desc_t coarse_desc(const wtconv_desc_t* d, int s) {
+  wtconv_desc_t c = *d;
+  c.H = (int)(((long)d->H + (1L << s) - 1) >> s);
+  c.W = (int)(((long)d->W + (1L << s) - 1) >> s);
+  c.levels = d->levels - s;
+  c.dtype = WTCONV_F32;
+  return c;
+}
+
+// Levels of the fine pass for a layer that has no plan of its own: the
+// largest s whose fine pass has a plan and whose coarse layer has one or
+// splits in turn (0 if the layer needs no split, or none works).  Each split
+// lowers the level count, so the recursion ends.
+int split_levels(const wtconv_desc_t* d, bool grad) {
+  bool (*plannable)(const wtconv_desc_t*) = grad ? bw_plannable : fwd_plannable;
+  if (plannable(d)) return 0;
+  for (int s = d->levels - 1; s >= 1; --s) {
+    const wtconv_desc_t f = fine_desc(d, s), c = coarse_desc(d, s);
+    if (plannable(&f) && (plannable(&c) || split_levels(&c, grad) > 0)) return s;
+  }
+  return 0;
+}
+
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Workspace of a split call, byte offsets (each 256-byte aligned):
+//   fine   the fine pass's own workspace (parameter gradients only);
+//   ll     low-pass planes of x (forward) or dy (input gradient) or x (parameter gradients);
+//   ll2    low-pass planes of dy (parameter gradients);
+//   carry  the coarse layer's output (forward, input gradient);
+//   zeros  the coarse layer's base kernels and base scales (C*k*k + C zeros);
+//   sw     its wavelet scales ((L-s)*4C);
+//   dummy  its base-kernel and base-scale gradients, discarded (parameter gradients);
+//   sub    its own workspace.
+struct SplitLayout {
+  size_t fine = 0, fine_bytes = 0, ll = 0, ll2 = 0, carry = 0, zeros = 0, sw = 0, dummy = 0, sub = 0, total = 0;
+};
+
+SplitLayout split_layout(const wtconv_desc_t* d, int op, int s) {
+  SplitLayout w;
+  const wtconv_desc_t f = fine_desc(d, s), c = coarse_desc(d, s);
+  const bool grad = op == WTCONV_OP_BWD_WEIGHT;
+  const size_t KK = (size_t)d->k * d->k, C = (size_t)d->C;
+  const size_t ll_bytes = 4 * (size_t)d->N * C * (size_t)c.H * (size_t)c.W;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  if (grad) {
+    w.fine_bytes = align256(wtconv_workspace_size(&f, WTCONV_OP_BWD_WEIGHT));
+    w.fine = take(w.fine_bytes);
+  }
+  w.ll = take(ll_bytes);
+  if (grad) w.ll2 = take(ll_bytes);
+  else w.carry = take(ll_bytes);
+  w.zeros = take(4 * (C * KK + C));
+  w.sw = take(4 * (size_t)(d->levels - s) * 4 * C);
+  if (grad) w.dummy = take(4 * (C * KK + C));
+  w.sub = take(wtconv_workspace_size(&c, grad ? WTCONV_OP_BWD_WEIGHT : op));
+  w.total = off;
+  return w;
+}
+
+size_t split_bytes(const wtconv_desc_t* d, int op) {
+  const int s = split_levels(d, op == WTCONV_OP_BWD_WEIGHT);
+  return s > 0 ? split_layout(d, op, s).total : 0;
+}
+
+wtconv_status_t split_workspace_ok(const SplitLayout& w, void* ws, size_t ws_bytes) {
+  if (!ws || ws_bytes < w.total)
+    return fail(WTCONV_ERR_WORKSPACE, "workspace of %zu B given, %zu B needed (coarse-level split)",
+                ws ? ws_bytes : 0, w.total);
+  if (!aligned(ws, 256)) return fail(WTCONV_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+  return WTCONV_OK;
+}
+
+// Zero base kernels and scales, and the scaled wavelet scales, of the coarse layer.
+wtconv_status_t split_params(const wtconv_desc_t* d, int s, const float* wavelet_scale, char* ws,
+                             const SplitLayout& w, cudaStream_t st) {
+  const size_t KK = (size_t)d->k * d->k, C = (size_t)d->C;
+  cudaError_t e = cudaMemsetAsync(ws + w.zeros, 0, 4 * (C * KK + C), st);
+  if (e == cudaSuccess)
+    e = wt::launch_scale(wavelet_scale + (size_t)s * 4 * C, reinterpret_cast<float*>(ws + w.sw),
+                         (d->levels - s) * 4 * d->C, ldexpf(1.f, -2 * s), st);
+  if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "coarse-level split: %s", cudaGetErrorString(e));
+  return WTCONV_OK;
+}
+
+// Forward (grad = false) or input gradient (grad = true) of a split layer.
+wtconv_status_t split_fwd(const wtconv_desc_t* d, int s, bool grad, const void* x, const float* w_base,
+                          const float* b_base, const float* w_sub, const float* base_scale,
+                          const float* wavelet_scale, void* y, void* ws, size_t ws_bytes, cudaStream_t st) {
+  const SplitLayout w = split_layout(d, grad ? WTCONV_OP_BWD_DATA : WTCONV_OP_FWD, s);
+  WT_TRY(split_workspace_ok(w, ws, ws_bytes));
+  const wtconv_desc_t f = fine_desc(d, s), c = coarse_desc(d, s);
+  char* b = static_cast<char*>(ws);
+  float* ll = reinterpret_cast<float*>(b + w.ll);
+  float* carry = reinterpret_cast<float*>(b + w.carry);
+  const float* wb0 = reinterpret_cast<const float*>(b + w.zeros);
+  const float* sb0 = wb0 + (size_t)d->C * d->k * d->k;
+  const float* sw = reinterpret_cast<const float*>(b + w.sw);
+  const float* wsub_c = w_sub + (size_t)s * 4 * d->C * d->k * d->k;
+  if (grad) {
+    WT_TRY(wtconv_bwd_data(&f, x, w_base, w_sub, base_scale, wavelet_scale, y, nullptr, 0, st));
+  } else {
+    WT_TRY(wtconv_fwd(&f, x, w_base, b_base, w_sub, base_scale, wavelet_scale, y, nullptr, 0, st));
+  }
+  WT_TRY(split_params(d, s, wavelet_scale, b, w, st));
+  cudaError_t e = wt::launch_lowpass(d->dtype, x, ll, (long long)d->N * d->C, d->H, d->W, s, st);
+  if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "coarse-level split: %s", cudaGetErrorString(e));
+  if (grad) {
+    WT_TRY(wtconv_bwd_data(&c, ll, wb0, wsub_c, sb0, sw, carry, b + w.sub, ws_bytes - w.sub, st));
+  } else {
+    WT_TRY(wtconv_fwd(&c, ll, wb0, nullptr, wsub_c, sb0, sw, carry, b + w.sub, ws_bytes - w.sub, st));
+  }
+  e = wt::launch_add_carry(d->dtype, y, carry, (long long)d->N * d->C, d->H, d->W, s, st);
+  if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "coarse-level split: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+// Parameter gradients of a split layer: the fine pass writes the base
+// gradients and levels 1..s, the coarse layer levels s+1..L (its wavelet-scale
+// gradient scaled by 4^-s afterwards).
+wtconv_status_t split_bw(const wtconv_desc_t* d, int s, const void* x, const void* dy, const float* w_base,
+                         const float* b_base, const float* w_sub, const float* base_scale,
+                         const float* wavelet_scale, float* dw_base, float* db_base, float* dw_sub,
+                         float* dbase_scale, float* dwavelet_scale, void* ws, size_t ws_bytes, cudaStream_t st) {
+  const SplitLayout w = split_layout(d, WTCONV_OP_BWD_WEIGHT, s);
+  WT_TRY(split_workspace_ok(w, ws, ws_bytes));
+  const wtconv_desc_t f = fine_desc(d, s), c = coarse_desc(d, s);
+  const size_t KK = (size_t)d->k * d->k, C = (size_t)d->C;
+  char* b = static_cast<char*>(ws);
+  float* llx = reinterpret_cast<float*>(b + w.ll);
+  float* lld = reinterpret_cast<float*>(b + w.ll2);
+  const float* wb0 = reinterpret_cast<const float*>(b + w.zeros);
+  const float* sb0 = wb0 + C * KK;
+  const float* sw = reinterpret_cast<const float*>(b + w.sw);
+  float* dwb0 = reinterpret_cast<float*>(b + w.dummy);
+  float* dsb0 = dwb0 + C * KK;
+  WT_TRY(wtconv_bwd_weight(&f, x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, dw_base, db_base, dw_sub,
+                           dbase_scale, dwavelet_scale, b + w.fine, w.fine_bytes, st));
+  WT_TRY(split_params(d, s, wavelet_scale, b, w, st));
+  cudaError_t e = wt::launch_lowpass(d->dtype, x, llx, (long long)d->N * d->C, d->H, d->W, s, st);
+  if (e == cudaSuccess) e = wt::launch_lowpass(d->dtype, dy, lld, (long long)d->N * d->C, d->H, d->W, s, st);
+  if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "coarse-level split: %s", cudaGetErrorString(e));
+  float* dsw_c = dwavelet_scale + (size_t)s * 4 * C;
+  WT_TRY(wtconv_bwd_weight(&c, llx, lld, wb0, nullptr, w_sub + (size_t)s * 4 * C * KK, sb0, sw, dwb0, nullptr,
+                           dw_sub + (size_t)s * 4 * C * KK, dsb0, dsw_c, b + w.sub, ws_bytes - w.sub, st));
+  e = wt::launch_scale(dsw_c, dsw_c, (d->levels - s) * 4 * d->C, ldexpf(1.f, -2 * s), st);
+  if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "coarse-level split: %s", cudaGetErrorString(e));
+  return ok();
+}
 
 }  // namespace
 
@@ -1162,8 +1356,11 @@ size_t wtconv_workspace_size(const wtconv_desc_t* desc, int op) {
     const wtconv_status_t st = plan_bwf(desc, pl, fp);
     if (st == WTCONV_OK) return bw_workspace_bytes(pl);
     if (st != WTCONV_ERR_UNSUPPORTED) return 0;
-    op = WTCONV_OP_BWD_WEIGHT;  // the call runs the two separate passes
+    // the call runs the two separate passes, one after the other, in the same workspace
+    return std::max(wtconv_workspace_size(desc, WTCONV_OP_BWD_DATA),
+                    wtconv_workspace_size(desc, WTCONV_OP_BWD_WEIGHT));
   }
+  if (op == WTCONV_OP_FWD || op == WTCONV_OP_BWD_DATA) return split_bytes(desc, op);
   if (op != WTCONV_OP_BWD_WEIGHT) return 0;
   WtBwPlan pl;
   const wtconv_status_t st = plan_bw(desc, pl);
@@ -1177,15 +1374,13 @@ size_t wtconv_workspace_size(const wtconv_desc_t* desc, int op) {
   for (int load = 0; load <= box; load += box > 0 ? box : 1) {
     if (plan_bw_win(desc, pl, load) == WTCONV_OK) bytes = std::max(bytes, bw_workspace_bytes(pl));
   }
-  return bytes;
+  return std::max(bytes, split_bytes(desc, WTCONV_OP_BWD_WEIGHT));
 }
 
 wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float* w_base,
                            const float* b_base, const float* w_sub, const float* base_scale,
                            const float* wavelet_scale, void* y, void* ws, size_t ws_bytes,
                            void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   WT_TRY(validate_desc(desc));
   WT_TRY(check_param(w_base, "w_base", false));
   WT_TRY(check_param(b_base, "b_base", true));
@@ -1193,8 +1388,13 @@ wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float
   WT_TRY(check_param(base_scale, "base_scale", false));
   WT_TRY(check_param(wavelet_scale, "wavelet_scale", false));
   WtFwdPlan pl;
-  WT_TRY(plan_any(desc, pl, x));
+  const wtconv_status_t pst = plan_any(desc, pl, x);
+  const int split = pst == WTCONV_ERR_UNSUPPORTED ? split_levels(desc, false) : 0;
+  if (split == 0) WT_TRY(pst);
   if (desc->N == 0) return ok();
+  if (split > 0)
+    return split_fwd(desc, split, false, x, w_base, b_base, w_sub, base_scale, wavelet_scale, y, ws, ws_bytes,
+                     (cudaStream_t)stream);
   WT_TRY(check_act(x, "x", desc));
   WT_TRY(check_act(y, "y", desc));
   alignas(64) CUtensorMap tmx;
@@ -1221,16 +1421,19 @@ wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const
                                 const float* w_sub, const float* base_scale,
                                 const float* wavelet_scale, void* dx, void* ws, size_t ws_bytes,
                                 void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   WT_TRY(validate_desc(desc));
   WT_TRY(check_param(w_base, "w_base", false));
   WT_TRY(check_param(w_sub, "w_sub", false));
   WT_TRY(check_param(base_scale, "base_scale", false));
   WT_TRY(check_param(wavelet_scale, "wavelet_scale", false));
   WtFwdPlan pl;
-  WT_TRY(plan_any(desc, pl, dy));
+  const wtconv_status_t pst = plan_any(desc, pl, dy);
+  const int split = pst == WTCONV_ERR_UNSUPPORTED ? split_levels(desc, false) : 0;
+  if (split == 0) WT_TRY(pst);
   if (desc->N == 0) return ok();
+  if (split > 0)
+    return split_fwd(desc, split, true, dy, w_base, nullptr, w_sub, base_scale, wavelet_scale, dx, ws, ws_bytes,
+                     (cudaStream_t)stream);
   WT_TRY(check_act(dy, "dy", desc));
   WT_TRY(check_act(dx, "dx", desc));
   alignas(64) CUtensorMap tmx;
@@ -1274,7 +1477,7 @@ wtconv_status_t wtconv_bwd(const wtconv_desc_t* desc, const void* x, const void*
   if (st == WTCONV_ERR_UNSUPPORTED || desc->N == 0) {
     // Planes beyond the fused kernel's working set (or an empty batch): the
     // two separate passes, with the same results.
-    WT_TRY(wtconv_bwd_data(desc, dy, w_base, w_sub, base_scale, wavelet_scale, dx, nullptr, 0, stream));
+    WT_TRY(wtconv_bwd_data(desc, dy, w_base, w_sub, base_scale, wavelet_scale, dx, ws, ws_bytes, stream));
     return wtconv_bwd_weight(desc, x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, dw_base, db_base,
                              dw_sub, dbase_scale, dwavelet_scale, ws, ws_bytes, stream);
   }
@@ -1321,7 +1524,9 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
   WT_TRY(check_param(dbase_scale, "dbase_scale", false));
   WT_TRY(check_param(dwavelet_scale, "dwavelet_scale", false));
   WtBwPlan pl;
-  WT_TRY(plan_bw_any(desc, pl, x, dy));
+  const wtconv_status_t pst = plan_bw_any(desc, pl, x, dy);
+  const int split = pst == WTCONV_ERR_UNSUPPORTED ? split_levels(desc, true) : 0;
+  if (split == 0) WT_TRY(pst);
   cudaStream_t st = (cudaStream_t)stream;
   const int C = desc->C, L = desc->levels, KK = desc->k * desc->k;
   if (desc->N == 0) {  // empty batch: every gradient is an empty sum
@@ -1333,6 +1538,9 @@ wtconv_status_t wtconv_bwd_weight(const wtconv_desc_t* desc, const void* x, cons
     if (e != cudaSuccess) return fail(WTCONV_ERR_CUDA, "wtconv_bwd_weight: %s", cudaGetErrorString(e));
     return ok();
   }
+  if (split > 0)
+    return split_bw(desc, split, x, dy, w_base, b_base, w_sub, base_scale, wavelet_scale, dw_base, db_base, dw_sub,
+                    dbase_scale, dwavelet_scale, ws, ws_bytes, st);
   WT_TRY(check_act(x, "x", desc));
   WT_TRY(check_act(dy, "dy", desc));
   alignas(64) CUtensorMap tmx, tmd;

@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
   if (bulk && tid == 0 && u_begin < u_end) issue_bulk(u_begin);
   if (cpa && u_begin < u_end) issue_cpa(u_begin);
   int c_prev = -1;
+  float bias = 0.f;  // folded bias of channel c_prev
   int slot = 0;
   const bool dbl = pl.nsets == 2;
   for (int u = u_begin; u < u_end; ++u, slot = (dbl && !staged) ? slot ^ 1 : 0) {
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
     float* const xs = sm + slot * pl.xslot;
     if (c != c_prev) {
       stage_weights<K, ROT>(wsm, wb, L, C, c, w_base, w_sub, s_base, s_w, tid, NT);
+      bias = (!ROT && b_base != nullptr) ? s_base[c] * b_base[c] : 0.f;
       c_prev = c;
     }
     if (tma) {
@@ -175,7 +177,6 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
         cp_async_commit();
       }
     }
-    const float bias = (!ROT && b_base != nullptr) ? s_base[c] * b_base[c] : 0.f;
     __syncthreads();  // planes of unit u and the weights are visible
     if ((tma || bulk) && !s_ok) {  // the copy did not complete in time: record it and stop (uniform exit)
       const int mb = bulk ? 0 : slot;

@@ -67,6 +67,17 @@ int bw_win_ctas_per_sm(const WtBwPlan& pl, int dtype);
 // dtype), read once from the runtime (0 when it cannot tell).
 int bw_win_regs(int k, int tbr, int dtype);
 
+// Coarse-level split (layers whose tile window does not fit one CTA):
+//   launch_lowpass: ll = block sums of x over 2^s x 2^s blocks (float32,
+//     planes x ceil(H / 2^s) x ceil(W / 2^s));
+//   launch_add_carry: y[i][j] += c[i >> s][j >> s] on every plane;
+//   launch_scale: out[i] = f * in[i] (in may equal out).
+cudaError_t launch_lowpass(int dtype, const void* x, float* ll, long long planes, int H, int W, int s,
+                           cudaStream_t stream);
+cudaError_t launch_add_carry(int dtype, void* y, const float* c, long long planes, int H, int W, int s,
+                             cudaStream_t stream);
+cudaError_t launch_scale(const float* in, float* out, int n, float f, cudaStream_t stream);
+
 // Sets the thread-local message returned by wtconv_last_error().
 void set_last_error(const char* msg);
 

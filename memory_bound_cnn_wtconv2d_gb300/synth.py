@@ -119,7 +119,9 @@ NETWORK_STAGES = ((96, 56, 3, 5), (192, 28, 3, 4), (384, 14, 9, 3), (768, 7, 3, 
 # maps.  (N, C, H, W, levels, k, dtype); every tensor is larger than the L2.
 LARGE_PLANES = ((16, 64, 224, 224, 1, 5, "f32"), (16, 64, 224, 224, 2, 5, "f32"), (16, 64, 224, 224, 3, 5, "f32"),
                 (16, 64, 224, 224, 4, 5, "f32"), (32, 64, 224, 224, 3, 5, "f16"), (32, 96, 128, 128, 3, 5, "f32"),
-                (16, 32, 384, 384, 2, 5, "f32"), (8, 32, 512, 512, 2, 5, "f16"))
+                (16, 32, 384, 384, 2, 5, "f32"), (8, 32, 512, 512, 2, 5, "f16"),
+                # reaches whose tile window does not fit one CTA: a fine pass and a coarse layer
+                (16, 64, 224, 224, 5, 5, "f32"), (16, 64, 224, 224, 6, 3, "f16"))
 
 
 def workload(name: str, **overrides) -> LayerInputs:

@@ -205,29 +205,56 @@ def _device_ctx(device):
     return torch.cuda.device(device)
 
 
-def wtconv_fwd(x, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k, y=None, stream=None):
+# Workspace bytes of the forward and input-gradient passes, per (layer,
+# pass): nonzero only for layers computed as a fine pass plus a coarse layer
+# (include/wtconv.h, "Limits"); the size does not depend on the device.
+_FWD_WS = {}
+
+
+def _fwd_workspace(desc, op, device, workspace):
+    """The workspace a forward / input-gradient call needs and its size in
+    bytes: the caller's, else a new one when the layer needs any, else
+    (None, 0).  The caller keeps the tensor alive until the call is enqueued."""
+    if workspace is not None:
+        return workspace, _workspace_bytes(workspace, device)
+    key = (desc.N, desc.C, desc.H, desc.W, desc.levels, desc.k, desc.dtype, op)
+    need = _FWD_WS.get(key)
+    if need is None:
+        need = _FWD_WS[key] = wtconv_workspace_size(desc, op)
+    if need == 0:
+        return None, 0
+    return torch.empty(need, dtype=torch.uint8, device=device), need
+
+
+def wtconv_fwd(x, w_base, b_base, w_sub, base_scale, wavelet_scale, levels, k, y=None, stream=None,
+               workspace=None):
     """y = WTConv2d(x)."""
     _act(x, "x")
     desc = desc_for(x, levels, k)
     ps = _params(x, levels, k, w_base, b_base, w_sub, base_scale, wavelet_scale)
     y = torch.empty_like(x) if y is None else _act(y, "y", like=x)
-    _disjoint([("y", y)], [("x", x), *zip(PARAM_NAMES, ps)])
+    outs = [("y", y)] + ([("workspace", workspace)] if workspace is not None else [])
+    _disjoint(outs, [("x", x), *zip(PARAM_NAMES, ps)])
     with _device_ctx(x.device):
-        _check(lib().wtconv_fwd(ctypes.byref(desc), _ptr(x), *map(_ptr, ps), _ptr(y), None, 0,
+        wt, wn = _fwd_workspace(desc, OP_FWD, x.device, workspace)
+        _check(lib().wtconv_fwd(ctypes.byref(desc), _ptr(x), *map(_ptr, ps), _ptr(y), _ptr(wt), wn,
                                 _stream(stream, x.device)))
     return y
 
 
-def wtconv_bwd_data(dy, w_base, w_sub, base_scale, wavelet_scale, levels, k, dx=None, stream=None):
+def wtconv_bwd_data(dy, w_base, w_sub, base_scale, wavelet_scale, levels, k, dx=None, stream=None,
+                    workspace=None):
     """dx = dL/dx for upstream gradient dy."""
     _act(dy, "dy")
     desc = desc_for(dy, levels, k)
     wb, _, ws_, sb, sw = _params(dy, levels, k, w_base, None, w_sub, base_scale, wavelet_scale)
     dx = torch.empty_like(dy) if dx is None else _act(dx, "dx", like=dy)
-    _disjoint([("dx", dx)], [("dy", dy), ("w_base", wb), ("w_sub", ws_), ("base_scale", sb), ("wavelet_scale", sw)])
+    outs = [("dx", dx)] + ([("workspace", workspace)] if workspace is not None else [])
+    _disjoint(outs, [("dy", dy), ("w_base", wb), ("w_sub", ws_), ("base_scale", sb), ("wavelet_scale", sw)])
     with _device_ctx(dy.device):
+        wt, wn = _fwd_workspace(desc, OP_BWD_DATA, dy.device, workspace)
         _check(lib().wtconv_bwd_data(ctypes.byref(desc), _ptr(dy), _ptr(wb), _ptr(ws_), _ptr(sb), _ptr(sw), _ptr(dx),
-                                     None, 0, _stream(stream, dy.device)))
+                                     _ptr(wt), wn, _stream(stream, dy.device)))
     return dx
 
 

@@ -51,11 +51,13 @@ def call_fwd(L, desc, x=FAKE, y=FAKE, w=FAKE):
     ("levels", 9, wtconv.WTCONV_ERR_INVALID_ARG), ("N", -1, wtconv.WTCONV_ERR_INVALID_ARG),
     ("C", 0, wtconv.WTCONV_ERR_INVALID_ARG), ("H", 0, wtconv.WTCONV_ERR_INVALID_ARG),
     ("dtype", 7, wtconv.WTCONV_ERR_INVALID_ARG), ("H", 8192, wtconv.WTCONV_ERR_UNSUPPORTED),
-    ("levels", 5, wtconv.WTCONV_ERR_UNSUPPORTED),
+    ("levels", 5, wtconv.WTCONV_ERR_WORKSPACE),
 ])
 def test_invalid_descriptors(L, field, value, code):
     # H = W = 8192: beyond 2^24 pixels per plane.  512 x 512 at 5 levels,
-    # k = 5: not one CTA, and a tile's window (64-pixel halo) neither.
+    # k = 5: not one CTA, and a tile's window (64-pixel halo) neither, so the
+    # layer is computed as a fine pass and a coarse layer, which needs a
+    # workspace (none given here).
     d = wtconv.make_desc(2, 3, 16, 16, 2, 5, 0)
     setattr(d, field, value)
     if field == "H" and value == 8192:

@@ -51,8 +51,10 @@ class FakeLib:
     wtconv_bwd = _record("wtconv_bwd")
     wtconv_bwd_weight_noalloc = _record("wtconv_bwd_weight_noalloc")
 
+    fwd_ws = 0  # forward / input-gradient workspace: none, as for every layer that needs no split
+
     def wtconv_workspace_size(self, desc, op):
-        return 4096
+        return self.fwd_ws if op in (wtconv.OP_FWD, wtconv.OP_BWD_DATA) else 4096
 
 
 @pytest.fixture
@@ -70,6 +72,7 @@ def fake(monkeypatch):
             lib.current = prev
 
     monkeypatch.setattr(wtconv, "_LIB", lib)
+    monkeypatch.setattr(wtconv, "_FWD_WS", {})
     monkeypatch.setattr(wtconv, "_on_cuda", lambda t: True)
     monkeypatch.setattr(wtconv, "_device_ctx", device_ctx)
     return lib
@@ -238,3 +241,24 @@ def test_module_checks_its_hyperparameters_at_construction():
             WTConv2d(4, **kw)
     with pytest.raises(ValueError):
         WTConv2d(0)
+
+
+def test_split_layers_get_a_forward_workspace(fake):
+    # a layer computed as a fine pass plus a coarse layer needs a workspace in
+    # the forward and input-gradient calls too: the binding sizes it from the
+    # library and passes it (or the caller's) with its byte count
+    fake.fwd_ws = 5000
+    inp, x, dy, ps = layer()
+    wb, bb, wsub, sb, sw = ps
+    wtconv.wtconv_fwd(x, *ps, 2, 5, stream=0)
+    args = fake.calls[-1][1]
+    assert ptr(args[8]) is not None and args[9] == 5000
+    wtconv.wtconv_bwd_data(dy, wb, wsub, sb, sw, 2, 5, stream=0)
+    args = fake.calls[-1][1]
+    assert ptr(args[7]) is not None and args[8] == 5000
+    own = torch.empty(6000, dtype=torch.uint8)
+    wtconv.wtconv_fwd(x, *ps, 2, 5, stream=0, workspace=own)
+    args = fake.calls[-1][1]
+    assert ptr(args[8]) == own.data_ptr() and args[9] == 6000
+    with pytest.raises(ValueError):  # a workspace may not overlap an input
+        wtconv.wtconv_bwd_data(dy, wb, wsub, sb, sw, 2, 5, stream=0, workspace=dy.view(torch.uint8))

@@ -247,23 +247,3 @@ def test_forward_and_input_gradient_at_maximum_plane(wt, N, C, H, W, L, k):
                                          (2, 2, 56, 55, 5, 7)])
 def test_all_passes_at_maximum_gradient_plane(wt, N, C, H, W, L, k):
     check_all(wt, synth.make_inputs(N, C, H, W, L, k, seed=H + W + L + k))
-
-
-def test_planes_beyond_the_limits_are_refused(wt):
-    # planes beyond one CTA run tile by tile, unless even one tile's window
-    # (a 64-pixel halo at 5 levels, k = 5) does not fit
-    inp = synth.make_inputs(1, 2, 224, 224, 5, 5, seed=1)
-    d = to_dev(inp)
-    with pytest.raises(wt.WtconvError) as e:
-        wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 5, 5)
-    assert e.value.status == wt.WTCONV_ERR_UNSUPPORTED
-    with pytest.raises(wt.WtconvError) as e:
-        wt.wtconv_bwd_weight(d["x"], d["dy"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"],
-                             d["wavelet_scale"], 5, 5)
-    assert e.value.status == wt.WTCONV_ERR_UNSUPPORTED
-    # the refusals launched nothing and left the context usable
-    inp = synth.make_inputs(1, 2, 57, 57, 3, 5, seed=2)
-    d = to_dev(inp)
-    y = wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 3, 5)
-    torch.cuda.synchronize()
-    compare("y", y.cpu().numpy(), oracle.fwd(inp), "f32", False)

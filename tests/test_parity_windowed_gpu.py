@@ -118,18 +118,10 @@ def test_windowed_parameter_gradient_is_deterministic_and_noalloc_agrees(wt):
         assert torch.equal(g1[name], g3[name]), name
 
 
-def test_reach_beyond_one_cta_is_refused(wt):
+def test_reach_beyond_one_cta_splits(wt):
     # 5 levels at k = 5 need a 64-pixel halo around every tile: even the
-    # smallest tile's window does not fit one CTA.  The refusal launches
-    # nothing and leaves the context usable.
-    inp = synth.make_inputs(1, 2, 224, 224, 5, 5, seed=3)
-    d = to_dev(inp)
-    for call in ("fwd", "bwd_weight"):
-        with pytest.raises(wt.WtconvError) as e:
-            if call == "fwd":
-                wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 5, 5)
-            else:
-                wt.wtconv_bwd_weight(d["x"], d["dy"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"],
-                                     d["wavelet_scale"], 5, 5)
-        assert e.value.status == wt.WTCONV_ERR_UNSUPPORTED
+    # smallest tile's window does not fit one CTA, so levels 5.. run as a
+    # coarse layer on the level-4 low-pass planes (tests/test_split_gpu.py);
+    # 4 levels still run tile by tile in one pass.
+    check_all(wt, synth.make_inputs(1, 2, 224, 224, 5, 5, seed=3))
     check_all(wt, synth.make_inputs(1, 2, 224, 224, 4, 5, seed=3))

@@ -1,0 +1,132 @@
+"""GPU parity of layers computed as a fine pass plus a coarse layer, against
+the float64 oracle.
+
+A layer whose tile window does not fit one CTA (a large plane with a deep
+pyramid and a wide kernel: a halo of 2^L * (k/2) pixels) runs levels 1..s and
+the base convolution on the full planes, and levels s+1..L as a layer of
+their own on the level-s low-pass planes (block sums over 2^s x 2^s), whose
+output is added back replicated over each block.  In the collapsed synthesis
+a pixel takes level l's coefficient at (i >> l, j >> l) with the sign bits of
+(i >> (l-1), j >> (l-1)); for l > s those are bits of (i >> s, j >> s), which
+is what makes the split exact up to rounding.
+
+Each case is checked three ways:
+  - every output of every pass against the oracle (tolerances of the
+    whole-plane tests), and each level of dw_sub and dwavelet_scale on its own,
+    so that a wrong coarse level cannot hide behind the larger fine ones;
+  - the coarse part alone: the base kernels and the fine levels' kernels set
+    to zero, so y and dx are the coarse layer's contribution only;
+  - the one-call backward (wtconv_bwd) against the two separate calls.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_cnn_wtconv2d_gb300 import synth
+
+from test_parity_gpu import GRADS, compare, to_dev, wt  # noqa: F401  (wt is a fixture)
+
+pytestmark = pytest.mark.gpu
+
+# (N, C, H, W, L, k, dtype, s): s = the fine pass's levels the library picks
+# (from the planner's limits: levels <= 4 at every k, 5 at k = 3, fewer for
+# 16-bit k = 9 gradients); recorded so a change of the split point is seen.
+CASES = [
+    (1, 2, 128, 128, 5, 5, "f32"),    # the 64-pixel halo case: split at 4
+    (2, 1, 130, 136, 5, 7, "f32"),    # ragged: odd block counts at the coarse levels
+    (1, 2, 160, 152, 6, 3, "f16"),    # k = 3: split at 5
+    (1, 2, 96, 100, 5, 9, "bf16"),    # whole-plane forward, split parameter gradient
+    (1, 1, 224, 224, 8, 5, "f32"),    # deepest pyramid: a 4-level coarse layer on 14 x 14 planes
+    (1, 1, 1024, 1024, 8, 9, "f16"),  # the coarse layer splits again
+]
+
+
+def ids(case):
+    return "x".join(map(str, case))
+
+
+def run_all(wt, inp, d):
+    L, k = inp.levels, inp.k
+    y = wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], L, k)
+    dx = wt.wtconv_bwd_data(d["dy"], d["w_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], L, k)
+    g = wt.wtconv_bwd_weight(d["x"], d["dy"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"],
+                             d["wavelet_scale"], L, k)
+    dx2, g2 = wt.wtconv_bwd(d["x"], d["dy"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"],
+                            d["wavelet_scale"], L, k)
+    torch.cuda.synchronize()
+    assert wt.wtconv_device_faults() == 0, "an in-kernel bounded wait gave up"
+    return y, dx, g, dx2, g2
+
+
+@pytest.mark.parametrize("case", CASES, ids=ids)
+def test_split_layer_matches_oracle(wt, case):
+    N, C, H, W, L, k, dtype = case
+    inp = synth.make_inputs(N, C, H, W, L, k, dtype=dtype, seed=H + 3 * W + 5 * L + k)
+    d = to_dev(inp)
+    y, dx, g, dx2, g2 = run_all(wt, inp, d)
+    y_ref = oracle.fwd(inp)
+    ref = oracle.bwd(inp)
+    compare("y", y.float().cpu().numpy(), y_ref, dtype, False)
+    compare("dx", dx.float().cpu().numpy(), ref["dx"], dtype, False)
+    for name in GRADS:
+        compare(name, g[name].cpu().numpy(), ref[name], dtype, True)
+    # every level of the wavelet-kernel and wavelet-scale gradients on its own
+    for l in range(L):
+        compare(f"dw_sub[{l}]", g["dw_sub"][l].cpu().numpy(), ref["dw_sub"][l], dtype, True)
+        compare(f"dwavelet_scale[{l}]", g["dwavelet_scale"][l].cpu().numpy(), ref["dwavelet_scale"][l], dtype, True)
+    # the one-call backward runs the same two passes
+    assert torch.equal(dx2, dx)
+    for name in GRADS:
+        assert torch.equal(g2[name], g[name]), name
+
+
+@pytest.mark.parametrize("case", CASES[:4], ids=ids)
+def test_coarse_part_alone(wt, case):
+    # base kernels and levels 1..L-1 zeroed: y and dx come from the deepest
+    # level only, which every split above computes in its coarse layer
+    N, C, H, W, L, k, dtype = case
+    inp = synth.make_inputs(N, C, H, W, L, k, dtype=dtype, seed=7 * H + W + L, bias=False)
+    inp.w_base[:] = 0
+    inp.w_sub[:L - 1] = 0
+    d = to_dev(inp)
+    y = wt.wtconv_fwd(d["x"], d["w_base"], None, d["w_sub"], d["base_scale"], d["wavelet_scale"], L, k)
+    dx = wt.wtconv_bwd_data(d["dy"], d["w_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], L, k)
+    torch.cuda.synchronize()
+    y_ref = oracle.fwd(inp)
+    assert np.abs(y_ref).max() > 0
+    compare("y", y.float().cpu().numpy(), y_ref, dtype, False)
+    compare("dx", dx.float().cpu().numpy(), oracle.bwd(inp)["dx"], dtype, False)
+
+
+def test_split_layer_empty_batch(wt):
+    inp = synth.make_inputs(0, 2, 128, 128, 5, 5, seed=3)
+    d = to_dev(inp)
+    y = wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 5, 5)
+    dx = wt.wtconv_bwd_data(d["dy"], d["w_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 5, 5)
+    g = wt.wtconv_bwd_weight(d["x"], d["dy"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"],
+                             d["wavelet_scale"], 5, 5)
+    torch.cuda.synchronize()
+    assert y.numel() == 0 and dx.numel() == 0
+    for name in GRADS:
+        assert torch.count_nonzero(g[name]) == 0, name
+
+
+def test_split_needs_its_workspace(wt):
+    # the forward of a split layer takes a workspace; a caller's that is too
+    # small is refused before anything is launched
+    inp = synth.make_inputs(1, 2, 128, 128, 5, 5, seed=5)
+    d = to_dev(inp)
+    desc = wt.desc_for(d["x"], 5, 5)
+    need = wt.wtconv_workspace_size(desc, wt.OP_FWD)
+    assert need > 0
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(wt.WtconvError) as e:
+        wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 5, 5,
+                      workspace=small)
+    assert e.value.status == wt.WTCONV_ERR_WORKSPACE
+    enough = torch.empty(need, dtype=torch.uint8, device="cuda")
+    y = wt.wtconv_fwd(d["x"], d["w_base"], d["b_base"], d["w_sub"], d["base_scale"], d["wavelet_scale"], 5, 5,
+                      workspace=enough)
+    torch.cuda.synchronize()
+    compare("y", y.cpu().numpy(), oracle.fwd(inp), "f32", False)
