@@ -50,10 +50,20 @@
  *     wtconv_fwd and wtconv_bwd_data, up to 56 px, or 64 px at levels = 1,
  *     for wtconv_bwd_weight, depending on k and levels).  Larger planes run
  *     in output tiles, each computed from a window of x (or dy) that adds a
- *     halo of 2^levels * (k/2) pixels, rounded up to 8, on every side.  That
- *     window must itself fit one CTA: levels <= 4 at every k, levels = 5 at
- *     k = 3.  Beyond that a call returns WTCONV_ERR_UNSUPPORTED before
- *     anything is launched.  N = 0 is a valid empty batch.
+ *     halo of 2^levels * (k/2) pixels, rounded up to 8, on every side.  When
+ *     that window does not fit one CTA either (levels >= 5 at k >= 5 and
+ *     levels >= 6 at k = 3; 16-bit layers at k = 9 from levels = 4), the
+ *     layer is computed as two: levels 1..s and the base convolution on the
+ *     full planes (s the deepest level count that fits), and levels s+1..L
+ *     as a layer of their own, without base convolution, on the float32
+ *     level-s low-pass planes (block sums over 2^s x 2^s pixels), whose
+ *     output is added back replicated over each block.  The collapsed
+ *     synthesis makes this exact up to rounding: for l > s, the coefficient
+ *     a pixel takes at level l and its sign bits depend on the pixel only
+ *     through (i >> s, j >> s).  Such calls need a workspace in every pass
+ *     (wtconv_workspace_size); 16-bit outputs are rounded twice (after the
+ *     fine pass and after adding the coarse part).  N = 0 is a valid empty
+ *     batch.
  *   - Pointers must be aligned to their element size (WTCONV_ERR_MISALIGNED
  *     otherwise); 16-byte alignment enables vector loads and stores.
  *   - Aliasing: no output (y, dx, a gradient, the workspace) may overlap an
@@ -111,7 +121,9 @@ size_t wtconv_workspace_size(const wtconv_desc_t* desc, int op);
  * Defined by the technical summary's "Methodology" (fused analysis +
  * depthwise conv, collapsed synthesis, folded scales) and "Problem
  * statement" (drop-in for a depthwise conv).  Needs no workspace (ws may be
- * NULL, ws_bytes 0). */
+ * NULL, ws_bytes 0), except for layers computed as a fine pass plus a coarse
+ * layer (see "Limits"): then ws must hold
+ * wtconv_workspace_size(desc, WTCONV_OP_FWD) bytes, 256-byte aligned. */
 wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float* w_base,
                            const float* b_base, const float* w_sub, const float* base_scale,
                            const float* wavelet_scale, void* y, void* ws, size_t ws_bytes,
@@ -121,7 +133,8 @@ wtconv_status_t wtconv_fwd(const wtconv_desc_t* desc, const void* x, const float
  * bias.  The summary's "Key contributions" report that the fused
  * implementation reproduces all gradients.  Because the Haar pair is
  * orthonormal and k is odd, A^T is the same fused pass with every kernel
- * rotated by 180 degrees, which is how it is computed.  Needs no workspace. */
+ * rotated by 180 degrees, which is how it is computed.  Workspace as for
+ * wtconv_fwd (WTCONV_OP_BWD_DATA). */
 wtconv_status_t wtconv_bwd_data(const wtconv_desc_t* desc, const void* dy, const float* w_base,
                                 const float* w_sub, const float* base_scale,
                                 const float* wavelet_scale, void* dx, void* ws, size_t ws_bytes,
