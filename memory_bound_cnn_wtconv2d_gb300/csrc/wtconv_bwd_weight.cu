@@ -243,6 +243,10 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
               const float* xw = in_x + g * XBF + Xb.off + p0 * Xb.stride + q0;
               const float* dw = in_d + g * DBF + Db.off + p0 * Db.stride + q0;
               gs[s] += corr_tile<K, TR, TC, 4 - R>(xw, Xb.stride, dw, Db.stride, acc[s]);
+            } else if (pl.Hs[l] <= 2 && pl.Ws[l] <= 2) {  // the whole band (at most 16 products)
+              const float* ps = work + g * WF;
+              tiny_band_corr<K>(ps + Xb.off + b * Xb.band + Xb.prow * Xb.stride + Xb.pcol, Xb.stride,
+                                ps + Db.off + b * Db.band + Db.prow * Db.stride + Db.pcol, Db.stride, acc[s]);
             } else {
               const float* ps = work + g * WF;
               corr_tile<K, TR, TC>(ps + Xb.off + b * Xb.band + p0 * Xb.stride + q0, Xb.stride,

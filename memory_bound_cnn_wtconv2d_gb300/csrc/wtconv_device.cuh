@@ -227,6 +227,56 @@ __device__ __forceinline__ float corr_tile(const float* __restrict__ win, int ws
   return dsum;
 }
 
+// Bands of at most 2 x 2 coefficients (the deep levels of small planes,
+// whose ceil-halved sizes end at 1 x 1): a k x k kernel on such a band only
+// ever meets the band's own <= 4 coefficients, so the convolution and the
+// correlation are at most 16 products, written out here instead of a whole
+// coefficient tile.  `y`, `x` and `d` point at the band's interior origin;
+// the band buffers keep zero margins around the interior, so the 2 x 2 block
+// read here is the band itself, zero-extended.
+//   z[p][q] = sum_{i,j} w[(i-p+r)*K + (j-q+r)] * y[i][j]            (p < Hl, q < Wl)
+template <int K>
+__device__ __forceinline__ void tiny_band_conv(const float* __restrict__ y, int ys, const float* __restrict__ w,
+                                               float* __restrict__ z, int zs, int Hl, int Wl) {
+  constexpr int R = K / 2;
+  const float v[2][2] = {{y[0], y[1]}, {y[ys], y[ys + 1]}};
+#pragma unroll
+  for (int p = 0; p < 2; ++p)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      if (p < Hl && q < Wl) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) acc = fmaf(w[(i - p + R) * K + (j - q + R)], v[i][j], acc);
+        z[p * zs + q] = acc;
+      }
+    }
+}
+
+//   acc[du*K+dv] += sum_{p,q} x[p+du-r][q+dv-r] * d[p][q]: every product of
+//   one of the band's x coefficients with one of its d coefficients lands on
+//   exactly one tap, so 16 products cover the whole correlation.
+template <int K>
+__device__ __forceinline__ void tiny_band_corr(const float* __restrict__ x, int xs, const float* __restrict__ d,
+                                               int ds, float (&acc)[K * K]) {
+  constexpr int R = K / 2;
+  const float xv[2][2] = {{x[0], x[1]}, {x[xs], x[xs + 1]}};
+  const float dv[2][2] = {{d[0], d[1]}, {d[ds], d[ds + 1]}};
+#pragma unroll
+  for (int p = 0; p < 2; ++p)
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float& a = acc[(i - p + R) * K + (j - q + R)];
+          a = fmaf(xv[i][j], dv[p][q], a);
+        }
+}
+
 // One Haar analysis level on the planes g < np of a CTA:
 //   dst_b[p][q] = sum_{u,v} sign_b(u,v) * src[2p+u][2q+v],  p < Hl, q < Wl
 // (unnormalised: the 1/2 per level is folded into the weights).  Reads past

@@ -221,6 +221,13 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
       const int p0 = tp * ZT, q0 = (t - tp * pl.ztc[l]) * ZT;
       float* ps = work + g * WF;
       const WtBuf Yb = pl.lev[l];
+      const int Hl = pl.Hs[l], Wl = pl.Ws[l];
+      if (Hl <= 2 && Wl <= 2) {  // the whole band is this item (at most 16 products)
+        const WtBuf Zb = pl.zb[l];
+        tiny_band_conv<K>(ps + Yb.off + b * Yb.band + Yb.prow * Yb.stride + Yb.pcol, Yb.stride,
+                          wsm + (1 + 4 * (l - 1) + b) * wb, ps + Zb.off + b * Zb.band, Zb.stride, Hl, Wl);
+        continue;
+      }
       float z[ZT][ZT];
 #pragma unroll
       for (int o = 0; o < ZT; ++o)
@@ -230,7 +237,6 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
                            wsm + (1 + 4 * (l - 1) + b) * wb, z);
       const WtBuf Zb = pl.zb[l];
       float* dst = ps + Zb.off + b * Zb.band + p0 * Zb.stride + q0;
-      const int Hl = pl.Hs[l], Wl = pl.Ws[l];
       if (p0 + ZT <= Hl && q0 + ZT <= Wl) {
 #pragma unroll
         for (int o = 0; o < ZT; ++o)

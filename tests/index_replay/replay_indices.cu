@@ -6,7 +6,8 @@
 // For each plan the replay walks the kernels' phases in order and recomputes
 // each index they form: input loads and box-copy geometry, the Haar analysis
 // reads and writes, the band-convolution and correlation windows, the final
-// tiles' reads of the Z buffers and of the input plane, the 16/8-byte vector
+// tiles' reads of the Z buffers and of the input plane (and the 2 x 2 blocks
+// of the bands of at most 2 x 2 coefficients), the 16/8-byte vector
 // stores to y / dx, the 16-bit staging areas, the mbarrier slots and the CTA
 // work ranges and record slots that the gradient finalize searches.  Every
 // access must stay inside its buffer, every read of a zero margin must hit a
@@ -140,6 +141,17 @@ static void check_fwd(int N, int C, int H, int W, int L, int K) {
   // band convolutions: windows must only see interior or untouched zero margin (true by construction: writes only interiors)
   for (int l = 1; l <= L; ++l) {
     const int NV = (ZT + K - 1 + 3) / 4;
+    if (pl.Hs[l] <= 2 && pl.Ws[l] <= 2) {  // tiny band: the 2x2 block at its interior origin, then its Z values
+      const WtBuf Y = pl.lev[l];
+      for (int b = 0; b < 4; ++b) {
+        for (int i = 0; i < 2; ++i) for (int j = 0; j < 2; ++j) {
+          acc_buf(Y, 4, b, i + Y.prow, j + Y.pcol, PF, "tiny-read");
+          if (!(i < pl.Hs[l] && j < pl.Ws[l])) CHECK(!written[Y.off + (long)b * Y.band + (i + Y.prow) * Y.stride + j + Y.pcol], "tiny reads non-zero margin");
+        }
+        for (int i = 0; i < pl.Hs[l]; ++i) for (int j = 0; j < pl.Ws[l]; ++j) wr(pl.zb[l], 4, b, i, j, "zconv-write");
+      }
+      continue;
+    }
     for (int b = 0; b < 4; ++b) for (int tp = 0; tp < pl.ztr[l]; ++tp) for (int tq = 0; tq < pl.ztc[l]; ++tq) {
       const int p0 = tp * ZT, q0 = tq * ZT;
       for (int a = 0; a < ZT + K - 1; ++a) for (int c = 0; c < 4 * NV; ++c) acc_buf(pl.lev[l], 4, b, p0 + a, q0 + c, PF, "zconv-read");
@@ -270,6 +282,11 @@ static void check_bw(int N, int C, int H, int W, int L, int K) {
         if (ii >= 0 && ii < H && jj >= 0 && jj < W && idx >= 0 && idx < XB) CHECK(xw[idx], "corr-x0 maps interior wrong");
       }
       for (int o = 0; o < TBR; ++o) for (int c = 0; c < TCW; ++c) acc_buf(pl.ds[0], 1, 0, p0 + o, q0 + c, DB, "corr-d0");
+    } else if (pl.Hs[l] <= 2 && pl.Ws[l] <= 2) {  // tiny band: 2x2 blocks at the interior origins
+      for (int i = 0; i < 2; ++i) for (int j = 0; j < 2; ++j) {
+        acc_buf(pl.xs[l], nb, b, i + pl.xs[l].prow, j + pl.xs[l].pcol, WF, "tiny-x");
+        acc_buf(pl.ds[l], nb, b, i + pl.ds[l].prow, j + pl.ds[l].pcol, WF, "tiny-d");
+      }
     } else {
       for (int a = 0; a < TBR + K - 1; ++a) for (int c = 0; c < 4 * NV; ++c) acc_buf(pl.xs[l], nb, b, p0 + a, q0 + c, WF, "corr-x");
       for (int o = 0; o < TBR; ++o) for (int c = 0; c < TCW; ++c) acc_buf(pl.ds[l], nb, b, p0 + o, q0 + c, WF, "corr-d");
