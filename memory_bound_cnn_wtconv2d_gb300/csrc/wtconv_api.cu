@@ -93,6 +93,15 @@ int place(WtBuf& b, int off, int er, int ec, int prow, int pcol, int nb, int min
   return off + nb * b.band;
 }
 
+// Bands of at most 2 x 2 coefficients are convolved and correlated from the
+// 2 x 2 block at their interior origin (tiny_band_conv / tiny_band_corr), and
+// the next level's analysis reads the same block; so their buffers need no
+// margin but one zero row and column after the interior: a 2 x 2 block in a
+// row of 4 floats.
+bool tiny_band(int h, int w) { return h <= 2 && w <= 2; }
+
+int place_tiny(WtBuf& b, int off) { return place(b, off, 2, 2, 0, 0, 4); }
+
 // Buffer geometry of the forward pass for final tiles of tp x WT_TQ level-1
 // positions (2tp x 2WT_TQ outputs).
 void fwd_geometry(const wtconv_desc_t* d, WtFwdPlan& pl, int tp) {
@@ -109,7 +118,8 @@ void fwd_geometry(const wtconv_desc_t* d, WtFwdPlan& pl, int tp) {
   for (int l = 1; l <= L; ++l) {
     pl.ztr[l] = ceil_div(pl.Hs[l], WT_ZT);
     pl.ztc[l] = ceil_div(pl.Ws[l], WT_ZT);
-    off = place(pl.lev[l], off, WT_ZT * pl.ztr[l], WT_ZT * pl.ztc[l], R, R, 4);
+    off = tiny_band(pl.Hs[l], pl.Ws[l]) ? place_tiny(pl.lev[l], off)
+                                        : place(pl.lev[l], off, WT_ZT * pl.ztr[l], WT_ZT * pl.ztc[l], R, R, 4);
     pl.zbegin[l + 1] = pl.zbegin[l] + 4 * pl.ztr[l] * pl.ztc[l];
   }
   pl.zipp = pl.zbegin[L + 1];
@@ -582,6 +592,11 @@ wtconv_status_t plan_bw_compute(const wtconv_desc_t* d, WtBwPlan& pl) {
   pl.dbf = place(pl.ds[0], 0, pl.tbr * pl.tr[0], pl.tcw * pl.tc[0], 0, 0, 1);
   int off = 0;
   for (int l = 1; l <= L; ++l) {
+    if (tiny_band(pl.Hs[l], pl.Ws[l])) {
+      off = place_tiny(pl.xs[l], off);
+      off = place_tiny(pl.ds[l], off);
+      continue;
+    }
     off = place(pl.xs[l], off, pl.tbr * pl.tr[l], pl.tcw * pl.tc[l], R, R, 4);
     off = place(pl.ds[l], off, pl.tbr * pl.tr[l], pl.tcw * pl.tc[l], 0, 0, 4);
   }

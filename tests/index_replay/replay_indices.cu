@@ -113,7 +113,7 @@ static void check_fwd(int N, int C, int H, int W, int L, int K) {
         acc_buf(pl.lev[0], 1, 0, 2 * p + u + R, 2 * q + v + 4, XF, "ana1-read");
         if (!(2 * p + u < H && 2 * q + v < W)) CHECK(!xwritten[pl.lev[0].off + (2 * p + u + R) * pl.lev[0].stride + 2 * q + v + 4], "ana1 reads non-zero margin");
       }
-      for (int b = 0; b < 4; ++b) wr(pl.lev[1], 4, b, p + R, q + R, "ana1-write");
+      for (int b = 0; b < 4; ++b) wr(pl.lev[1], 4, b, p + pl.lev[1].prow, q + pl.lev[1].pcol, "ana1-write");
     }
   } else {
     for (int P = 0; P < pl.Hs[2]; ++P) for (int Q = 0; Q < pl.Ws[2]; ++Q) {
@@ -123,19 +123,19 @@ static void check_fwd(int N, int C, int H, int W, int L, int K) {
       }
       for (int u = 0; u < 2; ++u) for (int v = 0; v < 2; ++v) {
         const int p = 2 * P + u, q = 2 * Q + v;
-        if (p < pl.Hs[1] && q < pl.Ws[1]) for (int b = 0; b < 4; ++b) wr(pl.lev[1], 4, b, p + R, q + R, "ana12-w1");
+        if (p < pl.Hs[1] && q < pl.Ws[1]) for (int b = 0; b < 4; ++b) wr(pl.lev[1], 4, b, p + pl.lev[1].prow, q + pl.lev[1].pcol, "ana12-w1");
       }
-      for (int b = 0; b < 4; ++b) wr(pl.lev[2], 4, b, P + R, Q + R, "ana12-w2");
+      for (int b = 0; b < 4; ++b) wr(pl.lev[2], 4, b, P + pl.lev[2].prow, Q + pl.lev[2].pcol, "ana12-w2");
     }
   }
   for (int l = 3; l <= L; ++l) {
     const WtBuf S = pl.lev[l - 1], D = pl.lev[l];
     for (int p = 0; p < pl.Hs[l]; ++p) for (int q = 0; q < pl.Ws[l]; ++q) {
       for (int u = 0; u < 2; ++u) for (int v = 0; v < 2; ++v) {
-        acc_buf(S, 4, 0, 2 * p + u + R, 2 * q + v + R, PF, "ana-read");
-        if (!(2 * p + u < pl.Hs[l - 1] && 2 * q + v < pl.Ws[l - 1])) CHECK(!written[S.off + (2 * p + u + R) * S.stride + 2 * q + v + R], "ana reads non-zero margin");
+        acc_buf(S, 4, 0, 2 * p + u + S.prow, 2 * q + v + S.pcol, PF, "ana-read");
+        if (!(2 * p + u < pl.Hs[l - 1] && 2 * q + v < pl.Ws[l - 1])) CHECK(!written[S.off + (2 * p + u + S.prow) * S.stride + 2 * q + v + S.pcol], "ana reads non-zero margin");
       }
-      for (int b = 0; b < 4; ++b) wr(D, 4, b, p + R, q + R, "ana-write");
+      for (int b = 0; b < 4; ++b) wr(D, 4, b, p + D.prow, q + D.pcol, "ana-write");
     }
   }
   // band convolutions: windows must only see interior or untouched zero margin (true by construction: writes only interiors)
