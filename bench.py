@@ -58,11 +58,12 @@ def fma_per_plane(H, W, L, k):
 # kernel of the step, from one ncu capture of the stage-1 layer, valid only
 # for the kernel sources they were taken on (hash below).
 MEASURED_TRAFFIC = {
-    "csrc_sha256": "0e0302296bcf78343303a5b4ad4f3022ce40e9ddcf8904b76a7795d53d030127",
+    "csrc_sha256": "389303727604e232b2b9f836cf89b206a1240d7de8f9915eb2a755da2ee791e9",
     "workload": "stage1",
     # fwd: fwd_kernel; bwd: the fused backward kernel (its finalize reads < 1 MB)
-    "bytes": {"fwd": 108_426_240, "bwd": 202_851_328},
+    "bytes": {"fwd": 108_204_544, "bwd": 203_060_736},
 }
+
 
 def csrc_sha256():
     import hashlib
