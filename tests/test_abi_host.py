@@ -170,3 +170,23 @@ def test_binding_argtypes_match_the_header(L):
                 assert t is ctypes.c_size_t, (name, decl, t)
             else:
                 assert t is ctypes.c_int, (name, decl, t)
+
+
+def test_split_layers_request_a_workspace_in_every_pass(L):
+    # Layers whose tile window does not fit one CTA run as a fine pass plus a
+    # coarse layer on the low-pass planes; their forward and input-gradient
+    # calls need a workspace then (the low-pass and coarse-output planes), and
+    # every pass's size covers the float32 low-pass planes at least.  Layers
+    # that fit need none in those passes.
+    split = wtconv.make_desc(2, 3, 512, 512, 5, 5, 0)  # 64-pixel halo at k = 5: split at 4 levels
+    low = 2 * 3 * (512 >> 4) * (512 >> 4) * 4          # float32 bytes of the level-4 low-pass planes
+    for op in (wtconv.OP_FWD, wtconv.OP_BWD_DATA):
+        assert L.wtconv_workspace_size(ctypes.byref(split), op) >= 2 * low  # low-pass planes + coarse output
+    assert L.wtconv_workspace_size(ctypes.byref(split), wtconv.OP_BWD_WEIGHT) >= 2 * low  # of x and of dy
+    assert L.wtconv_workspace_size(ctypes.byref(split), wtconv.OP_BWD) >= 2 * low
+    deep = wtconv.make_desc(1, 2, 1024, 1024, 8, 9, 1)  # the coarse layer splits again
+    assert L.wtconv_workspace_size(ctypes.byref(deep), wtconv.OP_FWD) > 0
+    for desc in (wtconv.make_desc(2, 3, 512, 512, 4, 5, 0), wtconv.make_desc(64, 96, 56, 56, 3, 5, 0),
+                 wtconv.make_desc(2, 3, 512, 512, 5, 3, 0)):
+        for op in (wtconv.OP_FWD, wtconv.OP_BWD_DATA):
+            assert L.wtconv_workspace_size(ctypes.byref(desc), op) == 0, (desc.H, desc.levels, desc.k, op)
