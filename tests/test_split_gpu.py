@@ -29,9 +29,9 @@ from test_parity_gpu import GRADS, compare, to_dev, wt  # noqa: F401  (wt is a f
 
 pytestmark = pytest.mark.gpu
 
-# (N, C, H, W, L, k, dtype, s): s = the fine pass's levels the library picks
-# (from the planner's limits: levels <= 4 at every k, 5 at k = 3, fewer for
-# 16-bit k = 9 gradients); recorded so a change of the split point is seen.
+# (N, C, H, W, L, k, dtype).  The fine pass takes the deepest level count
+# whose tile window fits one CTA: 4 at k = 5..9, 5 at k = 3, 3 for 16-bit
+# k = 9 (the comments give the split each case exercises).
 CASES = [
     (1, 2, 128, 128, 5, 5, "f32"),    # the 64-pixel halo case: split at 4
     (2, 1, 130, 136, 5, 7, "f32"),    # ragged: odd block counts at the coarse levels
@@ -130,3 +130,58 @@ def test_split_needs_its_workspace(wt):
                       workspace=enough)
     torch.cuda.synchronize()
     compare("y", y.cpu().numpy(), oracle.fwd(inp), "f32", False)
+
+
+def test_split_step_replays_from_a_cuda_graph(wt):
+    # The split calls enqueue a memset, small element-wise kernels and the
+    # fine and coarse layers' kernels on the caller's stream, nothing else:
+    # a whole step on caller-owned workspaces captures into a CUDA graph and
+    # replays bit for bit (new inputs copied into the captured buffers).
+    inp = synth.make_inputs(1, 2, 128, 128, 5, 5, seed=43)
+    d = to_dev(inp)
+    ps = [d[n] for n in ("w_base", "b_base", "w_sub", "base_scale", "wavelet_scale")]
+    x, dy = d["x"].clone(), d["dy"].clone()
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    g = {n: torch.empty_like(p) for n, p in zip(GRADS, ps)}
+    desc = wt.desc_for(x, 5, 5)
+    wsf = torch.empty(wt.wtconv_workspace_size(desc, wt.OP_FWD), dtype=torch.uint8, device="cuda")
+    wsb = torch.empty(wt.wtconv_workspace_size(desc, wt.OP_BWD), dtype=torch.uint8, device="cuda")
+
+    def step():
+        wt.wtconv_fwd(x, *ps, 5, 5, y=y, workspace=wsf)
+        wt.wtconv_bwd(x, dy, *ps, 5, 5, dx=dx, grads=g, workspace=wsb)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    x.copy_(torch.flip(d["x"], dims=[3]))
+    dy.copy_(torch.flip(d["dy"], dims=[2]))
+    graph.replay()
+    torch.cuda.synchronize()
+    got = (y.clone(), dx.clone(), {n: t.clone() for n, t in g.items()})
+    step()
+    torch.cuda.synchronize()
+    assert wt.wtconv_device_faults() == 0
+    assert torch.equal(got[0], y) and torch.equal(got[1], dx)
+    for n in GRADS:
+        assert torch.equal(got[2][n], g[n]), n
+
+
+def test_split_layer_through_the_no_alloc_entry_point(wt):
+    # the no-alloc entry point takes split layers whose scratch fits its
+    # 4 MiB array, with the same results bit for bit
+    inp = synth.make_inputs(1, 2, 128, 128, 5, 5, seed=47)
+    d = to_dev(inp)
+    ps = [d[n] for n in ("w_base", "b_base", "w_sub", "base_scale", "wavelet_scale")]
+    assert wt.wtconv_workspace_size(wt.desc_for(d["x"], 5, 5), wt.OP_BWD_WEIGHT) <= 4 << 20
+    ref = wt.wtconv_bwd_weight(d["x"], d["dy"], *ps, 5, 5)
+    got = wt.wtconv_bwd_weight_noalloc(d["x"], d["dy"], *ps, 5, 5)
+    torch.cuda.synchronize()
+    assert wt.wtconv_device_faults() == 0
+    for n in GRADS:
+        assert torch.equal(got[n], ref[n]), n
