@@ -185,3 +185,37 @@ def test_split_layer_through_the_no_alloc_entry_point(wt):
     assert wt.wtconv_device_faults() == 0
     for n in GRADS:
         assert torch.equal(got[n], ref[n]), n
+
+
+@pytest.mark.parametrize("which", ["both", "input_only", "params_only"])
+def test_split_layer_through_the_autograd_module(wt, which):
+    # the module's forward and each of its backward paths (one fused call, or
+    # the input / parameter gradient alone) size their workspaces for a split
+    from memory_bound_cnn_wtconv2d_gb300.layer import WTConv2d
+    torch.manual_seed(1)
+    m = WTConv2d(2, kernel_size=5, levels=5, device="cuda")
+    x = torch.randn(1, 2, 136, 128, device="cuda", requires_grad=which != "params_only")
+    if which == "input_only":
+        for p in m.parameters():
+            p.requires_grad_(False)
+    y = m(x)
+    dy = torch.randn_like(y)
+    y.backward(dy)
+    torch.cuda.synchronize()
+    assert wt.wtconv_device_faults() == 0
+    inp = synth.make_inputs(1, 2, 136, 128, 5, 5)
+    inp.x = x.detach().cpu().numpy()
+    inp.dy = dy.cpu().numpy()
+    inp.w_base = m.weight.detach().cpu().numpy()
+    inp.b_base = m.bias.detach().cpu().numpy()
+    inp.w_sub = m.wavelet_weight.detach().cpu().numpy()
+    inp.base_scale = m.base_scale.detach().cpu().numpy()
+    inp.wavelet_scale = m.wavelet_scale.detach().cpu().numpy()
+    compare("y", y.detach().cpu().numpy(), oracle.fwd(inp), "f32", False)
+    g = oracle.bwd(inp)
+    if which != "params_only":
+        compare("dx", x.grad.cpu().numpy(), g["dx"], "f32", False)
+    if which != "input_only":
+        compare("dw_base", m.weight.grad.cpu().numpy(), g["dw_base"], "f32", True)
+        compare("dw_sub", m.wavelet_weight.grad.cpu().numpy(), g["dw_sub"], "f32", True)
+        compare("dwavelet_scale", m.wavelet_scale.grad.cpu().numpy(), g["dwavelet_scale"], "f32", True)
