@@ -3,7 +3,8 @@
 The hand-picked cases elsewhere pin the planner's known corners; this sweep
 draws layers at random within the documented limits (planes up to 56 px
 at every level count; larger planes, which run in windowed tiles, with
-levels <= 4, or 5 at k = 3), so that plane grouping, final-tile heights,
+levels <= 4, or 5 at k = 3; and larger planes with deeper pyramids, which
+run as a fine pass plus a coarse layer), so that plane grouping, final-tile heights,
 input-set counts, load modes and the fused-or-separate backward choice meet
 combinations nobody picked.  Batch, channels, odd and even sizes, k, dtype
 and bias are drawn too.  Every call must accept its layer, and y, dx (from
@@ -42,12 +43,29 @@ def random_cases(n=96, seed=2026):
 CASES = random_cases()
 
 
+def random_split_cases(n=12, seed=2027):
+    """Larger planes with deep pyramids, whose tile window does not fit one CTA:
+    they run as a fine pass plus a coarse layer on the low-pass planes."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cases = []
+    for _ in range(n):
+        k = int(rng.choice([3, 5, 7, 9]))
+        H, W = (int(v) for v in rng.integers(113, 261, size=2))
+        L = int(rng.integers(6 if k == 3 else 5, 9))
+        N, C = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+        cases.append((N, C, H, W, L, k, DTYPES[int(rng.integers(0, 3))], bool(rng.random() < 0.8)))
+    return cases
+
+
+SPLIT_CASES = random_split_cases()
+
+
 def case_seed(case):
     return 7 + sum((i + 1) * v for i, v in enumerate(case[:6])) + 1000 * DTYPES.index(case[6])
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
+@pytest.mark.parametrize("case", CASES + SPLIT_CASES, ids=lambda c: "x".join(map(str, c)))
 def test_random_layer_all_entry_points(wt, case):
     N, C, H, W, L, k, dtype, bias = case
     inp = synth.make_inputs(N, C, H, W, L, k, dtype=dtype, seed=case_seed(case), bias=bias)
@@ -80,3 +98,7 @@ def test_cases_stay_within_the_documented_limits():
     assert any(max(c[2], c[3]) > 56 for c in CASES) and any(c[4] >= 6 for c in CASES)
     assert {c[5] for c in CASES} == {3, 5, 7, 9} and {c[6] for c in CASES} == set(DTYPES)
     assert {c[7] for c in CASES} == {True, False}
+    # the split draws: beyond one CTA, and deeper than one tile window reaches
+    for N, C, H, W, L, k, dtype, bias in SPLIT_CASES:
+        assert min(H, W) > 112 and L <= 8 and (L >= 5 if k > 3 else L >= 6)
+    assert {c[5] for c in SPLIT_CASES} == {3, 5, 7, 9} and {c[6] for c in SPLIT_CASES} == set(DTYPES)
