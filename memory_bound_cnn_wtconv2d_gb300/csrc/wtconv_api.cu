@@ -503,7 +503,7 @@ wtconv_status_t plan_win_compute(const wtconv_desc_t* d, WtFwdPlan& pl, int load
   pl.mb_off = round_up(pl.w_off + wfloats, 2);
   pl.smem_bytes = 4 * pl.mb_off + 16 + WT_SMEM_SLACK;
   pl.tma_bytes = load == 1 ? (uint32_t)(4L * P * pl.xf) : load == 2 ? (uint32_t)(2L * P * pl.Hs[0] * pl.Ws[0]) : 0u;
-  pl.wd_vec = 1;
+  pl.wd_vec = 4;
   pl.wd_pp = make_div(pl.Hs[0] * pl.Ws[0] / 4);
   pl.wd_w = make_div(pl.Ws[0] / 4);
   fwd_divs(pl);
@@ -927,7 +927,7 @@ wtconv_status_t plan_bw_win_compute(const wtconv_desc_t* d, WtBwPlan& pl, int lo
     pl.tcd[l] = make_div(pl.tc[l]);
   }
   pl.ipp = make_div(pl.items_per_plane);
-  pl.wd_vec = 1;
+  pl.wd_vec = 4;
   pl.wd_pp = make_div(pl.Hs[0] * pl.Ws[0] / 4);
   pl.wd_w = make_div(pl.Ws[0] / 4);
   pl.dwd_pp = make_div(pl.th * pl.tw / 4);
@@ -1066,8 +1066,8 @@ void set_bulk(Plan& pl, const wtconv_desc_t* d, const void* src, long capacity_b
   }
   pl.bulk_bytes = (uint32_t)plane;
   pl.cp_pp = make_div((int)(plane / 8 > 0 ? plane / 8 : 1));
-  pl.wd_vec = d->W % 4 == 0;
-  const int per_row = pl.wd_vec ? d->W / 4 : d->W;
+  pl.wd_vec = d->W % 4 == 0 ? 4 : (d->W % 2 == 0 ? 2 : 1);
+  const int per_row = d->W / pl.wd_vec;
   pl.wd_pp = make_div(d->H * per_row);
   pl.wd_w = make_div(per_row);
 }

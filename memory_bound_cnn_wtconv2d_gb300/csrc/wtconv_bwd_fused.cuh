@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
         return;  // records are not written: the caller sees the fault count
       }
       if (staged) {  // widen the raw planes, then start the next unit's copies
-        widen_planes<T>(in_x, XBF, pl.xs[0], stage_x, np, pl.H, pl.W, pl.wd_vec != 0, pl.wd_pp, pl.wd_w, tid, NT);
-        widen_planes<T>(in_d, DBF, pl.ds[0], stage_d, np, pl.H, pl.W, pl.wd_vec != 0, pl.wd_pp, pl.wd_w, tid, NT);
+        widen_planes<T>(in_x, XBF, pl.xs[0], stage_x, np, pl.H, pl.W, pl.wd_vec, pl.wd_pp, pl.wd_w, tid, NT);
+        widen_planes<T>(in_d, DBF, pl.ds[0], stage_d, np, pl.H, pl.W, pl.wd_vec, pl.wd_pp, pl.wd_w, tid, NT);
         __syncthreads();
         if (bulk && tid == 0 && u + 1 < u_end) issue_bulk(u + 1);
         if (cpa && u + 1 < u_end) issue_cpa(u + 1);

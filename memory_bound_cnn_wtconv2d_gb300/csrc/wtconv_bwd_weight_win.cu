@@ -149,8 +149,8 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
         return;  // records are not written: the caller sees the fault count
       }
       if (box16) {  // widen the raw windows and tiles, then request the next unit's
-        widen_planes<T>(in_x, XBF, pl.xs[0], stage_x, np, Hv, Wv, true, pl.wd_pp, pl.wd_w, tid, NT);
-        widen_planes<T>(in_d, DBF, pl.ds[0], stage_d, np, th, tw, true, pl.dwd_pp, pl.dwd_w, tid, NT);
+        widen_planes<T>(in_x, XBF, pl.xs[0], stage_x, np, Hv, Wv, 4, pl.wd_pp, pl.wd_w, tid, NT);
+        widen_planes<T>(in_d, DBF, pl.ds[0], stage_d, np, th, tw, 4, pl.dwd_pp, pl.dwd_w, tid, NT);
         __syncthreads();
         if (tid == 0 && u + 1 < u_end) issue(u + 1, 0);
       }

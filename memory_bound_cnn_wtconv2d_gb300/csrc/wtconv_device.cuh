@@ -386,14 +386,29 @@ __device__ __forceinline__ void haar_levels12(const float* sbase, int sps, float
 
 // Widen np raw 16-bit planes (H*W elements each, consecutive in `src`, as the
 // bulk copies leave them) into the float32 interiors of buffer B of each
-// plane slot.  `vec`: W % 4 == 0, 4 elements per item (8-byte loads, 16-byte
-// stores: B.pcol and B.stride are multiples of 4); else one element per item.
+// plane slot.  `per` elements per item: 4 when W % 4 == 0 (8-byte loads,
+// 16-byte stores: B.pcol and B.stride are multiples of 4), 2 when W is even
+// (4-byte loads, 8-byte stores), else 1; dpp and dw divide by the items per
+// plane and per row.
 template <typename T>
 __device__ __forceinline__ void widen_planes(float* dbase, int dps, const WtBuf B, const T* src, int np, int H,
-                                             int W, bool vec, const WtDiv& dpp, const WtDiv& dw, int tid,
+                                             int W, int per, const WtDiv& dpp, const WtDiv& dw, int tid,
                                              int nthreads) {
   const int HW = H * W;
-  if (vec) {
+  if (per == 2) {
+    const int Wv = W >> 1;
+    const int per_plane = H * Wv;
+    for (int it = tid; it < np * per_plane; it += nthreads) {
+      const int g = fdiv(it, dpp);
+      const int rem = it - g * per_plane;
+      const int i = fdiv(rem, dw);
+      const int j = (rem - i * Wv) << 1;
+      const uint32_t raw = *reinterpret_cast<const uint32_t*>(src + g * HW + i * W + j);
+      const T* h = reinterpret_cast<const T*>(&raw);
+      *reinterpret_cast<float2*>(dbase + g * dps + B.off + (i + B.prow) * B.stride + j + B.pcol) =
+          make_float2(to_f32(h[0]), to_f32(h[1]));
+    }
+  } else if (per == 4) {
     const int Wv = W >> 2;
     const int per_plane = H * Wv;
     for (int it = tid; it < np * per_plane; it += nthreads) {

@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
       break;
     }
     if (staged) {  // widen the raw planes, then start the next unit's copy
-      widen_planes<T>(xs, XF, pl.lev[0], stage, np, pl.H, pl.W, pl.wd_vec != 0, pl.wd_pp, pl.wd_w, tid, NT);
+      widen_planes<T>(xs, XF, pl.lev[0], stage, np, pl.H, pl.W, pl.wd_vec, pl.wd_pp, pl.wd_w, tid, NT);
       __syncthreads();
       if (bulk && tid == 0 && u + 1 < u_end) issue_bulk(u + 1);
       if (cpa && u + 1 < u_end) issue_cpa(u + 1);

@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, 3)
       break;
     }
     if (box16) {  // widen the raw windows, then request the next unit's
-      widen_planes<T>(xs, XF, pl.lev[0], reinterpret_cast<const T*>(sm + pl.stage_off), np, Hv, Wv, true,
+      widen_planes<T>(xs, XF, pl.lev[0], reinterpret_cast<const T*>(sm + pl.stage_off), np, Hv, Wv, 4,
                       pl.wd_pp, pl.wd_w, tid, NT);
       __syncthreads();
       if (tid == 0 && u + 1 < u_end) issue(u + 1, 0);

@@ -67,7 +67,7 @@ struct WtFwdPlan {
   int use_bulk;          // 16-bit planes are staged raw, then widened: 1 = bulk copies, 2 = 8-byte cp.async
   uint32_t bulk_bytes;   // bytes of one raw 16-bit plane (H*W*2: a multiple of 16, or of 8 for cp.async)
   WtDiv cp_pp;           // 8-byte chunks per raw plane (H*W/4), for the cp.async staging
-  int wd_vec;            // widening works on 4-element items (W % 4 == 0)
+  int wd_vec;            // elements per widening item: 4 (W % 4 == 0), 2 (W even) or 1
   WtDiv wd_pp, wd_w;     // widening: items per plane, items per row
   WtDiv ld_pp, ld_w;     // plane load: items per plane, items per row
   WtDiv an_pp[WT_MAXL + 1], an_w[WT_MAXL + 1];  // analysis at level l (l = 2: the fused 1+2 pass)
@@ -137,7 +137,7 @@ struct WtBwPlan {
   int use_bulk;          // 16-bit planes are staged raw, then widened: 1 = bulk copies, 2 = 8-byte cp.async
   uint32_t bulk_bytes;   // bytes of one raw 16-bit plane (H*W*2: a multiple of 16, or of 8 for cp.async)
   WtDiv cp_pp;           // 8-byte chunks per raw plane (H*W/4), for the cp.async staging
-  int wd_vec;            // widening works on 4-element items (W % 4 == 0)
+  int wd_vec;            // elements per widening item: 4 (W % 4 == 0), 2 (W even) or 1
   WtDiv wd_pp, wd_w;     // widening: items per plane, items per row
   int nbands;            // 1 + 4L
   int part_stride;       // floats per (group, channel) partial record = nbands*(k*k+1)

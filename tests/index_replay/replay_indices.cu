@@ -95,7 +95,9 @@ static void check_fwd(int N, int C, int H, int W, int L, int K) {
     if (pl.use_bulk) {
       CHECK((long)pl.P * H * W * 2 <= 4L * (pl.work_off - pl.stage_off), "staging beyond its region");
       CHECK(pl.bulk_bytes % (pl.use_bulk == 1 ? 16 : 8) == 0 && (pl.xslot * 4) % 128 == 0, "staging alignment");
-      if (pl.wd_vec) CHECK(W % 4 == 0 && (H * W) % 4 == 0, "widen vector alignment");
+      if (pl.wd_vec == 4) CHECK(W % 4 == 0 && (H * W) % 4 == 0, "widen vector alignment");
+      if (pl.wd_vec == 2) CHECK(W % 2 == 0 && pl.lev[0].pcol % 2 == 0 && pl.lev[0].stride % 2 == 0 && XF % 2 == 0, "widen pair alignment");
+      CHECK(pl.wd_vec == (W % 4 == 0 ? 4 : W % 2 == 0 ? 2 : 1), "widen item width");
       for (int g = 0; g < pl.P; ++g) CHECK(((long)g * H * W * 2) % (pl.use_bulk == 1 ? 16 : 8) == 0, "staging plane alignment");
     }
   }
@@ -209,7 +211,8 @@ static void check_bw(int N, int C, int H, int W, int L, int K) {
     set_bulk(pl, &d, (const void*)(uintptr_t)4096, 4L * (pl.work_off - pl.stage_off) / 2);
     CHECK(pl.use_bulk && pl.bulk_bytes % 8 == 0 && (pl.use_bulk == 2 || 2L * pl.P * pl.bulk_bytes < (1L << 20)), "bw staging eligibility");
     CHECK(2L * pl.P * H * W * 2 <= 4L * (pl.work_off - pl.stage_off), "bw staging capacity");
-    if (pl.wd_vec) CHECK(pl.ds[0].pcol % 4 == 0 && pl.xs[0].pcol % 4 == 0 && W % 4 == 0, "bw widen alignment");
+    if (pl.wd_vec == 4) CHECK(pl.ds[0].pcol % 4 == 0 && pl.xs[0].pcol % 4 == 0 && W % 4 == 0, "bw widen alignment");
+    if (pl.wd_vec == 2) CHECK(pl.ds[0].pcol % 2 == 0 && pl.xs[0].pcol % 2 == 0 && pl.xs[0].stride % 2 == 0 && pl.ds[0].stride % 2 == 0 && W % 2 == 0 && XB % 2 == 0 && DB % 2 == 0, "bw widen pair alignment");
     CHECK(pl.nsets == 1, "16-bit uses one input set");
   }
   CHECK(pl.P * WF <= pl.red_floats && pl.red_floats % 4 == 0 && pl.work_off + pl.red_floats == pl.mb_off, "work region");
@@ -639,7 +642,8 @@ static void check_bwf(int N, int C, int H, int W, int L, int K, int dtype) {
       const long xo = 4L * pl.stage_off + 2L * g * H * W, dof = dyoff + 2L * g * H * W;
       CHECK(xo % (pl.use_bulk == 1 ? 16 : 8) == 0 && dof % (pl.use_bulk == 1 ? 16 : 8) == 0, "staging plane alignment");
     }
-    if (pl.wd_vec) CHECK(W % 4 == 0 && pl.xs[0].pcol % 4 == 0 && pl.ds[0].pcol % 4 == 0, "widen alignment");
+    if (pl.wd_vec == 4) CHECK(W % 4 == 0 && pl.xs[0].pcol % 4 == 0 && pl.ds[0].pcol % 4 == 0, "widen alignment");
+    if (pl.wd_vec == 2) CHECK(W % 2 == 0 && pl.xs[0].pcol % 2 == 0 && pl.ds[0].pcol % 2 == 0 && XB % 2 == 0 && DB % 2 == 0, "widen pair alignment");
     pl.use_bulk = 0;
   }
   CHECK(pl.red_floats >= P * WF && pl.red_floats >= P * pl.items_per_plane * (KK + 1) && pl.red_floats % 4 == 0, "red");
