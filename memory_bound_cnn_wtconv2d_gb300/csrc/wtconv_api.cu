@@ -597,7 +597,10 @@ wtconv_status_t plan_bw_compute(const wtconv_desc_t* d, WtBwPlan& pl) {
       off = place_tiny(pl.ds[l], off);
       continue;
     }
-    off = place(pl.xs[l], off, pl.tbr * pl.tr[l], pl.tcw * pl.tc[l], R, R, 4);
+    // x bands: no left margin (a row's right margin is the next row's left
+    // one, 4 zero floats ahead of the buffer serve its first row), so every
+    // level's correlation window starts 4 - r floats after a 16-byte boundary
+    off = place(pl.xs[l], off + 4, pl.tbr * pl.tr[l], pl.tcw * pl.tc[l] + R, R, 0, 4);
     off = place(pl.ds[l], off, pl.tbr * pl.tr[l], pl.tcw * pl.tc[l], 0, 0, 4);
   }
   pl.wf = round_up(off, 4);
@@ -700,7 +703,11 @@ wtconv_status_t plan_bwf_compute(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan
   for (int l = 1; l <= L; ++l) {
     fp.ztr[l] = ceil_div(pl.Hs[l], WT_ZT);
     fp.ztc[l] = ceil_div(pl.Ws[l], WT_ZT);
-    off = place(pl.xs[l], off, pl.tbr * pl.tr[l], 4 * pl.tc[l], R, R, 4);
+    // x bands: no left margin.  A row's right margin (at least r zero
+    // columns) is the next row's left one, and 4 zero floats ahead of the
+    // buffer serve its first row; the correlation then reads every level
+    // at the same offset from a 16-byte boundary.
+    off = place(pl.xs[l], off + 4, pl.tbr * pl.tr[l], 4 * pl.tc[l] + R, R, 0, 4);
     off = place(pl.ds[l], off, std::max(pl.tbr * pl.tr[l], WT_ZT * fp.ztr[l]),
                 std::max(4 * pl.tc[l], WT_ZT * fp.ztc[l]), R, 4, 4);
     fp.zbegin[l + 1] = fp.zbegin[l] + 4 * fp.ztr[l] * fp.ztc[l];
@@ -767,14 +774,16 @@ wtconv_status_t plan_bwf_compute(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan
 // correlation tiles; pl.halo set.  x window: (th + 2h) x (tw + 2h) pixels
 // with r zero rows above and below and a 4-float margin left and right (the
 // float32 box copy fills exactly this); dy tile: th x tw, no margin.  x
-// level buffers: no top margin, a column margin (r - zo) mod 4 that puts
-// every correlation window's first column on a 16-byte boundary, and room
-// for the rows and float4 columns the last correlation tiles read past the
-// window; dy level buffers: the tile's coefficients rounded up to whole
-// correlation tiles (the rounding margin stays zero).
+// level buffers: no top margin, a column margin (-zo) mod 4 that puts every
+// correlation window's first column 4 - r floats after a 16-byte boundary
+// (as in the raw window, whose tile origin is zo[0] = h), and room for the
+// rows and columns the last correlation tiles read past the window; dy level
+// buffers: the tile's coefficients rounded up to whole correlation tiles
+// (the rounding margin stays zero).  Both strides of the bands are 4 mod 8
+// floats: the 4-row correlation tiles of a warp then start 16 banks apart
+// from one tile row to the next instead of on the same banks.
 void bw_win_geometry(const wtconv_desc_t* d, WtBwPlan& pl, int th, int tw, int tbr) {
   const int R = d->k / 2, L = d->levels, h = pl.halo;
-  const int NV = (4 + d->k - 1 + 3) / 4;  // float4s per row of a correlation window
   pl.th = th;
   pl.tw = tw;
   pl.tbr = tbr;
@@ -796,6 +805,7 @@ void bw_win_geometry(const wtconv_desc_t* d, WtBwPlan& pl, int th, int tw, int t
   pl.items_per_plane = pl.item_begin[L + 1];
   pl.xbf = place(pl.xs[0], 0, pl.Hs[0], pl.Ws[0], R, 4, 1);
   pl.dbf = place(pl.ds[0], 0, th, tw, 0, 0, 1);
+  pl.zo[0] = h;
   int off = 0;
   for (int l = 1; l <= L; ++l) {
     const int zo = h >> l;
@@ -803,13 +813,14 @@ void bw_win_geometry(const wtconv_desc_t* d, WtBwPlan& pl, int th, int tw, int t
     WtBuf& b = pl.xs[l];
     b.off = off;
     b.prow = 0;
-    b.pcol = ((R - zo) % 4 + 4) % 4;
+    b.pcol = (4 - zo % 4) % 4;
     const int rows = std::max(pl.Hs[l], zo + tbr * pl.tr[l] + R);
-    const int cols = std::max(b.pcol + pl.Ws[l], zo + 4 * (pl.tc[l] - 1) - R + b.pcol + 4 * NV);
+    const int cols = std::max(b.pcol + pl.Ws[l], zo + 4 * pl.tc[l] + R + b.pcol);
     b.stride = round_up(cols, 4);
+    if (b.stride % 8 == 0) b.stride += 4;
     b.band = rows * b.stride;
     off += 4 * b.band;
-    off = place(pl.ds[l], off, tbr * pl.tr[l], 4 * pl.tc[l], 0, 0, 4);
+    off = place(pl.ds[l], off, tbr * pl.tr[l], 4 * pl.tc[l], 0, 0, 4, 4 * pl.tc[l] % 8 == 0 ? 4 * pl.tc[l] + 4 : 0);
   }
   pl.wf = round_up(off, 4);
 }

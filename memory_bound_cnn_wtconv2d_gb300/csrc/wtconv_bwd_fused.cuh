@@ -241,17 +241,17 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
             const int t = rel - b * tiles;
             const int tp = fdiv(t, pl.tcd[l]);
             const int p0 = tp * TR, q0 = (t - tp * pl.tc[l]) * TC;
+            // One correlation instance serves every level: x's interior
+            // starts pcol floats into a row (4 for the raw plane, 0 for the
+            // bands, whose left margin is the previous row's right one), so
+            // the window starts 4 - r floats after a 16-byte boundary.
             const WtBuf Xb = pl.xs[l], Db = pl.ds[l];
-            if (l == 0) {  // raw planes; both interiors start 4 floats into each row
-              const float* xw = in_x + g * XBF + Xb.off + p0 * Xb.stride + q0;
-              const float* dw = in_d + g * DBF + Db.off + (p0 + Db.prow) * Db.stride + q0 + Db.pcol;
-              gs[s] += corr_tile<K, TR, TC, 4 - R>(xw, Xb.stride, dw, Db.stride, acc[s]);
-            } else {
-              const float* ps = work + g * WF;
-              corr_tile<K, TR, TC>(ps + Xb.off + b * Xb.band + p0 * Xb.stride + q0, Xb.stride,
-                                   ps + Db.off + b * Db.band + (p0 + Db.prow) * Db.stride + q0 + Db.pcol, Db.stride,
-                                   acc[s]);
-            }
+            const float* xb = l == 0 ? in_x + g * XBF : work + g * WF + b * Xb.band;
+            const float* db = l == 0 ? in_d + g * DBF : work + g * WF + b * Db.band;
+            const float sum = corr_tile<K, TR, TC, 4 - R>(xb + Xb.off + p0 * Xb.stride + q0 + Xb.pcol - 4, Xb.stride,
+                                                          db + Db.off + (p0 + Db.prow) * Db.stride + q0 + Db.pcol,
+                                                          Db.stride, acc[s]);
+            if (l == 0) gs[s] += sum;
           }
         }
       }

@@ -194,18 +194,19 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
             const int t = rel - b * tiles;
             const int tp = fdiv(t, pl.tcd[l]);
             const int p0 = tp * TR, q0 = (t - tp * pl.tc[l]) * TC;
+            // One instance for every level: the tile's origin sits zo floats
+            // into the level's window interior (h for the raw window), which
+            // starts pcol floats into a row with zo + pcol a multiple of 4, so
+            // the correlation window starts 4 - r floats after a 16-byte
+            // boundary.  The dy tile and its bands have no margins.
             const WtBuf Xb = pl.xs[l], Db = pl.ds[l];
-            if (l == 0) {  // raw x window: interior column 0 sits 4 floats into each row, h is a multiple of 4
-              const float* xw = in_x + g * XBF + Xb.off + (h + p0) * Xb.stride + h + q0;
-              const float* dw = in_d + g * DBF + Db.off + p0 * Db.stride + q0;
-              gs[s] += corr_tile<K, TR, TC, 4 - R>(xw, Xb.stride, dw, Db.stride, acc[s]);
-            } else {
-              const int zo = pl.zo[l];
-              const float* ps = work + g * WF;
-              corr_tile<K, TR, TC>(
-                  ps + Xb.off + b * Xb.band + (zo + p0 - R + Xb.prow) * Xb.stride + zo + q0 - R + Xb.pcol, Xb.stride,
-                  ps + Db.off + b * Db.band + p0 * Db.stride + q0, Db.stride, acc[s]);
-            }
+            const int zo = pl.zo[l];
+            const float* xb = l == 0 ? in_x + g * XBF : work + g * WF + b * Xb.band;
+            const float* db = l == 0 ? in_d + g * DBF : work + g * WF + b * Db.band;
+            const float sum = corr_tile<K, TR, TC, 4 - R>(
+                xb + Xb.off + (zo + p0 - R + Xb.prow) * Xb.stride + zo + q0 + Xb.pcol - 4, Xb.stride,
+                db + Db.off + p0 * Db.stride + q0, Db.stride, acc[s]);
+            if (l == 0) gs[s] += sum;
           }
         }
       }

@@ -121,6 +121,7 @@ struct WtBwPlan {
   int item_begin[WT_MAXL + 2];  // first tile item of level l within a plane (l = 0..L), [L+1] = total
   int items_per_plane;
   WtBuf xs[WT_MAXL + 1];  // shifted operand: x (l = 0: r zero rows, 4 zero columns) and its level-l bands, pad r
+                          // (whole-plane plans: r zero rows and a right margin only, which is the next row's left one)
   WtBuf ds[WT_MAXL + 1];  // unshifted operand: dy (l = 0, pad 0) and its level-l bands, pad 0
   int xbf, dbf;          // floats per raw x plane / raw dy plane (= one TMA box row set of one plane)
   int xr;                // offset of the dy planes within an input set (128-byte multiple)

@@ -275,7 +275,6 @@ static void check_bw(int N, int C, int H, int W, int L, int K) {
     const int p0 = tp * TBR, q0 = (t - tp * pl.tc[l]) * TCW;
     const int nb = l == 0 ? 1 : 4;
     CHECK(b < nb, "item band %d >= %d", b, nb);
-    const int NV = (TCW + K - 1 + 3) / 4;
     if (l == 0) {  // window columns q0 + (4-R) + c, c < TC+K-1; interior column = that - 4
       for (int a = 0; a < TBR + K - 1; ++a) for (int c = 0; c < TCW + K - 1; ++c) {
         acc_buf(pl.xs[0], 1, 0, p0 + a, q0 + 4 - R + c, XB, "corr-x0");
@@ -291,10 +290,27 @@ static void check_bw(int N, int C, int H, int W, int L, int K) {
         acc_buf(pl.ds[l], nb, b, i + pl.ds[l].prow, j + pl.ds[l].pcol, WF, "tiny-d");
       }
     } else {
-      for (int a = 0; a < TBR + K - 1; ++a) for (int c = 0; c < 4 * NV; ++c) acc_buf(pl.xs[l], nb, b, p0 + a, q0 + c, WF, "corr-x");
+      // x bands: pcol 0, reads left of a row's interior land in the previous
+      // row's right margin or in the 4 floats ahead of the buffer
+      const WtBuf X = pl.xs[l];
+      CHECK(X.pcol == 0 && X.prow == R && X.off % 4 == 0 && X.stride >= TCW * pl.tc[l] + R, "x band margins");
+      CHECK(((X.off + (long)b * X.band + (long)p0 * X.stride + q0 + X.pcol - 4) % 4) == 0, "corr-x align");
+      for (int a = 0; a < TBR + K - 1; ++a) for (int c = 0; c < TCW + K - 1; ++c) {
+        const int p = p0 + a - R, q = q0 + c - R;
+        const long k = X.off + (long)b * X.band + (long)(p + X.prow) * X.stride + q + X.pcol;
+        CHECK(k >= X.off - 4 && k < X.off + 4L * X.band && k >= 0 && k < WF, "corr-x outside x region");
+        const bool inside = p >= 0 && p < pl.Hs[l] && q >= 0 && q < pl.Ws[l];
+        bool interior = false;
+        if (k >= X.off) {  // decode: an interior position of some band of level l?
+          const long rel = k - X.off, bi = rel / X.band, r = (rel % X.band) / X.stride - X.prow, cc = (rel % X.band) % X.stride - X.pcol;
+          interior = r >= 0 && r < pl.Hs[l] && cc >= 0 && cc < pl.Ws[l];
+          if (inside) CHECK(bi == b && r == p && cc == q, "corr-x maps interior wrong");
+        }
+        if (!inside) CHECK(!interior, "corr-x margin (%d,%d) l=%d is an interior", p, q, l);
+      }
       for (int o = 0; o < TBR; ++o) for (int c = 0; c < TCW; ++c) acc_buf(pl.ds[l], nb, b, p0 + o, q0 + c, WF, "corr-d");
     }
-    CHECK(((pl.xs[l].off + p0 * pl.xs[l].stride + q0) % 4) == 0, "corr-x align");
+    if (l == 0) CHECK(((pl.xs[l].off + p0 * pl.xs[l].stride + q0) % 4) == 0, "corr-x align");
     CHECK(((pl.ds[l].off + p0 * pl.ds[l].stride + q0) % 4) == 0, "corr-d align");
   }
   for (int B = 0; B < pl.nbands; ++B) {
@@ -578,7 +594,7 @@ static void check_bw_win(int N, int C, int H, int W, int L, int K, int mode, int
       }
   }
   // correlations
-  const int NV = (4 + K - 1 + 3) / 4;
+  CHECK(pl.zo[0] == h, "level-0 tile origin");
   for (int l = 0; l <= L; ++l) {
     const WtBuf Xb = pl.xs[l], Db = pl.ds[l];
     const int nb = l == 0 ? 1 : 4;
@@ -602,9 +618,9 @@ static void check_bw_win(int N, int C, int H, int W, int L, int K, int mode, int
         }
       } else {
         const int zo = pl.zo[l];
-        const int r0 = zo + p0 - R + Xb.prow, c0 = zo + q0 - R + Xb.pcol;
+        const int r0 = zo + p0 - R + Xb.prow, c0 = zo + q0 + Xb.pcol - 4;  // aligned base; OFF = 4 - R
         CHECK(r0 >= 0 && c0 >= 0 && c0 % 4 == 0 && idx(Xb, b, r0, c0) % 4 == 0, "xl window align");
-        for (int a = 0; a < TR + K - 1; ++a) for (int c = 0; c < 4 * NV; ++c) acc_buf(Xb, 4, b, r0 + a, c0 + c, WF, "corr xl");
+        for (int a = 0; a < TR + K - 1; ++a) for (int c = 0; c < 4 + K - 1; ++c) acc_buf(Xb, 4, b, r0 + a, c0 + 4 - R + c, WF, "corr xl");
         for (int o = 0; o < TR; ++o) for (int j = 0; j < 4; ++j) {
           if (!(p0 + o < pl.dHs[l] && q0 + j < pl.dWs[l])) continue;
           for (int du = 0; du < K; ++du) for (int dv = 0; dv < K; ++dv) {
@@ -656,7 +672,7 @@ static void check_bwf(int N, int C, int H, int W, int L, int K, int dtype) {
   CHECK(pl.tma_bytes == 4u * P * (XB + DB), "tma bytes");
   CHECK(fp.xf == DB && fp.wf == WF && fp.L == L && fp.C == C && fp.H == H && fp.W == W, "fwd view");
   for (int l = 0; l <= L; ++l) CHECK(fp.lev[l].off == pl.ds[l].off && fp.lev[l].stride == pl.ds[l].stride && fp.lev[l].band == pl.ds[l].band && fp.lev[l].prow == pl.ds[l].prow && fp.lev[l].pcol == pl.ds[l].pcol, "fwd view lev");
-  for (int l = 1; l <= L; ++l) CHECK(pl.ds[l].pcol == 4 && pl.ds[l].prow == R && pl.xs[l].pcol == R && pl.xs[l].prow == R, "level margins");
+  for (int l = 1; l <= L; ++l) CHECK(pl.ds[l].pcol == 4 && pl.ds[l].prow == R && pl.xs[l].pcol == 0 && pl.xs[l].prow == R && pl.xs[l].off % 4 == 0, "level margins");
   // shadow: owner tags in the work area (1 x pyramid, 2 dy pyramid, 3 Z) and written flags
   std::vector<char> own(WF, 0), wr(WF, 0), xw(XB, 0), dw(DB, 0);
   auto tag = [&](const WtBuf& b, int nb, int t) { for (long i = b.off; i < b.off + (long)nb * b.band; ++i) { CHECK(i >= 0 && i < WF, "region beyond work area"); if (i >= 0 && i < WF) { CHECK(own[i] == 0, "regions overlap"); own[i] = t; } } };
@@ -727,9 +743,16 @@ static void check_bwf(int N, int C, int H, int W, int L, int K, int dtype) {
       CHECK(idx(Xb, 0, p0, q0) % 4 == 0, "x0 align");
       for (int a = 0; a < TR + K - 1; ++a) for (int c = 0; c < 4 + K - 1; ++c) rd(Xb, 0, 0, p0 + a - R, q0 + c - R, "corr x0", false, xw, XB);
     } else {
-      CHECK(idx(Xb, b, p0, q0) % 4 == 0, "xl align");
-      for (int a = 0; a < TR + K - 1; ++a) for (int c = 0; c < 4 * NV; ++c) acc_buf(Xb, 4, b, p0 + a, q0 + c, WF, "corr xl span");
-      for (int a = 0; a < TR + K - 1; ++a) for (int c = 0; c < 4 + K - 1; ++c) rd(Xb, b, l, p0 + a - R, q0 + c - R, "corr xl", true, wr, WF);
+      CHECK(idx(Xb, b, p0, q0 + Xb.pcol - 4) % 4 == 0, "xl align");
+      for (int a = 0; a < TR + K - 1; ++a) for (int c = 0; c < 4 + K - 1; ++c) {
+        const int p = p0 + a - R, q = q0 + c - R;
+        const long k = idx(Xb, b, p + Xb.prow, q + Xb.pcol);
+        CHECK(k >= Xb.off - 4 && k < Xb.off + 4L * Xb.band && k >= 0 && k < WF, "corr xl outside x region");
+        if (k < 0 || k >= WF) continue;
+        const bool inside = p >= 0 && p < pl.Hs[l] && q >= 0 && q < pl.Ws[l];
+        if (inside) CHECK(wr[k] && own[k] == 1, "corr xl unwritten interior");
+        else CHECK(!wr[k] && (own[k] == 1 || own[k] == 0), "corr xl margin written (%d,%d) l=%d", p, q, l);
+      }
     }
   }
   // band convolutions of the dy pyramid
