@@ -81,6 +81,13 @@ void level_sizes(const wtconv_desc_t* d, int* Hs, int* Ws) {
   }
 }
 
+// A row stride of n floats or more that is 4 mod 8: rows 4 apart then start
+// 16 banks apart.
+int pad48(int n) {
+  const int s = round_up(n, 4);
+  return s % 8 == 0 ? s + 4 : s;
+}
+
 // Places a plane buffer of `nb` bands at `off`; the interior is er x ec with
 // prow/pcol zero rows/columns before it and at least as many after it; rows
 // are padded to `min_stride` floats and to a multiple of 4.  Returns the next offset.
@@ -698,29 +705,35 @@ wtconv_status_t plan_bwf_compute(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan
   const int cols0 = std::max(4 * pl.tc[0], 2 * WT_TQ * fp.ftc);
   pl.xbf = place(pl.xs[0], 0, pl.tbr * pl.tr[0], 4 * pl.tc[0], R, 4, 1);
   pl.dbf = place(pl.ds[0], 0, rows0, cols0, R, 4, 1, cols0 + 8);
-  int off = 0;
-  fp.zbegin[1] = 0;
-  for (int l = 1; l <= L; ++l) {
-    fp.ztr[l] = ceil_div(pl.Hs[l], WT_ZT);
-    fp.ztc[l] = ceil_div(pl.Ws[l], WT_ZT);
-    // x bands: no left margin.  A row's right margin (at least r zero
-    // columns) is the next row's left one, and 4 zero floats ahead of the
-    // buffer serve its first row; the correlation then reads every level
-    // at the same offset from a 16-byte boundary.
-    off = place(pl.xs[l], off + 4, pl.tbr * pl.tr[l], 4 * pl.tc[l] + R, R, 0, 4);
-    off = place(pl.ds[l], off, std::max(pl.tbr * pl.tr[l], WT_ZT * fp.ztr[l]),
-                std::max(4 * pl.tc[l], WT_ZT * fp.ztc[l]), R, 4, 4);
-    fp.zbegin[l + 1] = fp.zbegin[l] + 4 * fp.ztr[l] * fp.ztc[l];
-  }
-  fp.zipp = fp.zbegin[L + 1];
-  for (int l = 1; l <= L; ++l) {
-    // Z^l: written at p < H_l, q < W_l; read by the final tiles at
-    // (p >> (l-1), q >> (l-1)) for every level-1 position of the tile grid.
-    const int fr = ((tp * fp.ftr - 1) >> (l - 1)) + 1, fc = ((WT_TQ * fp.ftc - 1) >> (l - 1)) + 1;
-    off = place(fp.zb[l], off, std::max(pl.Hs[l], fr), std::max(pl.Ws[l], fc), 0, 0, 4);
-  }
-  pl.wf = fp.wf = round_up(off, 4);
-  for (int l = 0; l <= L; ++l) fp.lev[l] = pl.ds[l];
+  // Work area: per level the x bands, the dy bands and (after all levels)
+  // the Z buffers.  With pad, the dy bands' strides are 4 mod 8 floats, so
+  // the 4-row band-convolution tiles of a warp start 16 banks apart; the
+  // padding is kept only where it costs no planes per unit.
+  auto work_geometry = [&](bool pad) {
+    int off = 0;
+    fp.zbegin[1] = 0;
+    for (int l = 1; l <= L; ++l) {
+      fp.ztr[l] = ceil_div(pl.Hs[l], WT_ZT);
+      fp.ztc[l] = ceil_div(pl.Ws[l], WT_ZT);
+      // x bands: no left margin.  A row's right margin (at least r zero
+      // columns) is the next row's left one, and 4 zero floats ahead of the
+      // buffer serve its first row; the correlation then reads every level
+      // at the same offset from a 16-byte boundary.
+      off = place(pl.xs[l], off + 4, pl.tbr * pl.tr[l], 4 * pl.tc[l] + R, R, 0, 4);
+      const int dcols = std::max(4 * pl.tc[l], WT_ZT * fp.ztc[l]);
+      off = place(pl.ds[l], off, std::max(pl.tbr * pl.tr[l], WT_ZT * fp.ztr[l]), dcols, R, 4, 4,
+                  pad ? pad48(dcols + 8) : 0);
+      fp.zbegin[l + 1] = fp.zbegin[l] + 4 * fp.ztr[l] * fp.ztc[l];
+    }
+    fp.zipp = fp.zbegin[L + 1];
+    for (int l = 1; l <= L; ++l) {
+      // Z^l: written at p < H_l, q < W_l; read by the final tiles at
+      // (p >> (l-1), q >> (l-1)) for every level-1 position of the tile grid.
+      const int fr = ((tp * fp.ftr - 1) >> (l - 1)) + 1, fc = ((WT_TQ * fp.ftc - 1) >> (l - 1)) + 1;
+      off = place(fp.zb[l], off, std::max(pl.Hs[l], fr), std::max(pl.Ws[l], fc), 0, 0, 4);
+    }
+    pl.wf = fp.wf = round_up(off, 4);
+  };
   fp.xf = pl.dbf;
   fp.w_band = round_up(KK, 4);
   const int wfloats = (1 + 4 * L) * fp.w_band;
@@ -745,18 +758,32 @@ wtconv_status_t plan_bwf_compute(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan
     pl.tma_bytes = (uint32_t)(4L * P * (pl.xbf + pl.dbf));
   };
   const long two_per_sm = kSmemPerSm / 2 - 1024 - kStaticSmem;
-  bool found = false;
-  for (int q = pl.P; q >= 1 && !found; --q)
-    for (int ns = staging ? 1 : 2; ns >= 1 && !found; --ns) {
-      layout(q, ns);
-      found = pl.smem_bytes <= two_per_sm;
+  const int p_max = pl.P;
+  auto fit = [&]() {
+    for (int q = p_max; q >= 1; --q)
+      for (int ns = staging ? 1 : 2; ns >= 1; --ns) {
+        layout(q, ns);
+        if (pl.smem_bytes <= two_per_sm) return true;
+      }
+    return false;
+  };
+  work_geometry(false);
+  bool found = fit();
+  const int P0 = pl.P, ns0 = pl.nsets;
+  if (found) {
+    work_geometry(true);
+    if (!fit() || pl.P != P0 || pl.nsets != ns0) {
+      work_geometry(false);
+      layout(P0, ns0);
     }
+  }
   // One 256-thread CTA per SM leaves too few warps to hide the phases'
   // latency: such layers run the two separate passes (which keep 2-3 CTAs
   // per SM) instead.
   if (!found)
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels: the fused backward's working set leaves "
                 "one CTA per SM", d->H, d->W, L);
+  for (int l = 0; l <= L; ++l) fp.lev[l] = pl.ds[l];
   fp.P = pl.P;
   fwd_divs(fp);
   pl.batches = d->N > 0 ? ceil_div(d->N, pl.P) : 0;
@@ -816,11 +843,10 @@ void bw_win_geometry(const wtconv_desc_t* d, WtBwPlan& pl, int th, int tw, int t
     b.pcol = (4 - zo % 4) % 4;
     const int rows = std::max(pl.Hs[l], zo + tbr * pl.tr[l] + R);
     const int cols = std::max(b.pcol + pl.Ws[l], zo + 4 * pl.tc[l] + R + b.pcol);
-    b.stride = round_up(cols, 4);
-    if (b.stride % 8 == 0) b.stride += 4;
+    b.stride = pad48(cols);
     b.band = rows * b.stride;
     off += 4 * b.band;
-    off = place(pl.ds[l], off, tbr * pl.tr[l], 4 * pl.tc[l], 0, 0, 4, 4 * pl.tc[l] % 8 == 0 ? 4 * pl.tc[l] + 4 : 0);
+    off = place(pl.ds[l], off, tbr * pl.tr[l], 4 * pl.tc[l], 0, 0, 4, pad48(4 * pl.tc[l]));
   }
   pl.wf = round_up(off, 4);
 }
