@@ -305,11 +305,17 @@ wtconv_status_t plan_fwd_compute(const wtconv_desc_t* d, WtFwdPlan& pl) {
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d with %d levels needs %ld B of shared memory (max %d)",
                 d->H, d->W, L, plane_bytes + 4L * wfloats, kMaxSmemPerBlock);
   // Planes per unit P and final-tile height: the pair with the least modelled
-  // time per plane.  Each phase of a unit costs (rounds of its items over the
-  // CTA's threads) x (the latency of one item, in issue slots measured on the
-  // stage shapes), plus a fixed cost per unit (barriers, copy wait); P is
-  // bounded by the shared-memory budget (3 CTAs per SM).  Half-height final
-  // tiles never need more shared memory.
+  // time for the layer.  Each phase of a unit costs (rounds of its items over
+  // the CTA's threads) x (the latency of one item, in issue slots measured on
+  // the stage shapes), plus a fixed cost per unit (barriers, copy wait).  The
+  // layer takes ceil(units / resident CTAs) such units, where a unit is P
+  // planes of one channel (the last group of a batch partly idle) and the
+  // resident CTAs per SM follow from the kernel's registers and the unit's
+  // shared memory; a unit's time grows with the CTAs sharing its SM as
+  // CTAs^0.3 (fitted to a sweep of forced P on 30 small-plane layers, where
+  // 16-bit kernels fit a fourth CTA below 56 KB).  P is bounded by the
+  // shared-memory budget of 3 CTAs per SM.  Half-height final tiles never
+  // need more shared memory.
   int fit = (int)((kFwdBudget - 4L * wfloats) / plane_bytes);
   if (fit < 1) fit = 1;
   if (d->N > 0 && fit > d->N) fit = d->N;
@@ -320,17 +326,26 @@ wtconv_status_t plan_fwd_compute(const wtconv_desc_t* d, WtFwdPlan& pl) {
     // per unit: 400, plus 200 for every level past the second (its own
     // analysis pass behind a CTA barrier)
     const long c12 = 100, c3 = 30, cz = 16L * KK + 130, cunit = 400 + 200L * (L > 2 ? L - 2 : 0);
+    const int regs = wt::fwd_regs(d->k, d->dtype);
+    const long ctas_r = regs > 0 ? 65536L / (T * (long)round_up(regs, 8)) : 3;
+    const long sms = wt::sm_count() > 0 ? wt::sm_count() : 152;
     double best = -1.0;
     for (int q = 1; q <= fit && q <= 64; ++q) {
+      const long smem = 4L * (2L * round_up(q * pl.xf, 32) + (long)q * pl.wf + wfloats) + 16 + WT_SMEM_SLACK;
+      long ctas = kSmemPerSm / (smem + 1024 + kStaticSmem);
+      if (ctas > ctas_r) ctas = ctas_r;
+      if (ctas < 1) ctas = 1;
+      const long units = (long)d->C * (d->N > 0 ? ceil_div(d->N, q) : 0);
+      const double rounds = (double)((units + ctas * sms - 1) / (ctas * sms)) * pow((double)ctas, 0.3);
       for (int t = WT_TP; t >= WT_TP / 2; t /= 2) {
         const long nf = (long)ceil_div(pl.Hs[1], t) * ceil_div(pl.Ws[1], WT_TQ);
         const long cf = 8L * t * KK + (t == WT_TP ? 400 : 300);  // 2t x 2TQ outputs, k*k FMAs each
         long cost = ceil_div((int)(q * n12), T) * c12 + ceil_div((int)(q * pl.zipp), T) * cz +
                     ceil_div((int)(q * nf), T) * cf + cunit;
         for (int l = 3; l <= L; ++l) cost += ceil_div(q * pl.Hs[l] * pl.Ws[l], T) * c3;
-        const double per_plane = (double)cost / q;
-        if (best < 0 || per_plane < best * (1 - 1e-9)) {
-          best = per_plane;
+        const double total = rounds * cost + 1e-6 * cost / q;  // equal totals (no units): least per plane
+        if (best < 0 || total < best * (1 - 1e-9)) {
+          best = total;
           P = q;
           tp = t;
         }

@@ -32,6 +32,8 @@
 #include "wtconv_fwd_tiles.cuh"
 #include "wtconv_launch.h"
 
+#include <mutex>
+
 namespace wt {
 
 // Bounded waits that gave up (see mbar_wait_bounded); read by take_fwd_faults().
@@ -301,6 +303,35 @@ cudaError_t launch_fwd(const WtFwdPlan& pl, const CUtensorMap& tmx, int dtype, b
                   : launch_fwd_k<__half, false>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
   return rotate ? launch_fwd_k<__nv_bfloat16, true>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream)
                 : launch_fwd_k<__nv_bfloat16, false>(pl, tmx, x, w_base, b_base, w_sub, s_base, s_w, y, stream);
+}
+
+template <typename T>
+static const void* fwd_pick(int k) {
+  switch (k) {
+    case 3: return (const void*)fwd_kernel<3, T, false>;
+    case 5: return (const void*)fwd_kernel<5, T, false>;
+    case 7: return (const void*)fwd_kernel<7, T, false>;
+    case 9: return (const void*)fwd_kernel<9, T, false>;
+    default: return nullptr;
+  }
+}
+
+int fwd_regs(int k, int dtype) {
+  static std::mutex mu;
+  static int cache[4][3];  // k = 3, 5, 7, 9; dtype; 0 = not yet read
+  const int ki = (k - 3) / 2;
+  if (ki < 0 || ki > 3 || dtype < 0 || dtype > 2) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[ki][dtype] == 0) {
+    const void* f = dtype == 0 ? fwd_pick<float>(k) : dtype == 1 ? fwd_pick<__half>(k) : fwd_pick<__nv_bfloat16>(k);
+    cudaFuncAttributes a;
+    if (!f || cudaFuncGetAttributes(&a, f) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[ki][dtype] = a.numRegs;
+  }
+  return cache[ki][dtype];
 }
 
 unsigned int take_fwd_faults() {

@@ -66,6 +66,8 @@ int bw_win_ctas_per_sm(const WtBwPlan& pl, int dtype);
 // Registers per thread of the windowed gradient kernel for (k, tile rows,
 // dtype), read once from the runtime (0 when it cannot tell).
 int bw_win_regs(int k, int tbr, int dtype);
+// The same for the whole-plane forward kernel (k, dtype).
+int fwd_regs(int k, int dtype);
 
 // Coarse-level split (layers whose tile window does not fit one CTA):
 //   launch_lowpass: ll = block sums of x over 2^s x 2^s blocks (float32,

@@ -45,6 +45,7 @@ cudaError_t launch_bwd_weight_win(const WtBwPlan&, const CUtensorMap&, const CUt
 int bw_win_ctas_per_sm(const WtBwPlan& pl, int) { int n = (int)(233472 / (pl.smem_bytes + 1024)); return n > 2 ? 2 : n; }
 unsigned int take_bww_faults() { return 0; }
 int bw_win_regs(int, int, int) { return 0; }
+int fwd_regs(int, int dtype) { return dtype == 0 ? 144 : 128; }  // the k = 5 kernels' registers
 cudaError_t launch_bwd_fused(const WtBwPlan&, const WtFwdPlan&, const CUtensorMap&, const CUtensorMap&, int, const void*, const void*, const float*, const float*,
                              const float*, const float*, const float*, void*, float*, float*, float*, float*, float*, float*, cudaStream_t) { return cudaSuccess; }
 int bwf_ctas_per_sm(const WtBwPlan& pl, const WtFwdPlan&, int) { int n = (int)(233472 / (pl.smem_bytes + 1024)); return n > 2 ? 2 : n; }
