@@ -45,9 +45,11 @@ static __device__ unsigned int g_fwd_faults;
 // input-plane buffers (the next unit's planes are prefetched with cp.async
 // while the current unit is computed, for float32), one work area per plane
 // (pyramid + convolved bands) and the weights.  It is zeroed once; later
-// writes touch interiors only, so every margin stays zero.
+// writes touch interiors only, so every margin stays zero.  Registers: at
+// most 128 per thread for k <= 5 (no spills), so four CTAs fit an SM when a
+// unit's shared memory allows it (small planes); 170 for k = 7, 9 (three).
 template <int K, typename T, bool ROT>
-__global__ void __launch_bounds__(WT_FWD_THREADS, 3)
+__global__ void __launch_bounds__(WT_FWD_THREADS, K <= 5 ? 4 : 3)
     fwd_kernel(const __grid_constant__ WtFwdPlan pl, const __grid_constant__ CUtensorMap tmx,
                const T* __restrict__ x,
                const float* __restrict__ w_base, const float* __restrict__ b_base,
