@@ -629,7 +629,22 @@ wtconv_status_t plan_bw_compute(const wtconv_desc_t* d, WtBwPlan& pl) {
   pl.items_per_plane = pl.item_begin[L + 1];
   pl.nbands = 1 + 4 * L;
   pl.part_stride = pl.nbands * (KK + 1);
-  const int slots = (pl.tbr == 8 ? 1 : WT_BW_MAX_ITEMS) * WT_BW_THREADS;
+  // Tiles per thread.  4-row tiles take one per thread when whole planes
+  // fill at least 85 % of the threads and the smaller kernel fits more CTAs
+  // per SM (its registers, read from the runtime; at k = 5 80 against 128,
+  // three CTAs against two), else two.  On GB300 one per thread was 6-16 %
+  // faster on 7 x 7 and 14 x 14 planes, where a CTA fills 94-98 % of its
+  // threads, and 20 % slower on 28 x 28 planes at 4-5 levels (54 %).
+  pl.mi = 1;
+  if (pl.tbr == 4) {
+    const int r1 = wt::bw_regs(d->k, 1, d->dtype), r2 = wt::bw_regs(d->k, WT_BW_MAX_ITEMS, d->dtype);
+    const long c1 = r1 > 0 ? 65536L / (WT_BW_THREADS * (long)round_up(r1, 8)) : 3;
+    const long c2 = r2 > 0 ? 65536L / (WT_BW_THREADS * (long)round_up(r2, 8)) : 2;
+    const bool fills = pl.items_per_plane <= WT_BW_THREADS &&
+                       (WT_BW_THREADS / pl.items_per_plane) * pl.items_per_plane * 100 >= 85 * WT_BW_THREADS;
+    if (!fills || c1 <= c2) pl.mi = WT_BW_MAX_ITEMS;
+  }
+  const int slots = pl.mi * WT_BW_THREADS;
   if (pl.items_per_plane > slots)
     return fail(WTCONV_ERR_UNSUPPORTED, "plane %dx%d has %d gradient tiles (max %d per CTA)", d->H, d->W,
                 pl.items_per_plane, slots);

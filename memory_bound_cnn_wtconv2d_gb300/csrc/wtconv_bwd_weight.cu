@@ -26,6 +26,8 @@
 #include "wtconv_device.cuh"
 #include "wtconv_launch.h"
 
+#include <mutex>
+
 namespace wt {
 
 // Bounded waits that gave up (see mbar_wait_bounded); read by take_bw_faults().
@@ -34,7 +36,7 @@ static __device__ unsigned int g_bw_faults;
 // TR = 8: 8x4 tiles, one per thread; TR = 4: 4x4 tiles, up to two per thread.
 // Tiles are 4 columns wide so neighbouring lanes read neighbouring 16-byte
 // chunks of a row (no shared-memory bank conflicts within a row).
-template <int K, typename T, int TR>
+template <int K, typename T, int TR, int MI>
 __global__ void __launch_bounds__(WT_BW_THREADS)
     bw_kernel(const __grid_constant__ WtBwPlan pl, const __grid_constant__ CUtensorMap tmx,
               const __grid_constant__ CUtensorMap tmd, const T* __restrict__ x, const T* __restrict__ dy,
@@ -43,7 +45,7 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
   float* const sm = align_smem128(sm_raw);  // TMA box destinations need 128-byte alignment
   constexpr int KK = K * K;
   constexpr int NT = WT_BW_THREADS;
-  constexpr int MI = TR == 8 ? 1 : WT_BW_MAX_ITEMS;
+  static_assert(MI == 1 || (TR == 4 && MI == WT_BW_MAX_ITEMS), "two items per thread with 4-row tiles only");
   constexpr int TC = 4;
   constexpr bool ASYNC = sizeof(T) == 4;
   constexpr int R = K / 2;
@@ -385,7 +387,9 @@ __global__ void bw_finalize_kernel(const __grid_constant__ WtBwPlan pl, const fl
 template <int K, typename T>
 static cudaError_t launch_bw_t(const WtBwPlan& pl, const CUtensorMap& tmx, const CUtensorMap& tmd, const void* x,
                                const void* dy, float* part, cudaStream_t stream) {
-  auto kern = pl.tbr == 8 ? bw_kernel<K, T, 8> : bw_kernel<K, T, 4>;
+  auto kern = pl.tbr == 8   ? bw_kernel<K, T, 8, 1>
+              : pl.mi == 1 ? bw_kernel<K, T, 4, 1>
+                           : bw_kernel<K, T, 4, WT_BW_MAX_ITEMS>;
   cudaError_t e = ensure_smem((const void*)kern, pl.smem_bytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)pl.grid;
@@ -431,24 +435,56 @@ cudaError_t launch_bw_finalize(const WtBwPlan& pl, const float* part, const floa
   return cudaGetLastError();
 }
 
-// Resident parameter-gradient CTAs per SM for this plan (0 if the runtime
-// cannot tell, e.g. without a device).
-int bw_ctas_per_sm(const WtBwPlan& pl, int dtype) {
+// The kernel instance a plan launches (nullptr for an unsupported k).
+static const void* bw_pick(const WtBwPlan& pl, int dtype) {
   const void* f = nullptr;
-#define WT_BW_PICK(KK, TT) f = pl.tbr == 8 ? (const void*)bw_kernel<KK, TT, 8> : (const void*)bw_kernel<KK, TT, 4>
-#define WT_BW_PICK_K(TT)          \
-  switch (pl.K) {                 \
+#define WT_BW_PICK(KK, TT)                                         \
+  f = pl.tbr == 8   ? (const void*)bw_kernel<KK, TT, 8, 1>         \
+      : pl.mi == 1 ? (const void*)bw_kernel<KK, TT, 4, 1>          \
+                   : (const void*)bw_kernel<KK, TT, 4, WT_BW_MAX_ITEMS>
+#define WT_BW_PICK_K(TT)              \
+  switch (pl.K) {                     \
     case 3: WT_BW_PICK(3, TT); break; \
     case 5: WT_BW_PICK(5, TT); break; \
     case 7: WT_BW_PICK(7, TT); break; \
     case 9: WT_BW_PICK(9, TT); break; \
-    default: return 0;            \
+    default: return nullptr;          \
   }
   if (dtype == 0) { WT_BW_PICK_K(float) }
   else if (dtype == 1) { WT_BW_PICK_K(__half) }
   else { WT_BW_PICK_K(__nv_bfloat16) }
 #undef WT_BW_PICK_K
 #undef WT_BW_PICK
+  return f;
+}
+
+int bw_regs(int k, int mi, int dtype) {
+  static std::mutex mu;
+  static int cache[4][2][3];  // k = 3, 5, 7, 9; tiles per thread 1, 2; dtype; 0 = not yet read
+  const int ki = (k - 3) / 2, mj = mi == 1 ? 0 : 1;
+  if (ki < 0 || ki > 3 || dtype < 0 || dtype > 2) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[ki][mj][dtype] == 0) {
+    WtBwPlan q;
+    q.K = k;
+    q.tbr = 4;
+    q.mi = mi;
+    const void* f = bw_pick(q, dtype);
+    cudaFuncAttributes a;
+    if (!f || cudaFuncGetAttributes(&a, f) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[ki][mj][dtype] = a.numRegs;
+  }
+  return cache[ki][mj][dtype];
+}
+
+// Resident parameter-gradient CTAs per SM for this plan (0 if the runtime
+// cannot tell, e.g. without a device).
+int bw_ctas_per_sm(const WtBwPlan& pl, int dtype) {
+  const void* f = bw_pick(pl, dtype);
+  if (!f) return 0;
   return occupancy(f, WT_BW_THREADS, pl.smem_bytes);
 }
 

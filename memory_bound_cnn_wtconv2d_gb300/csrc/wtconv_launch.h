@@ -62,6 +62,9 @@ int bwf_ctas_per_sm(const WtBwPlan& pl, const WtFwdPlan& fp, int dtype);
 // Resident parameter-gradient CTAs per SM for a plan, from the runtime's
 // occupancy calculator (0 when it cannot tell).
 int bw_ctas_per_sm(const WtBwPlan& pl, int dtype);
+// Registers per thread of the whole-plane gradient kernel with 4-row tiles,
+// mi (1 or 2) tiles per thread, read once from the runtime (0 when it cannot tell).
+int bw_regs(int k, int mi, int dtype);
 int bw_win_ctas_per_sm(const WtBwPlan& pl, int dtype);
 // Registers per thread of the windowed gradient kernel for (k, tile rows,
 // dtype), read once from the runtime (0 when it cannot tell).

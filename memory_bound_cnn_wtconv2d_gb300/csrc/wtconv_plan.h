@@ -115,6 +115,7 @@ struct WtBwPlan {
   int Hs[WT_MAXL + 1];
   int Ws[WT_MAXL + 1];
   int tbr;               // tile rows: 8 (one tile per thread) or 4 (up to two per thread)
+  int mi;                // tiles per thread: 1, or 2 (4-row tiles of the whole-plane gradient pass)
   int tcw;               // tile columns: 4
   int tr[WT_MAXL + 1];   // tbr x tcw tiles per level (level 0 = base path): rows, columns
   int tc[WT_MAXL + 1];

@@ -50,6 +50,7 @@ cudaError_t launch_bwd_fused(const WtBwPlan&, const WtFwdPlan&, const CUtensorMa
                              const float*, const float*, const float*, void*, float*, float*, float*, float*, float*, float*, cudaStream_t) { return cudaSuccess; }
 int bwf_ctas_per_sm(const WtBwPlan& pl, const WtFwdPlan&, int) { int n = (int)(233472 / (pl.smem_bytes + 1024)); return n > 2 ? 2 : n; }
 unsigned int take_bwf_faults() { return 0; }
+int bw_regs(int k, int mi, int) { return mi == 1 ? (k <= 5 ? 80 : 128) : (k <= 5 ? 128 : 232); }  // as the f32 kernels
 int bw_ctas_per_sm(const WtBwPlan& pl, int) { return (int)(233472 / (pl.smem_bytes + 1024)) > 3 ? 3 : (int)(233472 / (pl.smem_bytes + 1024)); }
 unsigned int take_bw_faults() { return 0; }
 cudaError_t launch_lowpass(int, const void*, float*, long long, int, int, int, cudaStream_t) { return cudaSuccess; }
@@ -219,7 +220,8 @@ static void check_bw(int N, int C, int H, int W, int L, int K) {
   CHECK(pl.P * WF <= pl.red_floats && pl.red_floats % 4 == 0 && pl.work_off + pl.red_floats == pl.mb_off, "work region");
   CHECK(pl.P * pl.items_per_plane * (KK + 1) <= pl.red_floats, "reduction beyond work region");
   CHECK(pl.mb_off % 2 == 0 && 4 * pl.mb_off + 16 <= pl.smem_bytes && pl.smem_bytes <= 232448, "mbarriers/smem");
-  CHECK(pl.P * pl.items_per_plane <= (pl.tbr == 8 ? 1 : WT_BW_MAX_ITEMS) * WT_BW_THREADS, "items beyond slots");
+  CHECK(pl.mi == 1 || (pl.tbr == 4 && pl.mi == WT_BW_MAX_ITEMS), "tiles per thread");
+  CHECK(pl.P * pl.items_per_plane <= pl.mi * WT_BW_THREADS, "items beyond slots");
   CHECK(XB % 4 == 0 && DB % 4 == 0 && WF % 4 == 0 && pl.xs[0].off == 0 && pl.ds[0].off == 0, "align");
   CHECK(pl.xs[0].pcol == 4 && pl.xs[0].prow == R && pl.ds[0].pcol == 0 && pl.ds[0].prow == 0, "level-0 margins");
   CHECK(XB == pl.xs[0].band && DB == pl.ds[0].band, "box = plane buffer");
