@@ -768,8 +768,10 @@ wtconv_status_t plan_bwf_compute(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan
   fp.w_band = round_up(KK, 4);
   const int wfloats = (1 + 4 * L) * fp.w_band;
   // 16-bit planes that are whole 8-byte chunks get a staging area for their
-  // raw planes, and one input set (used when the tensors are aligned enough).
-  const bool staging = d->dtype != WTCONV_F32 && (2L * d->H * d->W) % 8 == 0;
+  // raw planes, and one input set (used when the tensors are aligned enough);
+  // where the staging area would cost the second CTA per SM, the planes are
+  // loaded element-wise instead, without one.
+  bool staging = d->dtype != WTCONV_F32 && (2L * d->H * d->W) % 8 == 0;
   auto layout = [&](int P, int nsets) {
     pl.P = P;
     pl.nsets = nsets;
@@ -799,6 +801,10 @@ wtconv_status_t plan_bwf_compute(const wtconv_desc_t* d, WtBwPlan& pl, WtFwdPlan
   };
   work_geometry(false);
   bool found = fit();
+  if (!found && staging) {
+    staging = false;
+    found = fit();
+  }
   const int P0 = pl.P, ns0 = pl.nsets;
   if (found) {
     work_geometry(true);

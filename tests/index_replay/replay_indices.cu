@@ -648,7 +648,9 @@ static void check_bwf(int N, int C, int H, int W, int L, int K, int dtype) {
   const int XB = pl.xbf, DB = pl.dbf, WF = pl.wf;
   CHECK(TR == 8 && TP == 2, "tiles");
   CHECK(pl.xr % 32 == 0 && pl.xr >= P * XB && pl.islot % 32 == 0 && pl.islot - pl.xr >= P * DB, "input set");
-  const bool staging = dtype != 0 && (2L * H * W) % 8 == 0;
+  // 16-bit planes of whole 8-byte chunks are staged raw, unless the staging
+  // area would cost the second CTA per SM (then they are loaded element-wise)
+  const bool staging = dtype != 0 && (2L * H * W) % 8 == 0 && pl.work_off > pl.stage_off;
   CHECK(pl.stage_off == pl.nsets * pl.islot && pl.stage_off % 32 == 0, "stage off");
   CHECK(pl.work_off == pl.stage_off + (staging ? (P * H * W + 31) / 32 * 32 : 0) && pl.work_off % 4 == 0, "work off");
   if (staging) {
@@ -664,6 +666,9 @@ static void check_bwf(int N, int C, int H, int W, int L, int K, int dtype) {
     if (pl.wd_vec == 4) CHECK(W % 4 == 0 && pl.xs[0].pcol % 4 == 0 && pl.ds[0].pcol % 4 == 0, "widen alignment");
     if (pl.wd_vec == 2) CHECK(W % 2 == 0 && pl.xs[0].pcol % 2 == 0 && pl.ds[0].pcol % 2 == 0 && XB % 2 == 0 && DB % 2 == 0, "widen pair alignment");
     pl.use_bulk = 0;
+  } else if (dtype != 0) {
+    set_bulk(pl, &d, (const void*)(uintptr_t)4096, 0);
+    CHECK(pl.use_bulk == 0, "element-wise loads without a staging area");
   }
   CHECK(pl.red_floats >= P * WF && pl.red_floats >= P * pl.items_per_plane * (KK + 1) && pl.red_floats % 4 == 0, "red");
   CHECK(fp.w_off == pl.work_off + pl.red_floats && fp.w_off % 4 == 0 && fp.w_band % 4 == 0, "weights off");

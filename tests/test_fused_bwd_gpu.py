@@ -28,7 +28,7 @@ FUSED = [(2, 4, 56, 56, 3, 5), (3, 4, 28, 28, 2, 5), (2, 2, 40, 40, 1, 5), (2, 2
          # ragged last plane group (3 + 1, 3 + 3 + 1, 2 + 2 + 1 planes per unit) and the largest plane
          (4, 4, 28, 28, 2, 5), (7, 2, 32, 32, 1, 7), (5, 3, 40, 40, 1, 5), (2, 2, 64, 64, 1, 5)]
 FALLBACK = [(2, 3, 13, 17, 3, 5, "f32"), (9, 6, 7, 7, 2, 5, "f32"), (2, 3, 28, 28, 4, 5, "f16"),
-            (2, 2, 130, 124, 2, 5, "f32"), (2, 4, 56, 56, 3, 5, "bf16")]
+            (2, 2, 130, 124, 2, 5, "f32"), (2, 4, 56, 56, 5, 5, "bf16")]
 
 
 def run_fused(wt, inp, d):
