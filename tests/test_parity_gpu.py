@@ -111,6 +111,21 @@ def test_kernel_sizes(wt, k):
     check_all(wt, synth.make_inputs(2, 3, 19, 23, 3, k, seed=k))
 
 
+# Layers whose parameter-gradient plans take each tile variant of the
+# whole-plane kernel: one 4-row tile per thread (planes that fill the CTA:
+# 7 x 7, 14 x 14; at k = 9 two per thread, the one-tile kernel fitting no
+# more CTAs), two 4-row tiles per thread (28 x 28 at 4 levels) and 8-row
+# tiles (28 x 28 at 2 levels), each with several units per CTA slot.
+TILE_VARIANTS = [(24, 2, 7, 7, 2), (8, 3, 14, 14, 3), (3, 2, 28, 28, 4), (4, 2, 28, 28, 2)]
+
+
+@pytest.mark.parametrize("shape", TILE_VARIANTS, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("k", [3, 5, 7, 9])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_gradient_tile_variants(wt, shape, k, dtype):
+    check_all(wt, synth.make_inputs(*shape, k, dtype=dtype, seed=shape_seed(shape) + k))
+
+
 def test_no_bias(wt):
     check_all(wt, synth.make_inputs(2, 3, 21, 18, 3, 5, seed=4, bias=False))
 
