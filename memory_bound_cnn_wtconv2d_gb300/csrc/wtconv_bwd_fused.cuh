@@ -35,9 +35,12 @@ static __device__ unsigned int g_bwf_faults;
 
 // TR: correlation tile rows (8: one tile per thread; the code also handles
 // 4-row tiles, up to two per thread).  TP: final-tile height (level-1 rows)
-// of the input-gradient tiles.
+// of the input-gradient tiles.  16-bit instances at k <= 5 are held to the
+// registers of two CTAs per SM; the float32 ones are left to the compiler
+// (0: no minimum), which fits those by itself (at k = 7, 9 the planner hands
+// the layer to the two separate passes).
 template <int K, typename T, int TR, int TP>
-__global__ void __launch_bounds__(WT_BW_THREADS)
+__global__ void __launch_bounds__(WT_BW_THREADS, sizeof(T) == 2 && K <= 5 ? 2 : 0)
     bwf_kernel(const __grid_constant__ WtBwPlan pl, const __grid_constant__ WtFwdPlan fp,
                const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmd,
                const T* __restrict__ x, const T* __restrict__ dy, const float* __restrict__ w_base,
@@ -202,7 +205,11 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
         __syncthreads();
         return;  // records are not written: the caller sees the fault count
       }
-      if (staged) {  // widen the raw planes, then start the next unit's copies
+      // 16-bit raw planes: widened by the fused level-1/2 pass itself where
+      // rows are whole 4-element groups, else first, by a pass of their own.
+      // The next unit's copies follow once they are consumed.
+      const bool widen12 = staged && L >= 2 && (pl.W & 3) == 0;
+      if (staged && !widen12) {
         widen_planes<T>(in_x, XBF, pl.xs[0], stage_x, np, pl.H, pl.W, pl.wd_vec, pl.wd_pp, pl.wd_w, tid, NT);
         widen_planes<T>(in_d, DBF, pl.ds[0], stage_d, np, pl.H, pl.W, pl.wd_vec, pl.wd_pp, pl.wd_w, tid, NT);
         __syncthreads();
@@ -214,11 +221,20 @@ __global__ void __launch_bounds__(WT_BW_THREADS)
       if (L == 1) {
         haar_level(in_x, XBF, work, WF, np, pl.xs[0], pl.xs[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
         haar_level(in_d, DBF, work, WF, np, pl.ds[0], pl.ds[1], pl.Hs[1], pl.Ws[1], pl.an_pp[1], pl.an_w[1], tid, NT);
+      } else if (widen12) {
+        if constexpr (!ASYNC)  // (16-bit instances only)
+          widen_levels12_pair<T>(stage_x, in_x, XBF, pl.xs[0], pl.xs[1], pl.xs[2], stage_d, in_d, DBF, pl.ds[0],
+                                 pl.ds[1], pl.ds[2], pl.H, pl.W, work, WF, np, pl.Hs[1], pl.Ws[1], pl.Hs[2],
+                                 pl.Ws[2], pl.an_pp[2], pl.an_w[2], tid, NT);
       } else {
         haar_levels12_pair(in_x, XBF, pl.xs[0], pl.xs[1], pl.xs[2], in_d, DBF, pl.ds[0], pl.ds[1], pl.ds[2], work,
                            WF, np, pl.Hs[1], pl.Ws[1], pl.Hs[2], pl.Ws[2], pl.an_pp[2], pl.an_w[2], tid, NT);
       }
       __syncthreads();
+      if (widen12) {  // the raw planes are consumed: start the next unit's copies
+        if (bulk && tid == 0 && u + 1 < u_end) issue_bulk(u + 1);
+        if (cpa && u + 1 < u_end) issue_cpa(u + 1);
+      }
       for (int l = 3; l <= L; ++l) {
         haar_level_pair(work, WF, work, WF, np, pl.xs[l - 1], pl.xs[l], pl.ds[l - 1], pl.ds[l], pl.Hs[l], pl.Ws[l],
                         pl.an_pp[l], pl.an_w[l], tid, NT);

@@ -384,6 +384,88 @@ __device__ __forceinline__ void haar_levels12(const float* sbase, int sps, float
   }
 }
 
+// Levels 1 and 2 straight from np raw 16-bit planes (H*W elements each,
+// consecutive in `src`, as the bulk copies leave them): each 4 x 4 block of
+// the level-2 grid is read (zero past the plane), widened, written into the
+// float32 interior of buffer S of its plane slot (which the base convolution
+// reads later), and its butterflies stored as haar_levels12 stores them.
+// The grid's blocks cover each plane (4 ceil(ceil(W/2)/2) = 4 ceil(W/4) >= W,
+// so a block's first column is inside it), every interior element is
+// written once and the margins stay zero.
+template <typename T>
+__device__ __forceinline__ void widen_block4(const T* plane, int H, int W, int P, int Q, float* sp, const WtBuf S,
+                                             bool vec, float (&x)[4][4]) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int i = 4 * P + a;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[a][e] = 0.f;
+    if (i < H) {
+      const T* row = plane + i * W + 4 * Q;
+      float* dst = sp + S.off + (i + S.prow) * S.stride + 4 * Q + S.pcol;
+      if (vec) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(row);
+        const T* h = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[a][e] = to_f32(h[e]);
+        *reinterpret_cast<float4*>(dst) = make_float4(x[a][0], x[a][1], x[a][2], x[a][3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (4 * Q + e < W) {
+            x[a][e] = to_f32(row[e]);
+            dst[e] = x[a][e];
+          }
+      }
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void widen_levels12(const T* src, int H, int W, float* sbase, int sps, const WtBuf S,
+                                               float* dbase, int dps, int np, const WtBuf D1, const WtBuf D2,
+                                               int H1, int W1, int H2, int W2, const WtDiv& dpp, const WtDiv& dw,
+                                               int tid, int nthreads) {
+  const int HW = H * W;
+  const bool vec = (W & 3) == 0 && (S.pcol & 3) == 0;  // 8-byte loads, 16-byte stores (the kernels' case)
+  const int per_plane = H2 * W2;
+  for (int it = tid; it < np * per_plane; it += nthreads) {
+    const int g = fdiv(it, dpp);
+    const int rem = it - g * per_plane;
+    const int P = fdiv(rem, dw);
+    const int Q = rem - P * W2;
+    float x[4][4];
+    widen_block4<T>(src + g * HW, H, W, P, Q, sbase + g * sps, S, vec, x);
+    store_block12(x, dbase + g * dps, D1, D2, P, Q, H1, W1);
+  }
+}
+
+// widen_levels12 for x and dy at once (the parameter-gradient passes): each
+// item widens and stores the block of both raw planes before its butterflies.
+template <typename T>
+__device__ __forceinline__ void widen_levels12_pair(const T* srca, float* sa, int spa, const WtBuf SA,
+                                                    const WtBuf DA1, const WtBuf DA2, const T* srcb, float* sb,
+                                                    int spb, const WtBuf SB, const WtBuf DB1, const WtBuf DB2,
+                                                    int H, int W, float* dbase, int dps, int np, int H1, int W1,
+                                                    int H2, int W2, const WtDiv& dpp, const WtDiv& dw, int tid,
+                                                    int nthreads) {
+  const int HW = H * W;
+  const bool vec = (W & 3) == 0 && (SA.pcol & 3) == 0 && (SB.pcol & 3) == 0;
+  const int per_plane = H2 * W2;
+  for (int it = tid; it < np * per_plane; it += nthreads) {
+    const int g = fdiv(it, dpp);
+    const int rem = it - g * per_plane;
+    const int P = fdiv(rem, dw);
+    const int Q = rem - P * W2;
+    float xa[4][4], xb[4][4];
+    widen_block4<T>(srca + g * HW, H, W, P, Q, sa + g * spa, SA, vec, xa);
+    widen_block4<T>(srcb + g * HW, H, W, P, Q, sb + g * spb, SB, vec, xb);
+    float* ps = dbase + g * dps;
+    store_block12(xa, ps, DA1, DA2, P, Q, H1, W1);
+    store_block12(xb, ps, DB1, DB2, P, Q, H1, W1);
+  }
+}
+
 // Widen np raw 16-bit planes (H*W elements each, consecutive in `src`, as the
 // bulk copies leave them) into the float32 interiors of buffer B of each
 // plane slot.  `per` elements per item: 4 when W % 4 == 0 (8-byte loads,

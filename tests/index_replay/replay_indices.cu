@@ -73,6 +73,34 @@ static void acc_buf(const WtBuf& b, int nb, int bi, int pr, int pc, int plane_fl
 }
 
 
+// The fused level-1/2 pass over 16-bit raw planes (rows of whole 4-element
+// groups): each block of the level-2 grid reads its rows of the raw plane
+// (its first column inside the plane; 8-byte aligned) and writes the float32
+// interior of buffer X (16-byte aligned); together the blocks write every
+// interior element exactly once.
+static void check_widen12(int H, int W, int H2, int W2, const WtBuf X, int lim) {
+  std::vector<int> cnt(lim, 0);
+  for (int P = 0; P < H2; ++P) for (int Q = 0; Q < W2; ++Q) {
+    CHECK(4 * Q < W, "block's first column inside the plane");
+    for (int a = 0; a < 4; ++a) {
+      const int i = 4 * P + a;
+      if (i >= H) continue;
+      CHECK((i * W + 4 * Q) % 4 == 0 && (H * W) % 4 == 0 && (X.off + (i + X.prow) * X.stride + 4 * Q + X.pcol) % 4 == 0,
+            "widen12 vector alignment");
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * Q + e;
+        CHECK(j < W, "widen12 vector beyond the row");
+        CHECK(i * W + j < H * W, "widen12 staging read");
+        acc_buf(X, 1, 0, i + X.prow, j + X.pcol, lim, "widen12 write");
+        const long k = X.off + (long)(i + X.prow) * X.stride + j + X.pcol;
+        if (k >= 0 && k < lim) cnt[k]++;
+      }
+    }
+  }
+  for (int i = 0; i < H; ++i) for (int j = 0; j < W; ++j)
+    CHECK(cnt[X.off + (i + X.prow) * X.stride + j + X.pcol] == 1, "widen12 writes each interior element once");
+}
+
 static void check_fwd(int N, int C, int H, int W, int L, int K) {
   wtconv_desc_t d{N, C, H, W, L, K, (wtconv_dtype_t)g_dtype};
   WtFwdPlan pl;
@@ -101,6 +129,7 @@ static void check_fwd(int N, int C, int H, int W, int L, int K) {
       if (pl.wd_vec == 2) CHECK(W % 2 == 0 && pl.lev[0].pcol % 2 == 0 && pl.lev[0].stride % 2 == 0 && XF % 2 == 0, "widen pair alignment");
       CHECK(pl.wd_vec == (W % 4 == 0 ? 4 : W % 2 == 0 ? 2 : 1), "widen item width");
       for (int g = 0; g < pl.P; ++g) CHECK(((long)g * H * W * 2) % (pl.use_bulk == 1 ? 16 : 8) == 0, "staging plane alignment");
+      if (L >= 2 && W % 4 == 0) check_widen12(H, W, pl.Hs[2], pl.Ws[2], pl.lev[0], XF);
     }
   }
   std::vector<char> written(PF, 0), xwritten(XF, 0);  // interior writes, to check margins stay zero
@@ -216,6 +245,10 @@ static void check_bw(int N, int C, int H, int W, int L, int K) {
     if (pl.wd_vec == 4) CHECK(pl.ds[0].pcol % 4 == 0 && pl.xs[0].pcol % 4 == 0 && W % 4 == 0, "bw widen alignment");
     if (pl.wd_vec == 2) CHECK(pl.ds[0].pcol % 2 == 0 && pl.xs[0].pcol % 2 == 0 && pl.xs[0].stride % 2 == 0 && pl.ds[0].stride % 2 == 0 && W % 2 == 0 && XB % 2 == 0 && DB % 2 == 0, "bw widen pair alignment");
     CHECK(pl.nsets == 1, "16-bit uses one input set");
+    if (L >= 2 && W % 4 == 0) {
+      check_widen12(H, W, pl.Hs[2], pl.Ws[2], pl.xs[0], XB);
+      check_widen12(H, W, pl.Hs[2], pl.Ws[2], pl.ds[0], DB);
+    }
   }
   CHECK(pl.P * WF <= pl.red_floats && pl.red_floats % 4 == 0 && pl.work_off + pl.red_floats == pl.mb_off, "work region");
   CHECK(pl.P * pl.items_per_plane * (KK + 1) <= pl.red_floats, "reduction beyond work region");
@@ -665,6 +698,10 @@ static void check_bwf(int N, int C, int H, int W, int L, int K, int dtype) {
     }
     if (pl.wd_vec == 4) CHECK(W % 4 == 0 && pl.xs[0].pcol % 4 == 0 && pl.ds[0].pcol % 4 == 0, "widen alignment");
     if (pl.wd_vec == 2) CHECK(W % 2 == 0 && pl.xs[0].pcol % 2 == 0 && pl.ds[0].pcol % 2 == 0 && XB % 2 == 0 && DB % 2 == 0, "widen pair alignment");
+    if (L >= 2 && W % 4 == 0) {
+      check_widen12(H, W, pl.Hs[2], pl.Ws[2], pl.xs[0], XB);
+      check_widen12(H, W, pl.Hs[2], pl.Ws[2], pl.ds[0], DB);
+    }
     pl.use_bulk = 0;
   } else if (dtype != 0) {
     set_bulk(pl, &d, (const void*)(uintptr_t)4096, 0);
