@@ -421,14 +421,53 @@ __device__ __forceinline__ void widen_block4(const T* plane, int H, int W, int P
   }
 }
 
+// widen_block4 for rows of even length that are not whole 4-element groups:
+// pairs (4-byte loads, 8-byte stores; a pair past the row is skipped).
+template <typename T>
+__device__ __forceinline__ void widen_block4_pairs(const T* plane, int H, int W, int P, int Q, float* sp,
+                                                   const WtBuf S, float (&x)[4][4]) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int i = 4 * P + a;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[a][e] = 0.f;
+    if (i < H) {
+      const T* row = plane + i * W + 4 * Q;
+      float* dst = sp + S.off + (i + S.prow) * S.stride + 4 * Q + S.pcol;
+#pragma unroll
+      for (int e = 0; e < 4; e += 2)
+        if (4 * Q + e < W) {
+          const uint32_t raw = *reinterpret_cast<const uint32_t*>(row + e);
+          const T* h = reinterpret_cast<const T*>(&raw);
+          x[a][e] = to_f32(h[0]);
+          x[a][e + 1] = to_f32(h[1]);
+          *reinterpret_cast<float2*>(dst + e) = make_float2(x[a][e], x[a][e + 1]);
+        }
+    }
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void widen_levels12(const T* src, int H, int W, float* sbase, int sps, const WtBuf S,
                                                float* dbase, int dps, int np, const WtBuf D1, const WtBuf D2,
                                                int H1, int W1, int H2, int W2, const WtDiv& dpp, const WtDiv& dw,
                                                int tid, int nthreads) {
   const int HW = H * W;
-  const bool vec = (W & 3) == 0 && (S.pcol & 3) == 0;  // 8-byte loads, 16-byte stores (the kernels' case)
+  const bool vec = (W & 3) == 0 && (S.pcol & 3) == 0;  // 8-byte loads, 16-byte stores
+  const bool pairs = !vec && (W & 1) == 0 && ((S.pcol | S.stride) & 1) == 0;
   const int per_plane = H2 * W2;
+  if (pairs) {
+    for (int it = tid; it < np * per_plane; it += nthreads) {
+      const int g = fdiv(it, dpp);
+      const int rem = it - g * per_plane;
+      const int P = fdiv(rem, dw);
+      const int Q = rem - P * W2;
+      float x[4][4];
+      widen_block4_pairs<T>(src + g * HW, H, W, P, Q, sbase + g * sps, S, x);
+      store_block12(x, dbase + g * dps, D1, D2, P, Q, H1, W1);
+    }
+    return;
+  }
   for (int it = tid; it < np * per_plane; it += nthreads) {
     const int g = fdiv(it, dpp);
     const int rem = it - g * per_plane;

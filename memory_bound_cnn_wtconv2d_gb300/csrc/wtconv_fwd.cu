@@ -192,10 +192,10 @@ __global__ void __launch_bounds__(WT_FWD_THREADS, K <= 5 ? 4 : 3)
       break;
     }
     // 16-bit raw planes: widened by the fused level-1/2 pass itself where rows
-    // are whole 4-element groups (8-byte loads, 16-byte stores; 2-3 % faster
-    // at 28 x 28 and 56 x 56), else first, by a pass of their own.  The next
+    // have even length (4-element groups or pairs; 1-3 % faster at 14 x 14,
+    // 28 x 28 and 56 x 56), else first, by a pass of their own.  The next
     // unit's copy follows once they are consumed.
-    const bool widen12 = staged && L >= 2 && (pl.W & 3) == 0;
+    const bool widen12 = staged && L >= 2 && (pl.W & 1) == 0;
     if (staged && !widen12) {
       widen_planes<T>(xs, XF, pl.lev[0], stage, np, pl.H, pl.W, pl.wd_vec, pl.wd_pp, pl.wd_w, tid, NT);
       __syncthreads();

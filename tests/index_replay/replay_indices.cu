@@ -73,27 +73,33 @@ static void acc_buf(const WtBuf& b, int nb, int bi, int pr, int pc, int plane_fl
 }
 
 
-// The fused level-1/2 pass over 16-bit raw planes (rows of whole 4-element
-// groups): each block of the level-2 grid reads its rows of the raw plane
-// (its first column inside the plane; 8-byte aligned) and writes the float32
-// interior of buffer X (16-byte aligned); together the blocks write every
-// interior element exactly once.
+// The fused level-1/2 pass over 16-bit raw planes (rows of even length):
+// each block of the level-2 grid reads its rows of the raw plane (its first
+// column inside the plane) in 4-element groups (8-byte loads, 16-byte
+// stores) when rows are whole groups, else in pairs (4-byte loads, 8-byte
+// stores; a pair past the row is skipped), and writes the float32 interior
+// of buffer X; together the blocks write every interior element once.
 static void check_widen12(int H, int W, int H2, int W2, const WtBuf X, int lim) {
   std::vector<int> cnt(lim, 0);
+  const int vec = W % 4 == 0 ? 4 : 2;
+  CHECK(W % 2 == 0 && X.pcol % vec == 0 && X.stride % vec == 0 && X.off % vec == 0 && (H * W) % vec == 0, "widen12 alignment");
   for (int P = 0; P < H2; ++P) for (int Q = 0; Q < W2; ++Q) {
     CHECK(4 * Q < W, "block's first column inside the plane");
     for (int a = 0; a < 4; ++a) {
       const int i = 4 * P + a;
       if (i >= H) continue;
-      CHECK((i * W + 4 * Q) % 4 == 0 && (H * W) % 4 == 0 && (X.off + (i + X.prow) * X.stride + 4 * Q + X.pcol) % 4 == 0,
-            "widen12 vector alignment");
-      for (int e = 0; e < 4; ++e) {
-        const int j = 4 * Q + e;
-        CHECK(j < W, "widen12 vector beyond the row");
-        CHECK(i * W + j < H * W, "widen12 staging read");
-        acc_buf(X, 1, 0, i + X.prow, j + X.pcol, lim, "widen12 write");
-        const long k = X.off + (long)(i + X.prow) * X.stride + j + X.pcol;
-        if (k >= 0 && k < lim) cnt[k]++;
+      for (int e0 = 0; e0 < 4; e0 += vec) {
+        if (4 * Q + e0 >= W) { CHECK(vec == 2, "widen12 vector beyond the row"); continue; }
+        CHECK((i * W + 4 * Q + e0) % vec == 0 && (X.off + (i + X.prow) * X.stride + 4 * Q + e0 + X.pcol) % vec == 0,
+              "widen12 vector alignment");
+        for (int e = e0; e < e0 + vec; ++e) {
+          const int j = 4 * Q + e;
+          CHECK(j < W, "widen12 element beyond the row");
+          CHECK(i * W + j < H * W, "widen12 staging read");
+          acc_buf(X, 1, 0, i + X.prow, j + X.pcol, lim, "widen12 write");
+          const long k = X.off + (long)(i + X.prow) * X.stride + j + X.pcol;
+          if (k >= 0 && k < lim) cnt[k]++;
+        }
       }
     }
   }
@@ -129,7 +135,7 @@ static void check_fwd(int N, int C, int H, int W, int L, int K) {
       if (pl.wd_vec == 2) CHECK(W % 2 == 0 && pl.lev[0].pcol % 2 == 0 && pl.lev[0].stride % 2 == 0 && XF % 2 == 0, "widen pair alignment");
       CHECK(pl.wd_vec == (W % 4 == 0 ? 4 : W % 2 == 0 ? 2 : 1), "widen item width");
       for (int g = 0; g < pl.P; ++g) CHECK(((long)g * H * W * 2) % (pl.use_bulk == 1 ? 16 : 8) == 0, "staging plane alignment");
-      if (L >= 2 && W % 4 == 0) check_widen12(H, W, pl.Hs[2], pl.Ws[2], pl.lev[0], XF);
+      if (L >= 2 && W % 2 == 0) check_widen12(H, W, pl.Hs[2], pl.Ws[2], pl.lev[0], XF);
     }
   }
   std::vector<char> written(PF, 0), xwritten(XF, 0);  // interior writes, to check margins stay zero
