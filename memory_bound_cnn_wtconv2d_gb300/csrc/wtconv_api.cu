@@ -693,7 +693,18 @@ wtconv_status_t plan_bw_compute(const wtconv_desc_t* d, WtBwPlan& pl) {
     bw_layout(pl, 1, staging);
     if (pl.smem_bytes > kMaxSmemPerBlock) bw_layout(pl, 1, false);
   }
-  const int per_sm = per_sm_of(pl);
+  int per_sm = per_sm_of(pl);
+  // float32: one input set instead of two where that fits more CTAs per SM
+  // (the next unit's boxes then follow the unit, prefetched into L2 first).
+  if (d->dtype == WTCONV_F32 && pl.nsets == 2) {
+    WtBwPlan one = pl;
+    bw_layout(one, 1, false);
+    const int per_sm1 = per_sm_of(one);
+    if (per_sm1 > per_sm) {
+      pl = one;
+      per_sm = per_sm1;
+    }
+  }
   // Persistent grid: every resident CTA slot, at most one CTA per unit.
   pl.batches = d->N > 0 ? ceil_div(d->N, P) : 0;
   return bw_grid(d, pl, per_sm);
