@@ -27,10 +27,34 @@
 #include <string>
 #include <vector>
 
-// The launch functions, replaced: planning only.  The occupancy queries the
-// planner makes answer from shared memory alone (no device to ask), capped as
-// the registers of each kernel cap them on the GPU.
+// The launch functions, replaced: planning only.  The register and
+// occupancy queries the planner makes answer from tables of each kernel
+// instance's registers per thread (ptxas -v of the sources for sm_103a) and
+// from shared memory, as the device would, so that the plans replayed here
+// are the ones a GB300 runs (a kernel change that alters its registers
+// changes these tables too).  Index: (k - 3) / 2, then 0 float32 / 1 16-bit.
 namespace wt {
+static const int kFwdRegs[4] = {96, 128, 168, 168};
+static const int kBwRegs[4][2][3] = {  // bw_kernel <TR 4, MI 1>, <TR 4, MI 2>, <TR 8, MI 1>
+    {{76, 80, 76}, {70, 104, 70}},
+    {{80, 128, 80}, {80, 128, 80}},
+    {{111, 232, 128}, {128, 232, 128}},
+    {{200, 232, 208}, {198, 234, 208}}};
+static const int kBwWinRegs[4][2][2] = {  // bw_win_kernel TR 4, TR 8
+    {{64, 62}, {64, 64}},
+    {{128, 80}, {128, 80}},
+    {{228, 128}, {228, 128}},
+    {{236, 212}, {242, 220}}};
+static const int kBwfRegs[4][2] = {{64, 96}, {110, 124}, {194, 128}, {255, 236}};  // bwf_kernel (TR 8)
+// CTAs of 256 threads per SM: 228 KB of shared memory (1 KB reserved per
+// CTA), 64 K registers allocated per warp in steps of 8 per thread.
+static int occ256(int regs, int smem) {
+  const int by_smem = 233472 / (smem + 16 + 1024);
+  const int by_regs = 65536 / (256 * ((regs + 7) / 8 * 8));
+  return by_smem < by_regs ? by_smem : by_regs;
+}
+static int ki(int k) { return (k - 3) / 2; }
+static int di(int dtype) { return dtype == 0 ? 0 : 1; }
 cudaError_t launch_fwd(const WtFwdPlan&, const CUtensorMap&, int, bool, const void*, const float*, const float*, const float*,
                        const float*, const float*, void*, cudaStream_t) { return cudaSuccess; }
 cudaError_t launch_bwd_weight(const WtBwPlan&, const CUtensorMap&, const CUtensorMap&, int, const void*, const void*, const float*, const float*,
@@ -42,16 +66,23 @@ cudaError_t launch_fwd_win(const WtFwdPlan&, const CUtensorMap&, int, bool, cons
 unsigned int take_win_faults() { return 0; }
 cudaError_t launch_bwd_weight_win(const WtBwPlan&, const CUtensorMap&, const CUtensorMap&, int, const void*, const void*, const float*, const float*,
                                   const float*, const float*, const float*, float*, float*, float*, float*, float*, float*, cudaStream_t) { return cudaSuccess; }
-int bw_win_ctas_per_sm(const WtBwPlan& pl, int) { int n = (int)(233472 / (pl.smem_bytes + 1024)); return n > 2 ? 2 : n; }
+int bw_win_ctas_per_sm(const WtBwPlan& pl, int dtype) {
+  return occ256(kBwWinRegs[ki(pl.K)][di(dtype)][pl.tbr == 8 ? 1 : 0], pl.smem_bytes);
+}
 unsigned int take_bww_faults() { return 0; }
-int bw_win_regs(int, int, int) { return 0; }
-int fwd_regs(int, int dtype) { return dtype == 0 ? 144 : 128; }  // the k = 5 kernels' registers
+int bw_win_regs(int k, int tbr, int dtype) { return kBwWinRegs[ki(k)][di(dtype)][tbr == 8 ? 1 : 0]; }
+int fwd_regs(int k, int) { return kFwdRegs[ki(k)]; }
 cudaError_t launch_bwd_fused(const WtBwPlan&, const WtFwdPlan&, const CUtensorMap&, const CUtensorMap&, int, const void*, const void*, const float*, const float*,
                              const float*, const float*, const float*, void*, float*, float*, float*, float*, float*, float*, cudaStream_t) { return cudaSuccess; }
-int bwf_ctas_per_sm(const WtBwPlan& pl, const WtFwdPlan&, int) { int n = (int)(233472 / (pl.smem_bytes + 1024)); return n > 2 ? 2 : n; }
+int bwf_ctas_per_sm(const WtBwPlan& pl, const WtFwdPlan& fp, int dtype) {
+  if (fp.ftp != WT_TP / 2 || pl.tbr != 8) return 0;  // no instance for other tiles
+  return occ256(kBwfRegs[ki(pl.K)][di(dtype)], pl.smem_bytes);
+}
 unsigned int take_bwf_faults() { return 0; }
-int bw_regs(int k, int mi, int) { return mi == 1 ? (k <= 5 ? 80 : 128) : (k <= 5 ? 128 : 232); }  // as the f32 kernels
-int bw_ctas_per_sm(const WtBwPlan& pl, int) { return (int)(233472 / (pl.smem_bytes + 1024)) > 3 ? 3 : (int)(233472 / (pl.smem_bytes + 1024)); }
+int bw_regs(int k, int mi, int dtype) { return kBwRegs[ki(k)][di(dtype)][mi == 1 ? 0 : 1]; }  // (the TR 4 instances)
+int bw_ctas_per_sm(const WtBwPlan& pl, int dtype) {
+  return occ256(kBwRegs[ki(pl.K)][di(dtype)][pl.tbr == 8 ? 2 : pl.mi == 1 ? 0 : 1], pl.smem_bytes);
+}
 unsigned int take_bw_faults() { return 0; }
 cudaError_t launch_lowpass(int, const void*, float*, long long, int, int, int, cudaStream_t) { return cudaSuccess; }
 cudaError_t launch_add_carry(int, void*, const float*, long long, int, int, int, cudaStream_t) { return cudaSuccess; }
